@@ -1,0 +1,177 @@
+"""Seeded synthetic inputs for the quantized MoE layer.
+
+This module draws random numbers and nothing else: it holds none of the layer's
+arithmetic (no quantisation, routing or matmul).  Both the CUDA path and the
+oracle take their inputs from here.  Every draw comes from numpy's PCG64 seeded
+by a ``SeedSequence`` of (config seed, tensor id, index), so any tensor can be
+regenerated alone, in any order, on any thread.
+
+Workloads (GLM-5.2-shaped MoE layer: 256 routed experts, top-8, one shared
+expert, SwiGLU experts, hidden 6144, expert FFN 2048):
+
+* ``tiny``      hidden 256, FFN 128, 8 experts top-2, 4 tokens, seed 0
+* ``decode``    the GLM-5.2 shape, 1 token per forward, seed 1
+* ``verify``    the GLM-5.2 shape, 4 correlated tokens per forward
+                (x_t = 0.7 x_0 + 0.3 N(0,1)), seed 2
+* ``prefill``   the GLM-5.2 shape, 2048 tokens with per-token norm jitter
+                U(0.5, 2) and a Zipf-skewed router bias, seed 3
+* ``sweep``     8 stacked GLM-5.2-shaped layers (seeds 100..107), batches
+                1, 8, 32, 128, Zipf-skewed bias, router rows of layer l drawn
+                correlated with layer l-1's
+
+Distributions: router weights N(0, 0.02), router bias N(0, 0.01), expert
+weights N(0, 0.02) (F32, before the int4 container's quantiser), activations
+N(0, 1).
+"""
+from __future__ import annotations
+
+import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+# tensor ids inside one seed's stream family
+_T_ROUTER_W = 1
+_T_ROUTER_B = 2
+_T_EXPERT = 3
+_T_X = 4
+_T_X_NOISE = 5
+_T_JITTER = 6
+_T_ZIPF_PERM = 7
+_T_ROUTER_W_FRESH = 8
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    hidden: int
+    ffn: int
+    n_experts: int
+    top_k: int
+    n_tok: int
+    seed: int
+    routed_scale: float = 2.5
+    correlated_tokens: bool = False      # verify: x_t = 0.7 x_0 + 0.3 N(0,1)
+    norm_jitter: bool = False            # prefill: per-token factor U(0.5, 2)
+    zipf_beta: float = 0.0               # Zipf-skewed bias amplitude (0 = none)
+    zipf_s: float = 1.1
+    layers: int = 1
+    layer_corr: float = 0.0              # sweep: router rows correlated across layers
+    batches: tuple = ()
+
+    @property
+    def expert_bytes(self) -> int:
+        """Packed int4 bytes of one expert (gate, up, down)."""
+        return 3 * self.ffn * self.hidden // 2
+
+    @property
+    def expert_scales(self) -> int:
+        return 2 * self.ffn + self.hidden
+
+    def layer_seed(self, layer: int) -> int:
+        return self.seed + layer
+
+
+# Zipf amplitude of the prefill and sweep router bias, chosen so that on 2048
+# tokens the busiest expert receives a few hundred tokens while the quietest
+# receive ~0 ("per-expert token counts from ~0 to several hundred").
+ZIPF_BETA = 0.05
+# Correlation of a sweep layer's router rows with the previous layer's.
+SWEEP_LAYER_CORR = 0.8
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 256, 128, 8, 2, 4, 0),
+    "decode": Workload("decode", 6144, 2048, 256, 8, 1, 1),
+    "verify": Workload("verify", 6144, 2048, 256, 8, 4, 2, correlated_tokens=True),
+    "prefill": Workload("prefill", 6144, 2048, 256, 8, 2048, 3, norm_jitter=True,
+                        zipf_beta=ZIPF_BETA),
+    "sweep": Workload("sweep", 6144, 2048, 256, 8, 128, 100, zipf_beta=ZIPF_BETA, layers=8,
+                      layer_corr=SWEEP_LAYER_CORR, batches=(1, 8, 32, 128)),
+}
+
+
+def rng(*key: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(k) for k in key])))
+
+
+def normal(shape, std: float, *key: int) -> np.ndarray:
+    """N(0, std^2) F32 draws by the Box-Muller transform of PCG64 uniforms
+    (G. E. P. Box, M. E. Muller, 1958), in float32 throughout."""
+    n = int(np.prod(shape))
+    m = (n + 1) // 2
+    g = rng(*key)
+    u = g.random(m, dtype=np.float32)
+    v = g.random(m, dtype=np.float32)
+    np.subtract(np.float32(1.0), u, out=u)          # (0, 1]: log is finite
+    np.log(u, out=u)
+    np.multiply(u, np.float32(-2.0), out=u)
+    np.sqrt(u, out=u)                               # radius
+    np.multiply(v, np.float32(2.0 * np.pi), out=v)  # angle
+    out = np.empty(2 * m, np.float32)
+    np.cos(v, out=out[:m])                          # first half: r cos(theta)
+    np.sin(v, out=out[m:])                          # second half: r sin(theta)
+    out[:m] *= u
+    out[m:] *= u
+    a = out[:n].reshape(shape)
+    if std != 1.0:
+        a *= np.float32(std)
+    return a
+
+
+def router(wl: Workload, layer: int = 0):
+    """Router weights [E][H] and bias [E] (F32) of one layer."""
+    s = wl.layer_seed(layer)
+    W = normal((wl.n_experts, wl.hidden), 0.02, s, _T_ROUTER_W)
+    if wl.layer_corr and layer > 0:
+        a = np.float32(wl.layer_corr)
+        prev, _ = router(wl, layer - 1)
+        fresh = normal((wl.n_experts, wl.hidden), 0.02, s, _T_ROUTER_W_FRESH)
+        W = a * prev + np.float32(np.sqrt(1.0 - float(a) ** 2)) * fresh
+        W = W.astype(np.float32)
+    b = normal((wl.n_experts,), 0.01, s, _T_ROUTER_B)
+    if wl.zipf_beta:
+        perm = rng(s, _T_ZIPF_PERM).permutation(wl.n_experts)
+        rank = np.empty(wl.n_experts, np.int64)
+        rank[perm] = np.arange(wl.n_experts)
+        b = (b + np.float32(wl.zipf_beta) * ((rank + 1.0) ** -wl.zipf_s).astype(np.float32))
+        b = b.astype(np.float32)
+    return W, b
+
+
+def expert_f32(wl: Workload, e: int, layer: int = 0):
+    """F32 weights of expert ``e`` (``e == n_experts`` is the shared expert):
+    gate [F][H], up [F][H], down [H][F]."""
+    s = wl.layer_seed(layer)
+    F, H = wl.ffn, wl.hidden
+    a = normal((3 * F * H,), 0.02, s, _T_EXPERT, e)
+    return a[: F * H].reshape(F, H), a[F * H: 2 * F * H].reshape(F, H), a[2 * F * H:].reshape(H, F)
+
+
+def expert_f32_rows(wl: Workload, e: int, layer: int = 0) -> np.ndarray:
+    """Same draw as :func:`expert_f32`, as one [2F+H] list of rows in container
+    order (gate rows, up rows, down rows); rows are ragged (H or F long), so this
+    returns the flat F32 buffer."""
+    s = wl.layer_seed(layer)
+    return normal((3 * wl.ffn * wl.hidden,), 0.02, s, _T_EXPERT, e)
+
+
+def activations(wl: Workload, step: int, n_tok: int | None = None, layer: int = 0) -> np.ndarray:
+    """Input activations [T][H] (F32) of forward number ``step``."""
+    T = wl.n_tok if n_tok is None else n_tok
+    s = wl.layer_seed(layer)
+    x = normal((T, wl.hidden), 1.0, s, _T_X, step)
+    if wl.correlated_tokens:
+        noise = normal((T, wl.hidden), 1.0, s, _T_X_NOISE, step)
+        x = (np.float32(0.7) * x[0:1] + np.float32(0.3) * noise).astype(np.float32)
+    if wl.norm_jitter:
+        j = rng(s, _T_JITTER, step).uniform(0.5, 2.0, size=(T, 1)).astype(np.float32)
+        x = (x * j).astype(np.float32)
+    return x
+
+
+def parallel_map(fn, items, workers: int | None = None):
+    """Map over items on a thread pool (numpy releases the GIL while drawing)."""
+    workers = workers or min(16, os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, items))
