@@ -1,0 +1,306 @@
+"""Benchmark of the GB300 quantized MoE layer.
+
+Default workload: the GLM-5.2-shaped decode layer (hidden 6144, expert FFN
+2048, 256 routed experts top-8 + 1 shared expert, int4 experts all resident in
+HBM), one token per forward, fresh N(0,1) activations every forward.  One
+"step" is one full layer forward (quantise, route, dispatch, gate/up, down,
+combine).  L2 is flushed (a 512 MiB write) between timed steps, outside the
+timed region, so the shared expert and router weights are re-read from HBM
+like in a real multi-layer decode.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|verify|prefill]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer tok/s"
+EXPERT_BYTES_PER = None  # filled per workload: int4 bytes + row scales of one expert
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1910.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def expert_bytes(wl):
+    return wl.expert_bytes + 4 * wl.expert_scales
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"coli_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000):
+    """Time the CPU oracle on a bounded sample of the workload (forwards of the
+    same shape); returns (tok/s, threads, sample description)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from helpers import OracleLayer
+    oracle.build()
+    ref = OracleLayer(wl)
+    xs = [synth.activations(wl, seed_base + i) for i in range(n_forwards)]
+    # pack the experts the sample touches before timing (the oracle's converter)
+    for x in xs:
+        idx, _ = oracle.route(x, ref.W, ref.b, wl.top_k, wl.routed_scale)
+        for e in set(int(v) for v in idx.ravel()):
+            ref.expert(e)
+    t0 = time.perf_counter()
+    for x in xs:
+        ref.forward(x)
+    dt = time.perf_counter() - t0
+    toks = n_forwards * xs[0].shape[0]
+    return toks / dt, oracle.num_threads(), f"{n_forwards} forwards x {xs[0].shape[0]} tokens of the {wl.name} workload ({dt:.1f} s)"
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle (plain C, OpenMP over independent outputs)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    n = max(1, args.steps if args.steps <= 50 else 20)
+    for _ in range(min(args.warmup, 1)):
+        oracle_baseline(wl, 1, seed_base=800000)
+    tps, cores, sample = oracle_baseline(wl, n)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tok/s", "n_gpus": args.gpus,
+        "steps": n, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.n_tok / tps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tps, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    return {"workload": f"{wl.name}: GLM-5.2-shaped MoE layer, hidden {wl.hidden}, expert FFN {wl.ffn}, "
+                        f"{wl.n_experts} routed experts top-{wl.top_k} + 1 shared, {wl.n_tok} token(s) per forward",
+            "hidden": wl.hidden, "ffn": wl.ffn, "n_experts": wl.n_experts, "top_k": wl.top_k,
+            "tokens_per_forward": wl.n_tok, "weights": "int4 + F32 row scales, all experts resident in HBM",
+            "l2": "flushed between timed steps (512 MiB write, outside the timed region)"}
+
+
+def run(args):
+    import torch
+    import torch.distributed as dist
+
+    from int4_routed_expert_f32_gb300 import _build
+    _build.build()
+    import int4_routed_expert_f32_gb300 as coli
+    from synth.device import build_device_layer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    wl = synth.WORKLOADS[args.workload]
+    T = wl.n_tok
+    coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
+    t_build = time.perf_counter()
+    L = build_device_layer(wl)
+    W, b = synth.router(wl)
+    L["router_b"] = torch.from_numpy(b).cuda()
+    t_build = time.perf_counter() - t_build
+    n_total = args.warmup + args.steps
+    xs = torch.from_numpy(np.stack([synth.activations(wl, 10_000 + rank * 100_000 + i)
+                                    for i in range(n_total)])).cuda()
+    out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+
+    # union of routed experts per step (bookkeeping for weight bytes; not timed)
+    unions = []
+    for i in range(n_total):
+        idx, _ = coli.dbg_route(xs[i], L["router_w"], L["router_b"], wl.top_k)
+        unions.append(len(set(idx.cpu().numpy().ravel().tolist())))
+    torch.cuda.synchronize()
+
+    def fwd(i):
+        coli.layer_forward(xs[i], L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                           L["shared_w4"], L["shared_rs"], out=out)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        fwd(i)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    coli.timing_read()
+    coli.timing_enable(True)
+    coli.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(st)
+            fwd(args.warmup + s)
+            ev[s][1].record(st)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = coli.launch_count()
+    coli.timing_enable(False)
+    k_ms, k_n = coli.timing_read()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = coli.get_device_status()
+
+    # end to end through the host-I/O entry point: pinned host x in, host out
+    xh = torch.from_numpy(np.stack([synth.activations(wl, 20_000 + i) for i in range(args.steps)]))
+    xh = xh.pin_memory()
+    oh = torch.empty((T, wl.hidden), dtype=torch.float32).pin_memory()
+    for i in range(min(args.warmup, 5)):
+        coli.layer_forward_hostio(xh[i], L["router_w"], L["router_b"], L["expert_w4"],
+                                  L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
+    e2e_s = 0.0
+    for s in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        coli.layer_forward_hostio(xh[s], L["router_w"], L["router_b"], L["expert_w4"],
+                                  L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
+        e2e_s += time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    hbm_peak, _, peak_kind = peaks()
+    ub = np.array(unions[args.warmup:], dtype=np.float64)
+    bytes_per_fwd = float(np.mean((ub + 1) * expert_bytes(wl)))
+    k_avg_ms = k_ms / max(k_n, 1)
+    achieved = bytes_per_fwd / (k_avg_ms * 1e-3) / 1e9
+    value = world * args.steps * T / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32", "data": "synthetic",
+        "config": workload_config(wl),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "kernel": "expert gate/up + down (k_gateup_gemv, k_down_gemv)",
+                     "algorithmic_bytes_per_launch": bytes_per_fwd,
+                     "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} hbm_gbs"},
+        "weight_gbs_layer": bytes_per_fwd / (total_ms / args.steps * 1e-3) / 1e9,
+        "e2e": {"value": world * args.steps * T / e2e_s, "unit": "tok/s",
+                "h2d_bytes_per_step": T * wl.hidden * 4, "d2h_bytes_per_step": T * wl.hidden * 4},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "device_status": status,
+        "setup_s": round(t_build, 1),
+        "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, cores, sample = oracle_baseline(wl, args.cpu_forwards)
+        line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="decode", choices=["decode", "verify", "prefill"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-forwards", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run(args)
+
+
+if __name__ == "__main__":
+    main()

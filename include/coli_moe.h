@@ -1,0 +1,193 @@
+/*
+ * coli_moe.h -- C ABI of the GB300 (sm_103a) quantized MoE feed-forward layer.
+ *
+ * The layer (a GLM-5.2-class MoE FFN as the colibri pages describe it):
+ *   - a DeepSeek-V3-style F32 sigmoid router over E routed experts picks top-k
+ *     experts per token ("Open-source engine that ran 744B GLM-5.2 on a
+ *     25GB-RAM laptop" (jeff.news), section "Attention and kernels"; router in
+ *     F32: "GLM-5.2-colibri-int4" model card, section "Good to know");
+ *   - one shared expert runs on every token (same section);
+ *   - each expert is a SwiGLU FFN whose weights are packed int4 nibbles, two
+ *     per byte, with a per-row F32 scale (model card, "Technical features");
+ *   - activations are quantized Q8_0-style (blocks of 32, int8 codes, one F32
+ *     scale, lrintf rounding) and every matmul is an integer dot product
+ *     accumulated in int32 per block, then scaled in float ("colibri: a pure-C
+ *     inference engine ..." (discuss.pytorch.kr), section "Key features").
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers owned by the caller (except the
+ *     *_host arguments of coli_moe_layer_forward_hostio).  The library never
+ *     frees or retains them beyond the call's GPU work.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued asynchronously; no entry point synchronises the host
+ *     unless it says so.
+ *   - Row-major, contiguous layouts.  Int4 matrices [N][K] are N*K/2 bytes:
+ *     byte j of a row holds element 2j in its low nibble and element 2j+1 in its
+ *     high nibble, each stored as code + 8 (codes -7..7; a nibble of 0 decodes
+ *     to -8 and is accepted).
+ *   - One expert is gate [F][H], up [F][H], down [H][F] back to back
+ *     (3*F*H/2 bytes); its row scales are [gate F | up F | down H] F32.
+ *     expert_w4 is [E][3*F*H/2], expert_rowscale is [E][2F+H]; the shared
+ *     expert has the same layout without the E dimension.
+ *   - Return value: COLI_OK or a negative coli_status.  Argument errors are
+ *     reported before anything is launched.  A launch failure returns
+ *     COLI_E_CUDA after clearing the CUDA error state.  Device-side problems
+ *     (an expert index out of range, a bounded wait that gave up) set a device
+ *     status word that coli_moe_get_device_status() reads.
+ *   - Not thread-safe: one host thread drives the library at a time.
+ */
+#ifndef COLI_MOE_H
+#define COLI_MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    COLI_OK = 0,
+    COLI_E_INVAL = -1,     /* bad argument: NULL, misaligned, out of range   */
+    COLI_E_NOSHAPE = -2,   /* coli_moe_configure() has not succeeded yet      */
+    COLI_E_NOMEM = -3,     /* workspace allocation failed                     */
+    COLI_E_CUDA = -4,      /* a CUDA call or launch failed                    */
+    COLI_E_TIMEOUT = -5,   /* a bounded device-side wait gave up              */
+    COLI_E_UNIMPL = -6,    /* requested path or shape not implemented         */
+    COLI_E_DEVICE = -7     /* device status word reports a bad index          */
+} coli_status;
+
+/* Layer shape.  Limits: hidden % 128 == 0, ffn % 128 == 0, 1 <= top_k <= 16,
+ * top_k <= n_experts <= 256, 1 <= max_tok <= 65536, routed_scale finite > 0. */
+typedef struct {
+    int hidden;          /* H: model width                                     */
+    int ffn;             /* F: expert FFN width                                */
+    int n_experts;       /* E: routed experts                                  */
+    int top_k;           /* k: experts per token                               */
+    float routed_scale;  /* multiplier of the renormalised routed weights      */
+    int max_tok;         /* largest n_tok any later call will pass             */
+} coli_moe_shape;
+
+/* Execution path of the expert matmuls. */
+typedef enum {
+    COLI_PATH_AUTO = 0,  /* per-expert choice by tokens routed to the expert   */
+    COLI_PATH_GEMV = 1,  /* streaming int4 x int8 dp4a kernels for every expert */
+    COLI_PATH_GEMM = 2   /* tensor-core grouped GEMM for every routed expert    */
+} coli_path;
+
+/* Validate `s`, remember it and allocate the library-owned workspace for up to
+ * s->max_tok tokens on the current CUDA device (replacing an earlier one).
+ * Returns COLI_E_INVAL for a shape outside the limits, COLI_E_NOMEM if the
+ * workspace cannot be allocated.  Synchronises the device. */
+int coli_moe_configure(const coli_moe_shape *s);
+
+/* One MoE layer forward on n_tok tokens (0 <= n_tok <= max_tok; 0 is a no-op).
+ *   x               [n_tok][H] F32 input activations (16-byte aligned)
+ *   router_w        [E][H] F32, router_bias [E] F32
+ *   expert_w4       [E][3FH/2] packed int4 (16-byte aligned)
+ *   expert_rowscale [E][2F+H] F32
+ *   shared_w4       [3FH/2] packed int4 (16-byte aligned)
+ *   shared_rowscale [2F+H] F32
+ *   out             [n_tok][H] F32 output: shared expert + sum over the top-k of
+ *                   w_r * expert_r(x), w_r = sigma_r / sum(sigma_sel) * routed_scale.
+ * Steps, all on `stream`: Q8_0-quantise x; route (logits in a fixed F32
+ * order, sigmoid, +bias for selection, top-k, renormalise); build the stable
+ * token->expert permutation; gate/up with SiLU*up and Q8_0 requantisation;
+ * down; gate-weighted combine.  Asynchronous; `out` may not alias `x`. */
+int coli_moe_layer_forward(const float *x, int n_tok,
+                           const float *router_w, const float *router_bias,
+                           const uint8_t *expert_w4, const float *expert_rowscale,
+                           const uint8_t *shared_w4, const float *shared_rowscale,
+                           float *out, void *stream);
+
+/* The same forward with x and out in HOST memory (pinned memory gives
+ * asynchronous copies).  Copies x into a library-owned device buffer, runs the
+ * forward, copies the result back, and synchronises `stream` before
+ * returning, so out_host is valid on return.  Weights are device pointers. */
+int coli_moe_layer_forward_hostio(const float *x_host, int n_tok,
+                                  const float *router_w, const float *router_bias,
+                                  const uint8_t *expert_w4, const float *expert_rowscale,
+                                  const uint8_t *shared_w4, const float *shared_rowscale,
+                                  float *out_host, void *stream);
+
+/* Choose the expert-matmul path for later forwards (default COLI_PATH_AUTO).
+ * `gemm_min_tokens`: with COLI_PATH_AUTO, an expert receiving at least this many
+ * tokens uses the grouped GEMM (<= 0 keeps the built-in threshold). */
+int coli_moe_set_path(int path, int gemm_min_tokens);
+
+/* Synchronise `stream`, then read and clear the device status word.
+ * Returns COLI_OK, COLI_E_DEVICE (bad expert index seen), COLI_E_TIMEOUT
+ * (a bounded device wait gave up) or COLI_E_CUDA. */
+int coli_moe_get_device_status(void *stream);
+
+/* Static, human-readable text for a status code. */
+const char *coli_moe_strerror(int code);
+
+/* Free the workspace and forget the shape.  Synchronises the device. */
+void coli_moe_release(void);
+
+/* Converter: quantise F32 weight rows to the int4 container, on the GPU.
+ *   w [rows][K] F32 (K % 32 == 0) -> packed [rows][K/2], scale [rows] F32,
+ * s = max|row| / 7 (IEEE divide), q = clamp(lrintf(w / s), -7, 7), nibble q+8,
+ * low nibble first; an all-zero row gives s = 0 and codes 0 (model card
+ * "GLM-5.2-colibri-int4", sections "TL;DR" and "Technical features").
+ * Independent of coli_moe_configure(). */
+int coli_moe_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *scale,
+                       void *stream);
+
+/* Kernel timing for measurement: when enabled, the library records CUDA events
+ * around its dominant kernel (the expert gate/up + down matmuls) on the
+ * forward's stream.  coli_moe_timing_read() synchronises, returns the summed
+ * elapsed milliseconds and the number of timed launches, and resets them. */
+int coli_moe_timing_enable(int on);
+int coli_moe_timing_read(double *ms_total, int *n_timed);
+
+/* Number of kernels the library launched since the last call (then reset). */
+long long coli_moe_launch_count(void);
+
+/* ---- stage entry points (tests; same conventions, configured shape) ------- */
+
+/* Q8_0 of n floats (n % 32 == 0): q [n] int8, d [n/32] F32 (same rule as the
+ * forward's activation quantiser).  Independent of coli_moe_configure(). */
+int coli_moe_dbg_quantize(const float *x, int n, int8_t *q, float *d, void *stream);
+
+/* Router only: idx [n_tok][k] int32 (rank order), w [n_tok][k] F32;
+ * optional logits [n_tok][E] F32 (NULL to skip). */
+int coli_moe_dbg_route(const float *x, int n_tok, const float *router_w,
+                       const float *router_bias, int32_t *idx, float *w, float *logits,
+                       void *stream);
+
+/* Dispatch only: from idx [n_tok][k] (values < E) produce counts [E],
+ * offsets [E+1], perm [n_tok*k] (perm[pos] = pair t*k+r), inv [n_tok*k]. */
+int coli_moe_dbg_dispatch(const int32_t *idx, int n_tok, int32_t *counts, int32_t *offsets,
+                          int32_t *perm, int32_t *inv, void *stream);
+
+/* Per-block int32 dot products of `rows` packed int4 rows of length K
+ * (K % 32 == 0) with one int8 vector q [K]: I_out [rows][K/32]. */
+int coli_moe_dbg_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q,
+                            int32_t *I_out, void *stream);
+
+/* Run a full forward and copy out its intermediates (any pointer may be NULL):
+ * qx [n_tok][H] int8, dx [n_tok][H/32], idx/w [n_tok][k],
+ * qh [n_tok*k + n_tok][F] int8 and dh [n_tok*k + n_tok][F/32] in pair order
+ * (pair t*k+r, then the shared expert's rows t = 0..n_tok-1),
+ * y [n_tok*k + n_tok][H] F32 per pair in the same order. */
+int coli_moe_dbg_forward_intermediates(const float *x, int n_tok,
+                                       const float *router_w, const float *router_bias,
+                                       const uint8_t *expert_w4, const float *expert_rowscale,
+                                       const uint8_t *shared_w4, const float *shared_rowscale,
+                                       float *out, int8_t *qx, float *dx, int32_t *idx,
+                                       float *w, int8_t *qh, float *dh, float *y,
+                                       void *stream);
+
+/* Gate/up + SiLU*up + Q8_0 of h for one expert on given quantized activations
+ * (stage-isolated): qx [n][H] int8, dx [n][H/32] -> h [n][F] F32 (before
+ * requantisation), qh [n][F] int8, dh [n][F/32].  1 <= n <= max_tok. */
+int coli_moe_dbg_expert_hidden(const uint8_t *ew4, const float *ers, const int8_t *qx,
+                               const float *dx, int n, float *h, int8_t *qh, float *dh,
+                               void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COLI_MOE_H */

@@ -1,0 +1,252 @@
+"""Python binding of the GB300 quantized MoE layer (``libcoli_moe.so``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  The functions carry the C ABI's names without the ``coli_moe_``
+prefix (``include/coli_moe.h`` documents each one).  Tensors are
+``torch.Tensor`` objects on the current CUDA device; PyTorch provides the
+device memory and the stream, nothing else.
+
+Importing this package raises if the shared library is missing: there is no
+CPU or PyTorch fallback for any step.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcoli_moe.so")
+
+OK, E_INVAL, E_NOSHAPE, E_NOMEM, E_CUDA, E_TIMEOUT, E_UNIMPL, E_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
+PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
+
+EXPORTS = (
+    "coli_moe_configure", "coli_moe_layer_forward", "coli_moe_layer_forward_hostio",
+    "coli_moe_set_path", "coli_moe_get_device_status", "coli_moe_strerror", "coli_moe_release",
+    "coli_moe_pack_int4", "coli_moe_timing_enable", "coli_moe_timing_read",
+    "coli_moe_launch_count", "coli_moe_dbg_quantize", "coli_moe_dbg_route",
+    "coli_moe_dbg_dispatch", "coli_moe_dbg_block_dots", "coli_moe_dbg_forward_intermediates",
+    "coli_moe_dbg_expert_hidden",
+)
+
+
+class ColiError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {_lib.coli_moe_strerror(code).decode()} ({code})")
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("ffn", ctypes.c_int), ("n_experts", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("routed_scale", ctypes.c_float),
+                ("max_tok", ctypes.c_int)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(there is no fallback path)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sig = {
+        "coli_moe_configure": ([ctypes.POINTER(_Shape)], i),
+        "coli_moe_layer_forward": ([P, i, P, P, P, P, P, P, P, P], i),
+        "coli_moe_layer_forward_hostio": ([P, i, P, P, P, P, P, P, P, P], i),
+        "coli_moe_set_path": ([i, i], i),
+        "coli_moe_get_device_status": ([P], i),
+        "coli_moe_strerror": ([i], ctypes.c_char_p),
+        "coli_moe_release": ([], None),
+        "coli_moe_pack_int4": ([P, i, i, P, P, P], i),
+        "coli_moe_timing_enable": ([i], i),
+        "coli_moe_timing_read": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)], i),
+        "coli_moe_launch_count": ([], ctypes.c_longlong),
+        "coli_moe_dbg_quantize": ([P, i, P, P, P], i),
+        "coli_moe_dbg_route": ([P, i, P, P, P, P, P, P], i),
+        "coli_moe_dbg_dispatch": ([P, i, P, P, P, P, P], i),
+        "coli_moe_dbg_block_dots": ([P, i, i, P, P, P], i),
+        "coli_moe_dbg_forward_intermediates": ([P, i, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P], i),
+        "coli_moe_dbg_expert_hidden": ([P, P, P, P, i, P, P, P, P], i),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t):
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous host tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise ColiError(code, what)
+
+
+# --------------------------------------------------------------------------- #
+def configure(hidden: int, ffn: int, n_experts: int, top_k: int, routed_scale: float, max_tok: int):
+    s = _Shape(hidden, ffn, n_experts, top_k, routed_scale, max_tok)
+    _check(_lib.coli_moe_configure(ctypes.byref(s)), "configure")
+
+
+def release():
+    _lib.coli_moe_release()
+
+
+def set_path(path: int, gemm_min_tokens: int = 0):
+    _check(_lib.coli_moe_set_path(path, gemm_min_tokens), "set_path")
+
+
+def layer_forward(x, router_w, router_bias, expert_w4, expert_rowscale, shared_w4, shared_rowscale,
+                  out=None, stream=None):
+    if out is None:
+        out = torch.empty_like(x)
+    n_tok = x.shape[0] if x.dim() == 2 else 0
+    _check(_lib.coli_moe_layer_forward(_ptr(x), n_tok, _ptr(router_w), _ptr(router_bias),
+                                       _ptr(expert_w4), _ptr(expert_rowscale), _ptr(shared_w4),
+                                       _ptr(shared_rowscale), _ptr(out), _stream(stream)),
+           "layer_forward")
+    return out
+
+
+def layer_forward_hostio(x_host, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                         shared_rowscale, out_host, stream=None):
+    _check(_lib.coli_moe_layer_forward_hostio(_host_ptr(x_host), x_host.shape[0], _ptr(router_w),
+                                              _ptr(router_bias), _ptr(expert_w4),
+                                              _ptr(expert_rowscale), _ptr(shared_w4),
+                                              _ptr(shared_rowscale), _host_ptr(out_host),
+                                              _stream(stream)),
+           "layer_forward_hostio")
+    return out_host
+
+
+def get_device_status(stream=None) -> int:
+    return _lib.coli_moe_get_device_status(_stream(stream))
+
+
+def pack_int4(w, packed=None, scale=None, stream=None):
+    rows, K = w.shape
+    if packed is None:
+        packed = torch.empty((rows, K // 2), dtype=torch.uint8, device=w.device)
+    if scale is None:
+        scale = torch.empty((rows,), dtype=torch.float32, device=w.device)
+    _check(_lib.coli_moe_pack_int4(_ptr(w), rows, K, _ptr(packed), _ptr(scale), _stream(stream)),
+           "pack_int4")
+    return packed, scale
+
+
+def timing_enable(on: bool = True):
+    _check(_lib.coli_moe_timing_enable(1 if on else 0), "timing_enable")
+
+
+def timing_read():
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_int(0)
+    _check(_lib.coli_moe_timing_read(ctypes.byref(ms), ctypes.byref(n)), "timing_read")
+    return ms.value, n.value
+
+
+def launch_count() -> int:
+    return int(_lib.coli_moe_launch_count())
+
+
+# ---- stage entry points ---------------------------------------------------- #
+def dbg_quantize(x, stream=None):
+    n = x.numel()
+    q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    d = torch.empty(x.shape[:-1] + (x.shape[-1] // 32,), dtype=torch.float32, device=x.device)
+    _check(_lib.coli_moe_dbg_quantize(_ptr(x), n, _ptr(q), _ptr(d), _stream(stream)), "dbg_quantize")
+    return q, d
+
+
+def dbg_route(x, router_w, router_bias, top_k, want_logits=False, stream=None):
+    T = x.shape[0]
+    idx = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    logits = (torch.empty((T, router_w.shape[0]), dtype=torch.float32, device=x.device)
+              if want_logits else None)
+    _check(_lib.coli_moe_dbg_route(_ptr(x), T, _ptr(router_w), _ptr(router_bias), _ptr(idx),
+                                   _ptr(w), _ptr(logits), _stream(stream)), "dbg_route")
+    return (idx, w, logits) if want_logits else (idx, w)
+
+
+def dbg_dispatch(idx, n_experts, stream=None):
+    T, k = idx.shape
+    dev = idx.device
+    counts = torch.empty(n_experts, dtype=torch.int32, device=dev)
+    offsets = torch.empty(n_experts + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    _check(_lib.coli_moe_dbg_dispatch(_ptr(idx), T, _ptr(counts), _ptr(offsets), _ptr(perm),
+                                      _ptr(inv), _stream(stream)), "dbg_dispatch")
+    return counts, offsets, perm, inv
+
+
+def dbg_block_dots(w4, q, stream=None):
+    rows, K2 = w4.shape
+    I = torch.empty((rows, 2 * K2 // 32), dtype=torch.int32, device=w4.device)
+    _check(_lib.coli_moe_dbg_block_dots(_ptr(w4), rows, 2 * K2, _ptr(q), _ptr(I), _stream(stream)),
+           "dbg_block_dots")
+    return I
+
+
+def dbg_forward_intermediates(x, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                              shared_rowscale, hidden, ffn, top_k, stream=None):
+    T = x.shape[0]
+    dev = x.device
+    R = T * top_k + T
+    r = dict(
+        out=torch.empty_like(x),
+        qx=torch.empty((T, hidden), dtype=torch.int8, device=dev),
+        dx=torch.empty((T, hidden // 32), dtype=torch.float32, device=dev),
+        idx=torch.empty((T, top_k), dtype=torch.int32, device=dev),
+        w=torch.empty((T, top_k), dtype=torch.float32, device=dev),
+        qh=torch.empty((R, ffn), dtype=torch.int8, device=dev),
+        dh=torch.empty((R, ffn // 32), dtype=torch.float32, device=dev),
+        y=torch.empty((R, hidden), dtype=torch.float32, device=dev),
+    )
+    _check(_lib.coli_moe_dbg_forward_intermediates(
+        _ptr(x), T, _ptr(router_w), _ptr(router_bias), _ptr(expert_w4), _ptr(expert_rowscale),
+        _ptr(shared_w4), _ptr(shared_rowscale), _ptr(r["out"]), _ptr(r["qx"]), _ptr(r["dx"]),
+        _ptr(r["idx"]), _ptr(r["w"]), _ptr(r["qh"]), _ptr(r["dh"]), _ptr(r["y"]),
+        _stream(stream)), "dbg_forward_intermediates")
+    return r
+
+
+def dbg_expert_hidden(ew4, ers, qx, dx, ffn, stream=None):
+    n = qx.shape[0]
+    dev = qx.device
+    h = torch.empty((n, ffn), dtype=torch.float32, device=dev)
+    qh = torch.empty((n, ffn), dtype=torch.int8, device=dev)
+    dh = torch.empty((n, ffn // 32), dtype=torch.float32, device=dev)
+    _check(_lib.coli_moe_dbg_expert_hidden(_ptr(ew4), _ptr(ers), _ptr(qx), _ptr(dx), n, _ptr(h),
+                                           _ptr(qh), _ptr(dh), _stream(stream)),
+           "dbg_expert_hidden")
+    return h, qh, dh

@@ -1,0 +1,63 @@
+// coli_internal.h -- host-side declarations shared by the library's
+// translation units (launchers and the argument blocks of the kernels).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace coli {
+
+// Per-forward view of the workspace and the weights, passed by value to the
+// expert kernels.
+struct ExpertArgs {
+    int H, F, E, k;
+    int n_tok;                      // T
+    int P;                          // T * k (routed pairs); shared rows follow at P + t
+    const uint8_t *expert_w4;       // [E][3FH/2]
+    const float *expert_rs;         // [E][2F+H]
+    const uint8_t *shared_w4;       // [3FH/2]
+    const float *shared_rs;         // [2F+H]
+    const int8_t *qx;               // [T][H]
+    const float *dx;                // [T][H/32]
+    const int32_t *pos_token;       // [P+T] token of each dispatch position
+    const int32_t *tile_expert;     // [n_tiles] expert (E = shared)
+    const int32_t *tile_pos0;       // [n_tiles] first dispatch position
+    const int32_t *tile_m;          // [n_tiles] tokens in the tile (1..GEMV_MT)
+    const int32_t *n_tiles;         // device scalar
+    int8_t *qh;                     // [P+T][F] requantised hidden, by position
+    float *dh;                      // [P+T][F/32]
+    float *h_dbg;                   // optional [P+T][F] hidden before requantisation
+    float *y;                       // [P+T][H] expert outputs, by position
+    int *status;
+};
+
+void count_launch();
+
+int launch_q8_0(const float *x, long n, int8_t *q, float *d, cudaStream_t st);
+int launch_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *scale, cudaStream_t st);
+int launch_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q, int32_t *I, cudaStream_t st);
+
+int launch_router_logits(const float *x, int T, int H, const float *W, int E, float *logits,
+                         cudaStream_t st);
+int launch_topk(const float *logits, int T, int E, int k, const float *bias, float routed_scale,
+                int32_t *idx, float *w, cudaStream_t st);
+// Stable counting sort of the T*k pairs by expert, plus the GEMV tile list
+// (shared expert first, then routed experts in ascending id).
+int launch_dispatch(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                    int32_t *perm, int32_t *inv, int32_t *pos_token, int32_t *tile_expert,
+                    int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles, int *status,
+                    cudaStream_t st);
+// Tile list for one expert over n consecutive positions (stage tests).
+int launch_single_expert_tiles(int n, int32_t *pos_token, int32_t *tile_expert, int32_t *tile_pos0,
+                               int32_t *tile_m, int32_t *n_tiles, cudaStream_t st);
+
+int max_gemv_tiles(int T, int k, int E);
+int launch_gateup_gemv(const ExpertArgs &a, int num_sms, cudaStream_t st);
+int launch_down_gemv(const ExpertArgs &a, int num_sms, cudaStream_t st);
+int launch_combine(const float *y, const int32_t *inv, const float *w, int T, int k, int H, int P,
+                   float *out, cudaStream_t st);
+int launch_gather_pairs(const int32_t *inv, int T, int k, int P, const int8_t *qh, const float *dh,
+                        const float *y, int F, int H, int8_t *qh_out, float *dh_out, float *y_out,
+                        cudaStream_t st);
+
+}  // namespace coli

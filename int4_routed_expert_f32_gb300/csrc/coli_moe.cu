@@ -1,0 +1,464 @@
+// coli_moe.cu -- the C ABI (include/coli_moe.h): argument checks, the
+// library-owned workspace, and the launch sequence of one MoE layer forward.
+//
+// Forward sequence on the caller's stream (no host synchronisation):
+//   1. Q8_0-quantise x                        (k_q8_0)
+//   2. router logits in the fixed F32 order   (k_router_logits)
+//   3. sigmoid, top-k, renormalise            (k_topk)
+//   4. stable token->expert dispatch + tiles  (k_dispatch)
+//   5. gate/up + SiLU*up + requantise h       (k_gateup_gemv)
+//   6. down                                   (k_down_gemv)
+//   7. gate-weighted combine + shared expert  (k_combine)
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "../../include/coli_moe.h"
+#include "coli_common.cuh"
+#include "coli_internal.h"
+
+namespace coli {
+
+static long long g_launches = 0;
+void count_launch() { ++g_launches; }
+
+struct Workspace {
+    void *base = nullptr;
+    size_t bytes = 0;
+    int8_t *qx = nullptr;
+    float *dx = nullptr;
+    float *logits = nullptr;
+    int32_t *idx = nullptr;
+    float *wts = nullptr;
+    int32_t *counts = nullptr, *offsets = nullptr, *perm = nullptr, *inv = nullptr;
+    int32_t *pos_token = nullptr;
+    int32_t *tile_expert = nullptr, *tile_pos0 = nullptr, *tile_m = nullptr, *n_tiles = nullptr;
+    int8_t *qh = nullptr;
+    float *dh = nullptr;
+    float *y = nullptr;
+    float *x_io = nullptr, *out_io = nullptr;
+    int *status = nullptr;
+};
+
+struct State {
+    bool configured = false;
+    coli_moe_shape s{};
+    int device = -1;
+    int num_sms = 0;
+    Workspace ws;
+    int path = COLI_PATH_AUTO;
+    int gemm_min_tokens = 0;
+    bool timing = false;
+    std::vector<cudaEvent_t> ev_pool;  // pairs (start, stop)
+    int ev_used = 0;
+};
+
+static State g;
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int cuda_fail(cudaError_t e)
+{
+    (void)cudaGetLastError();
+    (void)e;
+    return COLI_E_CUDA;
+}
+
+#define CUDA_OK(call)                                  \
+    do {                                               \
+        cudaError_t e_ = (call);                       \
+        if (e_ != cudaSuccess) return cuda_fail(e_);   \
+    } while (0)
+
+#define LAUNCH_OK(call)                                        \
+    do {                                                       \
+        if ((call) != 0) return cuda_fail(cudaErrorUnknown);   \
+        cudaError_t e_ = cudaGetLastError();                   \
+        if (e_ != cudaSuccess) return cuda_fail(e_);           \
+    } while (0)
+
+static void free_workspace()
+{
+    if (g.ws.base) cudaFree(g.ws.base);
+    g.ws = Workspace{};
+    for (cudaEvent_t e : g.ev_pool) cudaEventDestroy(e);
+    g.ev_pool.clear();
+    g.ev_used = 0;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int check_shape(const coli_moe_shape *s)
+{
+    if (!s) return COLI_E_INVAL;
+    if (s->hidden <= 0 || s->hidden % 128 != 0 || s->hidden > 16384) return COLI_E_INVAL;
+    if (s->ffn <= 0 || s->ffn % 128 != 0 || s->ffn > 16384) return COLI_E_INVAL;
+    if (s->n_experts < 1 || s->n_experts > 256) return COLI_E_INVAL;
+    if (s->top_k < 1 || s->top_k > 16 || s->top_k > s->n_experts) return COLI_E_INVAL;
+    if (s->max_tok < 1 || s->max_tok > 65536) return COLI_E_INVAL;
+    if (!(s->routed_scale > 0.0f) || s->routed_scale > 3.0e38f) return COLI_E_INVAL;
+    return COLI_OK;
+}
+
+}  // namespace coli
+
+using namespace coli;
+
+extern "C" {
+
+const char *coli_moe_strerror(int code)
+{
+    switch (code) {
+    case COLI_OK: return "ok";
+    case COLI_E_INVAL: return "invalid argument";
+    case COLI_E_NOSHAPE: return "layer shape not configured";
+    case COLI_E_NOMEM: return "workspace allocation failed";
+    case COLI_E_CUDA: return "CUDA call or launch failed";
+    case COLI_E_TIMEOUT: return "a bounded device-side wait gave up";
+    case COLI_E_UNIMPL: return "not implemented";
+    case COLI_E_DEVICE: return "device status reports an out-of-range expert index";
+    default: return "unknown status";
+    }
+}
+
+void coli_moe_release(void)
+{
+    if (g.ws.base) cudaDeviceSynchronize();
+    free_workspace();
+    g.configured = false;
+}
+
+int coli_moe_configure(const coli_moe_shape *s)
+{
+    int st = check_shape(s);
+    if (st != COLI_OK) return st;
+    coli_moe_release();
+    int dev = 0;
+    CUDA_OK(cudaGetDevice(&dev));
+    int sms = 0;
+    CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+
+    const size_t T = (size_t)s->max_tok, H = (size_t)s->hidden, F = (size_t)s->ffn;
+    const size_t E = (size_t)s->n_experts, k = (size_t)s->top_k;
+    const size_t P = T * k, R = P + T;
+    const size_t tiles = (size_t)max_gemv_tiles((int)T, (int)k, (int)E);
+    // carve one allocation; every piece 256-byte aligned
+    struct Piece { void **dst; size_t bytes; };
+    Workspace w;
+    Piece pieces[] = {
+        {(void **)&w.qx, T * H},
+        {(void **)&w.dx, T * (H / 32) * 4},
+        {(void **)&w.logits, T * E * 4},
+        {(void **)&w.idx, P * 4},
+        {(void **)&w.wts, P * 4},
+        {(void **)&w.counts, E * 4},
+        {(void **)&w.offsets, (E + 1) * 4},
+        {(void **)&w.perm, P * 4},
+        {(void **)&w.inv, P * 4},
+        {(void **)&w.pos_token, R * 4},
+        {(void **)&w.tile_expert, tiles * 4},
+        {(void **)&w.tile_pos0, tiles * 4},
+        {(void **)&w.tile_m, tiles * 4},
+        {(void **)&w.n_tiles, 4},
+        {(void **)&w.qh, R * F},
+        {(void **)&w.dh, R * (F / 32) * 4},
+        {(void **)&w.y, R * H * 4},
+        {(void **)&w.x_io, T * H * 4},
+        {(void **)&w.out_io, T * H * 4},
+        {(void **)&w.status, 4},
+    };
+    size_t total = 0;
+    for (auto &p : pieces) total += align_up(p.bytes, 256);
+    void *base = nullptr;
+    if (cudaMalloc(&base, total) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return COLI_E_NOMEM;
+    }
+    size_t off = 0;
+    for (auto &p : pieces) {
+        *p.dst = (char *)base + off;
+        off += align_up(p.bytes, 256);
+    }
+    w.base = base;
+    w.bytes = total;
+    if (cudaMemset(base, 0, total) != cudaSuccess) {
+        cudaFree(base);
+        return cuda_fail(cudaErrorUnknown);
+    }
+    CUDA_OK(cudaDeviceSynchronize());
+    g.ws = w;
+    g.s = *s;
+    g.device = dev;
+    g.num_sms = sms;
+    g.configured = true;
+    return COLI_OK;
+}
+
+int coli_moe_set_path(int path, int gemm_min_tokens)
+{
+    if (path < COLI_PATH_AUTO || path > COLI_PATH_GEMM) return COLI_E_INVAL;
+    if (path == COLI_PATH_GEMM) return COLI_E_UNIMPL;
+    g.path = path;
+    g.gemm_min_tokens = gemm_min_tokens;
+    return COLI_OK;
+}
+
+long long coli_moe_launch_count(void)
+{
+    long long n = g_launches;
+    g_launches = 0;
+    return n;
+}
+
+int coli_moe_timing_enable(int on)
+{
+    g.timing = on != 0;
+    return COLI_OK;
+}
+
+int coli_moe_timing_read(double *ms_total, int *n_timed)
+{
+    if (!ms_total || !n_timed) return COLI_E_INVAL;
+    double sum = 0.0;
+    for (int i = 0; i < g.ev_used; ++i) {
+        CUDA_OK(cudaEventSynchronize(g.ev_pool[2 * i + 1]));
+        float ms = 0.0f;
+        CUDA_OK(cudaEventElapsedTime(&ms, g.ev_pool[2 * i], g.ev_pool[2 * i + 1]));
+        sum += ms;
+    }
+    *ms_total = sum;
+    *n_timed = g.ev_used;
+    g.ev_used = 0;
+    return COLI_OK;
+}
+
+static int timing_events(cudaEvent_t *start, cudaEvent_t *stop)
+{
+    if (g.ev_used * 2 + 2 > (int)g.ev_pool.size()) {
+        if (g.ev_pool.size() >= 2 * 65536) return COLI_E_NOMEM;
+        for (int i = 0; i < 2; ++i) {
+            cudaEvent_t e;
+            CUDA_OK(cudaEventCreate(&e));
+            g.ev_pool.push_back(e);
+        }
+    }
+    *start = g.ev_pool[2 * g.ev_used];
+    *stop = g.ev_pool[2 * g.ev_used + 1];
+    ++g.ev_used;
+    return COLI_OK;
+}
+
+int coli_moe_get_device_status(void *stream)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    cudaStream_t st = (cudaStream_t)stream;
+    CUDA_OK(cudaStreamSynchronize(st));
+    int v = 0;
+    CUDA_OK(cudaMemcpy(&v, g.ws.status, 4, cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemset(g.ws.status, 0, 4));
+    if (v & ST_TIMEOUT) return COLI_E_TIMEOUT;
+    if (v & (ST_BAD_INDEX | ST_BAD_SHAPE)) return COLI_E_DEVICE;
+    return COLI_OK;
+}
+
+int coli_moe_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *scale, void *stream)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0) return COLI_E_INVAL;
+    if (rows == 0) return COLI_OK;
+    if (!w || !packed || !scale || ((uintptr_t)w & 7u)) return COLI_E_INVAL;
+    LAUNCH_OK(launch_pack_int4(w, rows, K, packed, scale, (cudaStream_t)stream));
+    return COLI_OK;
+}
+
+int coli_moe_dbg_quantize(const float *x, int n, int8_t *q, float *d, void *stream)
+{
+    if (n < 0 || n % 32 != 0) return COLI_E_INVAL;
+    if (n == 0) return COLI_OK;
+    if (!x || !q || !d) return COLI_E_INVAL;
+    LAUNCH_OK(launch_q8_0(x, n, q, d, (cudaStream_t)stream));
+    return COLI_OK;
+}
+
+int coli_moe_dbg_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q, int32_t *I_out,
+                            void *stream)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0) return COLI_E_INVAL;
+    if (rows == 0) return COLI_OK;
+    if (!w4 || !q || !I_out || !aligned16(w4) || !aligned16(q)) return COLI_E_INVAL;
+    LAUNCH_OK(launch_block_dots(w4, rows, K, q, I_out, (cudaStream_t)stream));
+    return COLI_OK;
+}
+
+int coli_moe_dbg_route(const float *x, int n_tok, const float *router_w, const float *router_bias,
+                       int32_t *idx, float *w, float *logits, void *stream)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    const coli_moe_shape &s = g.s;
+    if (n_tok < 0 || n_tok > s.max_tok) return COLI_E_INVAL;
+    if (n_tok == 0) return COLI_OK;
+    if (!x || !router_w || !router_bias || !idx || !w) return COLI_E_INVAL;
+    if (!aligned16(x) || !aligned16(router_w)) return COLI_E_INVAL;
+    cudaStream_t st = (cudaStream_t)stream;
+    float *lg = logits ? logits : g.ws.logits;
+    LAUNCH_OK(launch_router_logits(x, n_tok, s.hidden, router_w, s.n_experts, lg, st));
+    LAUNCH_OK(launch_topk(lg, n_tok, s.n_experts, s.top_k, router_bias, s.routed_scale, idx, w, st));
+    return COLI_OK;
+}
+
+int coli_moe_dbg_dispatch(const int32_t *idx, int n_tok, int32_t *counts, int32_t *offsets,
+                          int32_t *perm, int32_t *inv, void *stream)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    const coli_moe_shape &s = g.s;
+    if (n_tok < 0 || n_tok > s.max_tok) return COLI_E_INVAL;
+    if (n_tok == 0) return COLI_OK;
+    if (!idx || !counts || !offsets || !perm || !inv) return COLI_E_INVAL;
+    Workspace &w = g.ws;
+    LAUNCH_OK(launch_dispatch(idx, n_tok, s.top_k, s.n_experts, counts, offsets, perm, inv,
+                              w.pos_token, w.tile_expert, w.tile_pos0, w.tile_m, w.n_tiles, w.status,
+                              (cudaStream_t)stream));
+    return COLI_OK;
+}
+
+static int check_forward_args(const float *x, int n_tok, const float *router_w,
+                              const float *router_bias, const uint8_t *expert_w4,
+                              const float *expert_rowscale, const uint8_t *shared_w4,
+                              const float *shared_rowscale, const float *out)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    if (n_tok < 0 || n_tok > g.s.max_tok) return COLI_E_INVAL;
+    if (n_tok == 0) return COLI_OK;
+    if (!x || !router_w || !router_bias || !expert_w4 || !expert_rowscale || !shared_w4 ||
+        !shared_rowscale || !out)
+        return COLI_E_INVAL;
+    if (!aligned16(x) || !aligned16(router_w) || !aligned16(expert_w4) || !aligned16(shared_w4) ||
+        !aligned16(out))
+        return COLI_E_INVAL;
+    if (x == out) return COLI_E_INVAL;
+    return COLI_OK;
+}
+
+// The forward body; optionally keeps the h values before requantisation.
+static int forward_impl(const float *x, int n_tok, const float *router_w, const float *router_bias,
+                        const uint8_t *expert_w4, const float *expert_rowscale,
+                        const uint8_t *shared_w4, const float *shared_rowscale, float *out,
+                        cudaStream_t st, float *h_dbg)
+{
+    const coli_moe_shape &s = g.s;
+    Workspace &w = g.ws;
+    const int T = n_tok, H = s.hidden, F = s.ffn, E = s.n_experts, k = s.top_k;
+    const int P = T * k;
+
+    LAUNCH_OK(launch_q8_0(x, (long)T * H, w.qx, w.dx, st));
+    LAUNCH_OK(launch_router_logits(x, T, H, router_w, E, w.logits, st));
+    LAUNCH_OK(launch_topk(w.logits, T, E, k, router_bias, s.routed_scale, w.idx, w.wts, st));
+    LAUNCH_OK(launch_dispatch(w.idx, T, k, E, w.counts, w.offsets, w.perm, w.inv, w.pos_token,
+                              w.tile_expert, w.tile_pos0, w.tile_m, w.n_tiles, w.status, st));
+
+    ExpertArgs a{};
+    a.H = H; a.F = F; a.E = E; a.k = k; a.n_tok = T; a.P = P;
+    a.expert_w4 = expert_w4; a.expert_rs = expert_rowscale;
+    a.shared_w4 = shared_w4; a.shared_rs = shared_rowscale;
+    a.qx = w.qx; a.dx = w.dx; a.pos_token = w.pos_token;
+    a.tile_expert = w.tile_expert; a.tile_pos0 = w.tile_pos0; a.tile_m = w.tile_m;
+    a.n_tiles = w.n_tiles;
+    a.qh = w.qh; a.dh = w.dh; a.h_dbg = h_dbg; a.y = w.y; a.status = w.status;
+
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (g.timing) {
+        int r = timing_events(&e0, &e1);
+        if (r != COLI_OK) return r;
+        CUDA_OK(cudaEventRecord(e0, st));
+    }
+    LAUNCH_OK(launch_gateup_gemv(a, g.num_sms, st));
+    LAUNCH_OK(launch_down_gemv(a, g.num_sms, st));
+    if (g.timing) CUDA_OK(cudaEventRecord(e1, st));
+    LAUNCH_OK(launch_combine(w.y, w.inv, w.wts, T, k, H, P, out, st));
+    return COLI_OK;
+}
+
+int coli_moe_layer_forward(const float *x, int n_tok, const float *router_w,
+                           const float *router_bias, const uint8_t *expert_w4,
+                           const float *expert_rowscale, const uint8_t *shared_w4,
+                           const float *shared_rowscale, float *out, void *stream)
+{
+    int st = check_forward_args(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale,
+                                shared_w4, shared_rowscale, out);
+    if (st != COLI_OK || n_tok == 0) return st;
+    return forward_impl(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                        shared_rowscale, out, (cudaStream_t)stream, nullptr);
+}
+
+int coli_moe_layer_forward_hostio(const float *x_host, int n_tok, const float *router_w,
+                                  const float *router_bias, const uint8_t *expert_w4,
+                                  const float *expert_rowscale, const uint8_t *shared_w4,
+                                  const float *shared_rowscale, float *out_host, void *stream)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    if (!x_host || !out_host) return COLI_E_INVAL;
+    int st = check_forward_args(g.ws.x_io, n_tok, router_w, router_bias, expert_w4,
+                                expert_rowscale, shared_w4, shared_rowscale, g.ws.out_io);
+    if (st != COLI_OK || n_tok == 0) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = (size_t)n_tok * g.s.hidden * sizeof(float);
+    CUDA_OK(cudaMemcpyAsync(g.ws.x_io, x_host, bytes, cudaMemcpyHostToDevice, s));
+    st = forward_impl(g.ws.x_io, n_tok, router_w, router_bias, expert_w4, expert_rowscale,
+                      shared_w4, shared_rowscale, g.ws.out_io, s, nullptr);
+    if (st != COLI_OK) return st;
+    CUDA_OK(cudaMemcpyAsync(out_host, g.ws.out_io, bytes, cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaStreamSynchronize(s));
+    return COLI_OK;
+}
+
+int coli_moe_dbg_forward_intermediates(const float *x, int n_tok, const float *router_w,
+                                       const float *router_bias, const uint8_t *expert_w4,
+                                       const float *expert_rowscale, const uint8_t *shared_w4,
+                                       const float *shared_rowscale, float *out, int8_t *qx,
+                                       float *dx, int32_t *idx, float *wts, int8_t *qh, float *dh,
+                                       float *y, void *stream)
+{
+    int st = check_forward_args(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale,
+                                shared_w4, shared_rowscale, out);
+    if (st != COLI_OK || n_tok == 0) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = forward_impl(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                      shared_rowscale, out, s, nullptr);
+    if (st != COLI_OK) return st;
+    const coli_moe_shape &sh = g.s;
+    Workspace &w = g.ws;
+    const size_t T = (size_t)n_tok, H = sh.hidden, F = sh.ffn, k = sh.top_k;
+    if (qx) CUDA_OK(cudaMemcpyAsync(qx, w.qx, T * H, cudaMemcpyDeviceToDevice, s));
+    if (dx) CUDA_OK(cudaMemcpyAsync(dx, w.dx, T * (H / 32) * 4, cudaMemcpyDeviceToDevice, s));
+    if (idx) CUDA_OK(cudaMemcpyAsync(idx, w.idx, T * k * 4, cudaMemcpyDeviceToDevice, s));
+    if (wts) CUDA_OK(cudaMemcpyAsync(wts, w.wts, T * k * 4, cudaMemcpyDeviceToDevice, s));
+    if (qh || dh || y)
+        LAUNCH_OK(launch_gather_pairs(w.inv, n_tok, sh.top_k, n_tok * sh.top_k, w.qh, w.dh, w.y,
+                                      (int)F, (int)H, qh, dh, y, s));
+    return COLI_OK;
+}
+
+int coli_moe_dbg_expert_hidden(const uint8_t *ew4, const float *ers, const int8_t *qx,
+                               const float *dx, int n, float *h, int8_t *qh, float *dh,
+                               void *stream)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    const coli_moe_shape &s = g.s;
+    if (n < 1 || n > s.max_tok) return COLI_E_INVAL;
+    if (!ew4 || !ers || !qx || !dx || !h || !qh || !dh) return COLI_E_INVAL;
+    if (!aligned16(ew4) || !aligned16(qx)) return COLI_E_INVAL;
+    cudaStream_t st = (cudaStream_t)stream;
+    Workspace &w = g.ws;
+    LAUNCH_OK(launch_single_expert_tiles(n, w.pos_token, w.tile_expert, w.tile_pos0, w.tile_m,
+                                         w.n_tiles, st));
+    ExpertArgs a{};
+    a.H = s.hidden; a.F = s.ffn; a.E = 1; a.k = 1; a.n_tok = n; a.P = 0;
+    a.expert_w4 = ew4; a.expert_rs = ers; a.shared_w4 = ew4; a.shared_rs = ers;
+    a.qx = qx; a.dx = dx; a.pos_token = w.pos_token;
+    a.tile_expert = w.tile_expert; a.tile_pos0 = w.tile_pos0; a.tile_m = w.tile_m;
+    a.n_tiles = w.n_tiles;
+    a.qh = qh; a.dh = dh; a.h_dbg = h; a.y = w.y; a.status = w.status;
+    LAUNCH_OK(launch_gateup_gemv(a, g.num_sms, st));
+    return COLI_OK;
+}
+
+}  // extern "C"

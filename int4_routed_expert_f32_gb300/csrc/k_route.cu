@@ -1,0 +1,356 @@
+// k_route.cu -- F32 sigmoid router (logits, top-k, renormalisation) and the
+// batch-union dispatch (stable counting sort of token->expert pairs).
+//
+// Router: DeepSeek-V3-style sigmoid gating with a selection-only bias and a
+// shared expert ("Open-source engine that ran 744B GLM-5.2 on a 25GB-RAM
+// laptop", jeff.news, section "Attention and kernels"), kept in F32
+// ("GLM-5.2-colibri-int4" model card, section "Good to know").
+// Dispatch: prefill routes the union of the batch's experts in one pass
+// ("Colibri: an AI engine running a 744B model in 25GB of RAM", alphamatch.ai,
+// section "Technical excellence").
+#include <climits>
+
+#include "coli_common.cuh"
+#include "coli_internal.h"
+
+namespace coli {
+
+// ---------------------------------------------------------------------------
+// Router logits in one fixed F32 order, so that expert choices are bit-exact
+// wherever they are computed.  The H inputs form chunks of 4 consecutive
+// elements; chunk c accumulates into partial p[c mod 256] (thread c mod 256 of
+// the block), chunks ascending, elements of a chunk ascending, each step an
+// fma from p = +0.  The 256 partials fold as 8 groups of 32 by an xor
+// butterfly (p[j] + p[j ^ o], o = 16..1: a warp shuffle), and the 8 group sums
+// fold the same way with o = 4, 2, 1.
+// A block computes ET experts x TT tokens; each weight and input chunk is
+// loaded once per block.
+// ---------------------------------------------------------------------------
+template <int ET, int TT>
+__global__ void __launch_bounds__(256) k_router_logits(const float *__restrict__ x, int T, int H,
+                                                       const float *__restrict__ W, int E,
+                                                       float *__restrict__ logits)
+{
+    const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
+    const int e0 = blockIdx.x * ET, t0 = blockIdx.y * TT;
+    float acc[ET][TT];
+#pragma unroll
+    for (int e = 0; e < ET; ++e)
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc[e][t] = 0.0f;
+
+    const int nch = H >> 2;
+    for (int c = j; c < nch; c += 256) {
+        float4 wv[ET], xv[TT];
+#pragma unroll
+        for (int e = 0; e < ET; ++e)
+            wv[e] = (e0 + e < E) ? __ldg(reinterpret_cast<const float4 *>(W + (size_t)(e0 + e) * H) + c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+            xv[t] = (t0 + t < T) ? __ldg(reinterpret_cast<const float4 *>(x + (size_t)(t0 + t) * H) + c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < ET; ++e)
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                float p = acc[e][t];
+                p = __fmaf_rn(xv[t].x, wv[e].x, p);
+                p = __fmaf_rn(xv[t].y, wv[e].y, p);
+                p = __fmaf_rn(xv[t].z, wv[e].z, p);
+                p = __fmaf_rn(xv[t].w, wv[e].w, p);
+                acc[e][t] = p;
+            }
+    }
+
+    __shared__ float red[ET * TT][8];
+#pragma unroll
+    for (int e = 0; e < ET; ++e)
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+            float v = acc[e][t];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(FULL, v, o));
+            if (lane == 0) red[e * TT + t][warp] = v;
+        }
+    __syncthreads();
+    for (int i = j; i < ET * TT; i += 256) {
+        float s[8], tmp[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s[w] = red[i][w];
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) tmp[w] = __fadd_rn(s[w], s[w ^ o]);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s[w] = tmp[w];
+        }
+        int e = e0 + i / TT, t = t0 + i % TT;
+        if (e < E && t < T) logits[(size_t)t * E + e] = s[0];
+    }
+}
+
+int launch_router_logits(const float *x, int T, int H, const float *W, int E, float *logits,
+                         cudaStream_t st)
+{
+    if (T <= 0) return 0;
+    if (T == 1) {
+        k_router_logits<1, 1><<<dim3(E, 1), 256, 0, st>>>(x, T, H, W, E, logits);
+    } else if (T <= 4) {
+        k_router_logits<1, 4><<<dim3(E, 1), 256, 0, st>>>(x, T, H, W, E, logits);
+    } else {
+        k_router_logits<8, 8><<<dim3((E + 7) / 8, (T + 7) / 8), 256, 0, st>>>(x, T, H, W, E, logits);
+    }
+    count_launch();
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Top-k with lowest-index ties, one warp per token (E <= 256: 8 experts per
+// lane).  sigma_e = sigmoid(logit_e); key_e = sigma_e + bias_e (selection
+// only); S = sum of the chosen sigma in rank order from 0;
+// w_r = (sigma_r / S) * routed_scale.
+// ---------------------------------------------------------------------------
+constexpr int MAX_K = 16;
+
+__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int T, int E, int k,
+                                              const float *__restrict__ bias, float scale,
+                                              int32_t *__restrict__ idx, float *__restrict__ w)
+{
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    float sig[8], key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int e = lane + 32 * i;
+        if (e < E) {
+            sig[i] = own_sigmoid(logits[(size_t)t * E + e]);
+            key[i] = __fadd_rn(sig[i], bias[e]);
+        } else {
+            sig[i] = 0.0f;
+            key[i] = -__int_as_float(0x7f800000);
+        }
+    }
+    unsigned taken = 0;
+    float S = 0.0f;
+    int ce[MAX_K];
+    float cs[MAX_K];
+#pragma unroll
+    for (int r = 0; r < MAX_K; ++r) {
+        if (r < k) {
+            float bv = -__int_as_float(0x7f800000);
+            int be = INT_MAX;
+            float bs = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                int e = lane + 32 * i;
+                if (e < E && !((taken >> i) & 1u) && (key[i] > bv || be == INT_MAX)) {
+                    bv = key[i];
+                    be = e;
+                    bs = sig[i];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                float ov = __shfl_xor_sync(FULL, bv, o);
+                int oe = __shfl_xor_sync(FULL, be, o);
+                float os = __shfl_xor_sync(FULL, bs, o);
+                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                    bv = ov;
+                    be = oe;
+                    bs = os;
+                }
+            }
+            if (be != INT_MAX && (be & 31) == lane) taken |= 1u << (be >> 5);
+            ce[r] = (be == INT_MAX) ? -1 : be;
+            cs[r] = bs;
+            S = __fadd_rn(S, bs);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < MAX_K; ++r)
+            if (r < k) {
+                idx[(size_t)t * k + r] = ce[r];
+                w[(size_t)t * k + r] = __fmul_rn(__fdiv_rn(cs[r], S), scale);
+            }
+    }
+}
+
+int launch_topk(const float *logits, int T, int E, int k, const float *bias, float routed_scale,
+                int32_t *idx, float *w, cudaStream_t st)
+{
+    if (T <= 0) return 0;
+    unsigned grid = (unsigned)(((long)T * 32 + 255) / 256);
+    k_topk<<<grid, 256, 0, st>>>(logits, T, E, k, bias, routed_scale, idx, w);
+    count_launch();
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch: one block of 1024 threads.  Pair p = t*k + r goes to position
+// offsets[e_p] + #{p' < p : e_p' = e_p} (a stable counting sort, so the
+// tokens of an expert stay in ascending order).  Pairs are ranked 1024 at a
+// time: warp-level match gives the rank inside a warp, a per-(warp, expert)
+// count table scanned across the 32 warps gives the rank inside the chunk,
+// and a running base per expert carries it across chunks.  All integer, no
+// order-dependent atomics.
+// Also emits pos_token (token of each position; the shared expert's rows sit
+// at P + t) and the GEMV tile list: shared expert tiles first, then each
+// routed expert's tokens in tiles of GEMV_MT, experts ascending.
+// ---------------------------------------------------------------------------
+constexpr int DISPATCH_THREADS = 1024;
+constexpr int MAX_E = 256;
+
+__global__ void __launch_bounds__(DISPATCH_THREADS) k_dispatch(
+    const int32_t *__restrict__ idx, int T, int k, int E, int32_t *__restrict__ counts,
+    int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+    int32_t *__restrict__ pos_token, int32_t *__restrict__ tile_expert,
+    int32_t *__restrict__ tile_pos0, int32_t *__restrict__ tile_m, int32_t *__restrict__ n_tiles,
+    int *status)
+{
+    __shared__ int s_cnt[MAX_E];
+    __shared__ int s_base[MAX_E];
+    __shared__ int s_wc[32][MAX_E];
+    __shared__ int s_tile0[MAX_E];
+    __shared__ int s_ntiles;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = T * k;
+
+    if (tid < MAX_E) s_cnt[tid] = 0;
+    __syncthreads();
+    for (int p = tid; p < P; p += DISPATCH_THREADS) {
+        int e = idx[p];
+        if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+        else set_status(status, ST_BAD_INDEX);
+    }
+    __syncthreads();
+
+    // exclusive scan of the counts (E <= 256: 8 per lane of warp 0), and of the
+    // per-expert tile counts
+    if (warp == 0) {
+        int v[8], nt[8], sum = 0, tsum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int e = lane * 8 + i;
+            v[i] = (e < E) ? s_cnt[e] : 0;
+            nt[i] = (v[i] + GEMV_MT - 1) / GEMV_MT;
+            sum += v[i];
+            tsum += nt[i];
+        }
+        int inc = sum, tinc = tsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int a = __shfl_up_sync(FULL, inc, o);
+            int b = __shfl_up_sync(FULL, tinc, o);
+            if (lane >= o) { inc += a; tinc += b; }
+        }
+        int run = inc - sum, trun = tinc - tsum;
+        const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int e = lane * 8 + i;
+            if (e < E) {
+                s_base[e] = run;
+                offsets[e] = run;
+                counts[e] = v[i];
+                s_tile0[e] = shared_tiles + trun;
+            }
+            run += v[i];
+            trun += nt[i];
+        }
+        if (lane == 31) {
+            offsets[E] = inc;
+            s_ntiles = shared_tiles + tinc;
+        }
+    }
+    __syncthreads();
+
+    for (int c0 = 0; c0 < P; c0 += DISPATCH_THREADS) {
+        for (int i = tid; i < 32 * MAX_E; i += DISPATCH_THREADS) (&s_wc[0][0])[i] = 0;
+        __syncthreads();
+        const int p = c0 + tid;
+        int e = (p < P) ? idx[p] : -1;
+        const bool valid = (e >= 0 && e < E);
+        if (!valid) e = -1;
+        const unsigned peers = __match_any_sync(FULL, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (valid && rank == 0) s_wc[warp][e] = __popc(peers);
+        __syncthreads();
+        int chunk_total = 0;
+        if (tid < E) {
+            for (int w = 0; w < 32; ++w) {
+                int c = s_wc[w][tid];
+                s_wc[w][tid] = chunk_total;
+                chunk_total += c;
+            }
+        }
+        __syncthreads();
+        if (valid) {
+            int pos = s_base[e] + s_wc[warp][e] + rank;
+            perm[pos] = p;
+            inv[p] = pos;
+            pos_token[pos] = p / k;
+        } else if (p < P) {
+            inv[p] = -1;
+        }
+        __syncthreads();
+        if (tid < E) s_base[tid] += chunk_total;
+        __syncthreads();
+    }
+
+    for (int t = tid; t < T; t += DISPATCH_THREADS) pos_token[P + t] = t;
+    const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
+    for (int j = tid; j < shared_tiles; j += DISPATCH_THREADS) {
+        tile_expert[j] = E;
+        tile_pos0[j] = P + j * GEMV_MT;
+        tile_m[j] = min(GEMV_MT, T - j * GEMV_MT);
+    }
+    if (tid < E) {
+        const int e = tid, cnt = s_cnt[e], t0 = s_tile0[e], off = offsets[e];
+        for (int j = 0; j * GEMV_MT < cnt; ++j) {
+            tile_expert[t0 + j] = e;
+            tile_pos0[t0 + j] = off + j * GEMV_MT;
+            tile_m[t0 + j] = min(GEMV_MT, cnt - j * GEMV_MT);
+        }
+    }
+    if (tid == 0) *n_tiles = s_ntiles;
+}
+
+int launch_dispatch(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                    int32_t *perm, int32_t *inv, int32_t *pos_token, int32_t *tile_expert,
+                    int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles, int *status,
+                    cudaStream_t st)
+{
+    k_dispatch<<<1, DISPATCH_THREADS, 0, st>>>(idx, T, k, E, counts, offsets, perm, inv, pos_token,
+                                               tile_expert, tile_pos0, tile_m, n_tiles, status);
+    count_launch();
+    return 0;
+}
+
+// Tile list for a single expert (index 0) over positions 0..n-1.
+__global__ void k_single_expert_tiles(int n, int32_t *pos_token, int32_t *tile_expert,
+                                      int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles)
+{
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) pos_token[i] = i;
+    int nt = (n + GEMV_MT - 1) / GEMV_MT;
+    if (i < nt) {
+        tile_expert[i] = 0;
+        tile_pos0[i] = i * GEMV_MT;
+        tile_m[i] = min(GEMV_MT, n - i * GEMV_MT);
+    }
+    if (i == 0) *n_tiles = nt;
+}
+
+int launch_single_expert_tiles(int n, int32_t *pos_token, int32_t *tile_expert, int32_t *tile_pos0,
+                               int32_t *tile_m, int32_t *n_tiles, cudaStream_t st)
+{
+    k_single_expert_tiles<<<(n + 255) / 256, 256, 0, st>>>(n, pos_token, tile_expert, tile_pos0,
+                                                          tile_m, n_tiles);
+    count_launch();
+    return 0;
+}
+
+}  // namespace coli

@@ -11,10 +11,11 @@ expert, SwiGLU experts, hidden 6144, expert FFN 2048):
 
 * ``tiny``      hidden 256, FFN 128, 8 experts top-2, 4 tokens, seed 0
 * ``decode``    the GLM-5.2 shape, 1 token per forward, seed 1
-* ``verify``    the GLM-5.2 shape, 4 correlated tokens per forward
-                (x_t = 0.7 x_0 + 0.3 N(0,1)), seed 2
-* ``prefill``   the GLM-5.2 shape, 2048 tokens with per-token norm jitter
-                U(0.5, 2) and a Zipf-skewed router bias, seed 3
+* ``verify``    the decode layer's weights, 4 correlated tokens per forward
+                (x_t = 0.7 x_0 + 0.3 N(0,1)), activation seed 2
+* ``prefill``   the decode layer's weights, 2048 tokens with per-token norm
+                jitter U(0.5, 2) and a Zipf-skewed router bias, activation
+                seed 3
 * ``sweep``     8 stacked GLM-5.2-shaped layers (seeds 100..107), batches
                 1, 8, 32, 128, Zipf-skewed bias, router rows of layer l drawn
                 correlated with layer l-1's
@@ -59,6 +60,7 @@ class Workload:
     layers: int = 1
     layer_corr: float = 0.0              # sweep: router rows correlated across layers
     batches: tuple = ()
+    weight_seed: int | None = None       # seed of the layer's weights (default: seed)
 
     @property
     def expert_bytes(self) -> int:
@@ -70,7 +72,12 @@ class Workload:
         return 2 * self.ffn + self.hidden
 
     def layer_seed(self, layer: int) -> int:
-        return self.seed + layer
+        """Seed of the weights of layer ``layer``."""
+        base = self.seed if self.weight_seed is None else self.weight_seed
+        return base + layer
+
+    def act_seed(self, layer: int) -> int:
+        return self.seed + 1000 * layer
 
 
 # Zipf amplitude of the prefill and sweep router bias, chosen so that on 2048
@@ -83,9 +90,10 @@ SWEEP_LAYER_CORR = 0.8
 WORKLOADS = {
     "tiny": Workload("tiny", 256, 128, 8, 2, 4, 0),
     "decode": Workload("decode", 6144, 2048, 256, 8, 1, 1),
-    "verify": Workload("verify", 6144, 2048, 256, 8, 4, 2, correlated_tokens=True),
+    "verify": Workload("verify", 6144, 2048, 256, 8, 4, 2, correlated_tokens=True,
+                       weight_seed=1),
     "prefill": Workload("prefill", 6144, 2048, 256, 8, 2048, 3, norm_jitter=True,
-                        zipf_beta=ZIPF_BETA),
+                        zipf_beta=ZIPF_BETA, weight_seed=1),
     "sweep": Workload("sweep", 6144, 2048, 256, 8, 128, 100, zipf_beta=ZIPF_BETA, layers=8,
                       layer_corr=SWEEP_LAYER_CORR, batches=(1, 8, 32, 128)),
 }
@@ -159,7 +167,7 @@ def expert_f32_rows(wl: Workload, e: int, layer: int = 0) -> np.ndarray:
 def activations(wl: Workload, step: int, n_tok: int | None = None, layer: int = 0) -> np.ndarray:
     """Input activations [T][H] (F32) of forward number ``step``."""
     T = wl.n_tok if n_tok is None else n_tok
-    s = wl.layer_seed(layer)
+    s = wl.act_seed(layer)
     x = normal((T, wl.hidden), 1.0, s, _T_X, step)
     if wl.correlated_tokens:
         noise = normal((T, wl.hidden), 1.0, s, _T_X_NOISE, step)

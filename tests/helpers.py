@@ -1,0 +1,64 @@
+"""Test-side helpers: oracle-packed experts from the seeded draws, and the
+parity tolerance."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+
+import synth
+
+
+def oracle_expert(wl: synth.Workload, e: int, layer: int = 0):
+    """(packed bytes [3FH/2], row scales [2F+H]) of expert e (E = shared),
+    packed by the oracle's own converter from the seeded F32 draw."""
+    import oracle
+    F, H = wl.ffn, wl.hidden
+    flat = synth.expert_f32_rows(wl, e, layer)
+    pg, sg = oracle.pack_int4_rows(flat[:F * H].reshape(F, H))
+    pu, su = oracle.pack_int4_rows(flat[F * H:2 * F * H].reshape(F, H))
+    pd, sd = oracle.pack_int4_rows(flat[2 * F * H:].reshape(H, F))
+    return (np.concatenate([pg.ravel(), pu.ravel(), pd.ravel()]),
+            np.concatenate([sg, su, sd]))
+
+
+class OracleLayer:
+    """Lazily packs only the experts a sample touches."""
+
+    def __init__(self, wl: synth.Workload, layer: int = 0):
+        self.wl = wl
+        self.layer = layer
+        self.W, self.b = synth.router(wl, layer)
+        self.shared = oracle_expert(wl, wl.n_experts, layer)
+        self._cache = {}
+
+    def expert(self, e):
+        if e not in self._cache:
+            self._cache[e] = oracle_expert(self.wl, e, self.layer)
+        return self._cache[e]
+
+    def forward(self, x, intermediates=False):
+        import oracle
+        wl = self.wl
+        idx, _ = oracle.route(x, self.W, self.b, wl.top_k, wl.routed_scale)
+        need = set(int(v) for v in idx.ravel())
+        w4 = [None] * wl.n_experts
+        rs = [None] * wl.n_experts
+        for e in need:
+            w4[e], rs[e] = self.expert(e)
+        return oracle.moe_forward(x, self.W, self.b, w4, rs, self.shared[0], self.shared[1],
+                                  wl.hidden, wl.ffn, wl.top_k, wl.routed_scale,
+                                  intermediates=intermediates)
+
+
+# Float outputs must agree within max|err| <= 1e-3 * rms(oracle output).
+FLOAT_TOL = 1e-3
+
+
+def assert_float_close(got, want, tol=FLOAT_TOL, what="out"):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    err = float(np.max(np.abs(got - want))) if want.size else 0.0
+    assert err <= tol * rms, f"{what}: max|err| {err:.3e} > {tol} * rms {rms:.3e} ({err / max(rms, 1e-30):.2e})"
+    return err / max(rms, 1e-30)

@@ -1,0 +1,69 @@
+"""Host-side checks of the C ABI: the library builds, loads, and exports every
+symbol the header declares; argument errors come back before any launch (no
+GPU needed for those)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "coli_moe.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(coli_moe_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int4_routed_expert_f32_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    assert "coli_moe_layer_forward" in names and "coli_moe_configure" in names
+    assert len(names) >= 15
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_lists_every_declared_symbol():
+    import int4_routed_expert_f32_gb300 as coli
+    assert sorted(coli.EXPORTS) == _declared()
+
+
+def test_shape_validation_without_gpu(lib):
+    import int4_routed_expert_f32_gb300 as coli
+    bad = [
+        (255, 128, 8, 2, 2.5, 4),     # hidden not a multiple of 128
+        (256, 100, 8, 2, 2.5, 4),     # ffn not a multiple of 128
+        (256, 128, 300, 2, 2.5, 4),   # too many experts
+        (256, 128, 8, 9, 2.5, 4),     # top_k > n_experts
+        (256, 128, 8, 2, 0.0, 4),     # routed_scale must be > 0
+        (256, 128, 8, 2, 2.5, 0),     # max_tok >= 1
+    ]
+    for s in bad:
+        with pytest.raises(coli.ColiError) as ei:
+            coli.configure(*s)
+        assert ei.value.code == coli.E_INVAL
+
+
+def test_calls_before_configure_report_noshape(lib):
+    import int4_routed_expert_f32_gb300 as coli
+    coli.release()
+    L = coli.lib()
+    assert L.coli_moe_layer_forward(None, 1, None, None, None, None, None, None, None, None) == coli.E_NOSHAPE
+    assert L.coli_moe_dbg_route(None, 1, None, None, None, None, None, None) == coli.E_NOSHAPE
+    assert L.coli_moe_pack_int4(None, 4, 33, None, None, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_quantize(None, 31, None, None, None) == coli.E_INVAL
+    assert L.coli_moe_set_path(7, 0) == coli.E_INVAL
+    assert L.coli_moe_strerror(coli.E_NOSHAPE) == b"layer shape not configured"

@@ -1,0 +1,157 @@
+"""End-to-end parity of the layer forward (C ABI) against the oracle.
+
+Every float output is held to max|err| <= 1e-3 * rms(oracle); because the CUDA
+path follows the oracle's F32 order wherever a float decides an integer, the
+outputs are in fact expected bit-identical, which is asserted too.  Integer
+intermediates (Q8_0 codes, router indices, hidden codes) are bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from helpers import OracleLayer, assert_float_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def coli():
+    import int4_routed_expert_f32_gb300 as c
+    torch.cuda.set_device(0)
+    return c
+
+
+def _cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _forward(coli, L, x, router_b=None):
+    return coli.layer_forward(_cuda(x), L["router_w"], L["router_b"] if router_b is None else router_b,
+                              L["expert_w4"], L["expert_rs"], L["shared_w4"], L["shared_rs"])
+
+
+def _configure(coli, wl, max_tok):
+    coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, max_tok)
+
+
+# --------------------------------------------------------------------------- #
+# tiny layer: full intermediates                                               #
+# --------------------------------------------------------------------------- #
+@pytest.fixture(scope="module")
+def tiny(coli):
+    from synth.device import build_device_layer
+    wl = synth.WORKLOADS["tiny"]
+    return wl, build_device_layer(wl), OracleLayer(wl)
+
+
+@pytest.mark.parametrize("T", [4, 1, 3, 37])
+def test_tiny_forward_and_intermediates(coli, tiny, T):
+    wl, L, ref = tiny
+    _configure(coli, wl, 64)
+    x = synth.activations(wl, T, n_tok=T)
+    r = coli.dbg_forward_intermediates(_cuda(x), L["router_w"], L["router_b"], L["expert_w4"],
+                                       L["expert_rs"], L["shared_w4"], L["shared_rs"],
+                                       wl.hidden, wl.ffn, wl.top_k)
+    out, it = ref.forward(x, intermediates=True)
+    assert coli.get_device_status() == coli.OK
+    np.testing.assert_array_equal(r["qx"].cpu().numpy(), it["qx"])
+    np.testing.assert_array_equal(r["dx"].cpu().numpy(), it["dx"])
+    np.testing.assert_array_equal(r["idx"].cpu().numpy(), it["idx"])
+    np.testing.assert_array_equal(r["w"].cpu().numpy(), it["w"])
+    y = r["y"].cpu().numpy()
+    P = T * wl.top_k
+    np.testing.assert_array_equal(y[:P].reshape(T, wl.top_k, wl.hidden), it["y_routed"])
+    np.testing.assert_array_equal(y[P:], it["y_shared"])
+    got = r["out"].cpu().numpy()
+    assert_float_close(got, out)
+    np.testing.assert_array_equal(got, out)
+
+
+def test_tiny_edge_cases(coli, tiny):
+    wl, L, ref = tiny
+    _configure(coli, wl, 8)
+    empty = torch.empty((0, wl.hidden), dtype=torch.float32, device="cuda")
+    coli.layer_forward(empty, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                       L["shared_w4"], L["shared_rs"])
+    # n_tok above max_tok is an argument error, reported before any launch
+    x = _cuda(synth.activations(wl, 0, n_tok=9))
+    with pytest.raises(coli.ColiError) as ei:
+        coli.layer_forward(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                           L["shared_w4"], L["shared_rs"])
+    assert ei.value.code == coli.E_INVAL
+    # exactly max_tok tokens
+    x = synth.activations(wl, 5, n_tok=8)
+    np.testing.assert_array_equal(_forward(coli, L, x).cpu().numpy(), ref.forward(x))
+    # misaligned weights are rejected
+    with pytest.raises(coli.ColiError):
+        coli.layer_forward(_cuda(x), L["router_w"], L["router_b"], L["expert_w4"].view(-1)[1:],
+                           L["expert_rs"], L["shared_w4"], L["shared_rs"])
+
+
+def test_tiny_hostio_matches_device_call(coli, tiny):
+    wl, L, ref = tiny
+    _configure(coli, wl, 8)
+    x = synth.activations(wl, 3, n_tok=4)
+    xh = torch.from_numpy(x).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    coli.layer_forward_hostio(xh, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                              L["shared_w4"], L["shared_rs"], oh)
+    np.testing.assert_array_equal(oh.numpy(), ref.forward(x))
+
+
+# --------------------------------------------------------------------------- #
+# GLM-5.2-shaped layer (256 experts + shared, all resident)                    #
+# --------------------------------------------------------------------------- #
+@pytest.fixture(scope="module")
+def glm(coli):
+    from synth.device import build_device_layer
+    wl = synth.WORKLOADS["decode"]
+    return build_device_layer(wl), OracleLayer(wl)
+
+
+def test_decode_batch1(coli, glm):
+    L, ref = glm
+    wl = synth.WORKLOADS["decode"]
+    _configure(coli, wl, 2048)
+    for step in range(3):
+        x = synth.activations(wl, step)
+        got = _forward(coli, L, x).cpu().numpy()
+        want = ref.forward(x)
+        assert_float_close(got, want)
+        np.testing.assert_array_equal(got, want)
+    assert coli.get_device_status() == coli.OK
+
+
+def test_verify_batch4(coli, glm):
+    L, ref = glm
+    wl = synth.WORKLOADS["verify"]
+    _configure(coli, wl, 2048)
+    for step in range(2):
+        x = synth.activations(wl, step)
+        got = _forward(coli, L, x).cpu().numpy()
+        want = ref.forward(x)
+        assert_float_close(got, want)
+        np.testing.assert_array_equal(got, want)
+
+
+def test_prefill_2048_sampled(coli, glm, orc):
+    L, ref = glm
+    wl = synth.WORKLOADS["prefill"]
+    _configure(coli, wl, 2048)
+    W, b = synth.router(wl)
+    bd = _cuda(b)
+    x = synth.activations(wl, 0)
+    got = _forward(coli, L, x, router_b=bd).cpu().numpy()
+    # routing of every token, bit-exact
+    idx, w = coli.dbg_route(_cuda(x), L["router_w"], bd, wl.top_k)
+    ridx, rw = orc.route(x, W, b, wl.top_k, wl.routed_scale)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    counts = np.bincount(ridx.ravel(), minlength=wl.n_experts)
+    assert counts.max() >= 100, counts.max()          # the Zipf skew is in effect
+    # outputs of sampled tokens (each token's result does not depend on the batch)
+    ref_p = OracleLayer(wl)
+    ref_p._cache = ref._cache
+    sample = [0, 1, 777, 1500, 2046, 2047]
+    want = ref_p.forward(x[sample])
+    assert_float_close(got[sample], want)
+    np.testing.assert_array_equal(got[sample], want)
