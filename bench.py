@@ -159,8 +159,8 @@ def run(args):
     import torch
     import torch.distributed as dist
 
-    from int4_routed_expert_f32_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._builder().build()
     import int4_routed_expert_f32_gb300 as coli
     from synth.device import build_device_layer
 

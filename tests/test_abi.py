@@ -20,8 +20,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from int4_routed_expert_f32_gb300 import _build
-    path = _build.build()
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path)
 
 
