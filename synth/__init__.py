@@ -94,6 +94,9 @@ WORKLOADS = {
                        weight_seed=1),
     "prefill": Workload("prefill", 6144, 2048, 256, 8, 2048, 3, norm_jitter=True,
                         zipf_beta=ZIPF_BETA, weight_seed=1),
+    # the decode shape with 16 routed experts (~0.3 GB resident): a small case of
+    # the same kernels for profiler captures; one forward still reads 170 MB
+    "profile": Workload("profile", 6144, 2048, 16, 8, 1, 1),
     "sweep": Workload("sweep", 6144, 2048, 256, 8, 128, 100, zipf_beta=ZIPF_BETA, layers=8,
                       layer_corr=SWEEP_LAYER_CORR, batches=(1, 8, 32, 128)),
 }
