@@ -3,19 +3,28 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace coli {
 
+// Tensor maps of the expert weights (3-D: bytes of a row, rows, expert).
+struct ExpertMaps {
+    CUtensorMap gu;    // routed gate/up rows [E][2F][H/2], box KC x 32 x 1
+    CUtensorMap dn;    // routed down rows    [E][H][F/2],  box KC x 64 x 1
+    CUtensorMap sgu;   // shared expert gate/up
+    CUtensorMap sdn;   // shared expert down
+};
+
 // Per-forward view of the workspace and the weights, passed by value to the
-// expert kernels.
+// expert kernel.
 struct ExpertArgs {
     int H, F, E, k;
     int n_tok;                      // T
     int P;                          // T * k (routed pairs); shared rows follow at P + t
-    const uint8_t *expert_w4;       // [E][3FH/2]
+    int KC;                         // bytes of a weight row per pipeline stage (128 or 64)
+    int gate_up_only;               // 1: stop after h (stage tests)
     const float *expert_rs;         // [E][2F+H]
-    const uint8_t *shared_w4;       // [3FH/2]
     const float *shared_rs;         // [2F+H]
     const int8_t *qx;               // [T][H]
     const float *dx;                // [T][H/32]
@@ -24,12 +33,40 @@ struct ExpertArgs {
     const int32_t *tile_pos0;       // [n_tiles] first dispatch position
     const int32_t *tile_m;          // [n_tiles] tokens in the tile (1..GEMV_MT)
     const int32_t *n_tiles;         // device scalar
+    const int32_t *inv;             // [P] position of each pair
+    const float *wts;               // [P] routed weights
     int8_t *qh;                     // [P+T][F] requantised hidden, by position
     float *dh;                      // [P+T][F/32]
     float *h_dbg;                   // optional [P+T][F] hidden before requantisation
     float *y;                       // [P+T][H] expert outputs, by position
+    float *out;                     // [T][H]
+    int *g_done;                    // [n_tiles] finished gate/up units per tile
+    int *w_done;                    // [H/64] finished down units per row chunk
+    int *work_counter;              // next unit to claim
     int *status;
 };
+
+// Small-batch routing in one launch: Q8_0 of x, router logits, top-k, dispatch,
+// tile list, and zeroing of the expert kernel's counters.
+struct RouteArgs {
+    const float *x;
+    int T, H, E, k;
+    float routed_scale;
+    const float *W;
+    const float *bias;
+    int8_t *qx;
+    float *dx;
+    float *logits;
+    int32_t *idx;
+    float *wts;
+    int32_t *counts, *offsets, *perm, *inv, *pos_token;
+    int32_t *tile_expert, *tile_pos0, *tile_m, *n_tiles;
+    int *sync;                      // expert-kernel counters to zero
+    int n_sync;
+    int *route_counter;             // blocks finished (reset by the last block)
+    int *status;
+};
+constexpr int ROUTE_SMALL_MAX_T = 8;
 
 void count_launch();
 
@@ -41,21 +78,21 @@ int launch_router_logits(const float *x, int T, int H, const float *W, int E, fl
                          cudaStream_t st);
 int launch_topk(const float *logits, int T, int E, int k, const float *bias, float routed_scale,
                 int32_t *idx, float *w, cudaStream_t st);
-// Stable counting sort of the T*k pairs by expert, plus the GEMV tile list
-// (shared expert first, then routed experts in ascending id).
+// Stable counting sort of the T*k pairs by expert, the GEMV tile list (shared
+// expert first, then routed experts in ascending id), and zeroing of `sync`.
 int launch_dispatch(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
                     int32_t *perm, int32_t *inv, int32_t *pos_token, int32_t *tile_expert,
-                    int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles, int *status,
-                    cudaStream_t st);
+                    int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles, int *sync, int n_sync,
+                    int *status, cudaStream_t st);
+int launch_route_small(const RouteArgs &r, cudaStream_t st);
 // Tile list for one expert over n consecutive positions (stage tests).
 int launch_single_expert_tiles(int n, int32_t *pos_token, int32_t *tile_expert, int32_t *tile_pos0,
-                               int32_t *tile_m, int32_t *n_tiles, cudaStream_t st);
+                               int32_t *tile_m, int32_t *n_tiles, int *sync, int n_sync,
+                               cudaStream_t st);
 
 int max_gemv_tiles(int T, int k, int E);
-int launch_gateup_gemv(const ExpertArgs &a, int num_sms, cudaStream_t st);
-int launch_down_gemv(const ExpertArgs &a, int num_sms, cudaStream_t st);
-int launch_combine(const float *y, const int32_t *inv, const float *w, int T, int k, int H, int P,
-                   float *out, cudaStream_t st);
+size_t experts_smem_bytes(int H, int F);
+int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st);
 int launch_gather_pairs(const int32_t *inv, int T, int k, int P, const int8_t *qh, const float *dh,
                         const float *y, int F, int H, int8_t *qh_out, float *dh_out, float *y_out,
                         cudaStream_t st);

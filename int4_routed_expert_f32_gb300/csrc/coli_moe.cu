@@ -2,13 +2,12 @@
 // library-owned workspace, and the launch sequence of one MoE layer forward.
 //
 // Forward sequence on the caller's stream (no host synchronisation):
-//   1. Q8_0-quantise x                        (k_q8_0)
-//   2. router logits in the fixed F32 order   (k_router_logits)
-//   3. sigmoid, top-k, renormalise            (k_topk)
-//   4. stable token->expert dispatch + tiles  (k_dispatch)
-//   5. gate/up + SiLU*up + requantise h       (k_gateup_gemv)
-//   6. down                                   (k_down_gemv)
-//   7. gate-weighted combine + shared expert  (k_combine)
+//   routing, T <= 8: one launch (k_route_small) doing Q8_0 of x, the router
+//   logits in the fixed F32 order, sigmoid/top-k/renormalisation, the stable
+//   token->expert dispatch and the tile list;
+//   routing, T > 8: k_q8_0, k_router_logits, k_topk, k_dispatch;
+//   experts: one persistent launch (k_experts): gate/up + SiLU*up + Q8_0 of h,
+//   down, and the gate-weighted combine with the shared expert.
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -33,6 +32,9 @@ struct Workspace {
     int32_t *counts = nullptr, *offsets = nullptr, *perm = nullptr, *inv = nullptr;
     int32_t *pos_token = nullptr;
     int32_t *tile_expert = nullptr, *tile_pos0 = nullptr, *tile_m = nullptr, *n_tiles = nullptr;
+    int *sync = nullptr;            // g_done[max tiles] | w_done[H/64] | work counter
+    int n_sync = 0;
+    int *route_counter = nullptr;
     int8_t *qh = nullptr;
     float *dh = nullptr;
     float *y = nullptr;
@@ -51,6 +53,11 @@ struct State {
     bool timing = false;
     std::vector<cudaEvent_t> ev_pool;  // pairs (start, stop)
     int ev_used = 0;
+    int max_tiles = 0;
+    // tensor maps of the last weights seen (re-encoded when a pointer changes)
+    ExpertMaps maps{};
+    const void *maps_key[2] = {nullptr, nullptr};
+    bool maps_valid = false;
 };
 
 static State g;
@@ -87,6 +94,72 @@ static void free_workspace()
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// ---- TMA tensor maps of the expert weights --------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
+
+// Bytes of a weight row moved per pipeline stage.
+static int stage_kc(int H, int F) { return ((H / 2) % 128 == 0 && (F / 2) % 128 == 0) ? 128 : 64; }
+
+// rows of `row_bytes` bytes, `n_exp` experts `exp_stride` bytes apart; box =
+// kc bytes x box_rows rows of one expert
+static bool encode_rows(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows,
+                        uint64_t n_exp, uint64_t exp_stride, uint32_t box_rows, uint32_t kc)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {row_bytes, rows, n_exp};
+    cuuint64_t strides[2] = {row_bytes, exp_stride};
+    cuuint32_t box[3] = {kc, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    kc == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Maps for routed experts at `ew4` ([E][3FH/2]) and the shared expert at `sw4`.
+static bool expert_maps(const uint8_t *ew4, int E, const uint8_t *sw4, ExpertMaps *out)
+{
+    if (g.maps_valid && g.maps_key[0] == ew4 && g.maps_key[1] == sw4) {
+        *out = g.maps;
+        return true;
+    }
+    const uint64_t H = g.s.hidden, F = g.s.ffn, stride = 3 * F * H / 2;
+    const uint32_t kc = (uint32_t)stage_kc((int)H, (int)F);
+    ExpertMaps m;
+    bool ok = encode_rows(&m.gu, ew4, H / 2, 2 * F, (uint64_t)E, stride, 32, kc) &&
+              encode_rows(&m.dn, ew4 + F * H, F / 2, H, (uint64_t)E, stride, 64, kc) &&
+              encode_rows(&m.sgu, sw4, H / 2, 2 * F, 1, stride, 32, kc) &&
+              encode_rows(&m.sdn, sw4 + F * H, F / 2, H, 1, stride, 64, kc);
+    if (!ok) return false;
+    g.maps = m;
+    g.maps_key[0] = ew4;
+    g.maps_key[1] = sw4;
+    g.maps_valid = true;
+    *out = m;
+    return true;
+}
 
 static int check_shape(const coli_moe_shape *s)
 {
@@ -160,6 +233,8 @@ int coli_moe_configure(const coli_moe_shape *s)
         {(void **)&w.tile_pos0, tiles * 4},
         {(void **)&w.tile_m, tiles * 4},
         {(void **)&w.n_tiles, 4},
+        {(void **)&w.sync, (tiles + H / 64 + 1) * 4},
+        {(void **)&w.route_counter, 4},
         {(void **)&w.qh, R * F},
         {(void **)&w.dh, R * (F / 32) * 4},
         {(void **)&w.y, R * H * 4},
@@ -186,7 +261,10 @@ int coli_moe_configure(const coli_moe_shape *s)
         return cuda_fail(cudaErrorUnknown);
     }
     CUDA_OK(cudaDeviceSynchronize());
+    w.n_sync = (int)(tiles + H / 64 + 1);
     g.ws = w;
+    g.max_tiles = (int)tiles;
+    g.maps_valid = false;
     g.s = *s;
     g.device = dev;
     g.num_sms = sms;
@@ -315,8 +393,8 @@ int coli_moe_dbg_dispatch(const int32_t *idx, int n_tok, int32_t *counts, int32_
     if (!idx || !counts || !offsets || !perm || !inv) return COLI_E_INVAL;
     Workspace &w = g.ws;
     LAUNCH_OK(launch_dispatch(idx, n_tok, s.top_k, s.n_experts, counts, offsets, perm, inv,
-                              w.pos_token, w.tile_expert, w.tile_pos0, w.tile_m, w.n_tiles, w.status,
-                              (cudaStream_t)stream));
+                              w.pos_token, w.tile_expert, w.tile_pos0, w.tile_m, w.n_tiles, w.sync,
+                              w.n_sync, w.status, (cudaStream_t)stream));
     return COLI_OK;
 }
 
@@ -338,42 +416,72 @@ static int check_forward_args(const float *x, int n_tok, const float *router_w,
     return COLI_OK;
 }
 
-// The forward body; optionally keeps the h values before requantisation.
-static int forward_impl(const float *x, int n_tok, const float *router_w, const float *router_bias,
-                        const uint8_t *expert_w4, const float *expert_rowscale,
-                        const uint8_t *shared_w4, const float *shared_rowscale, float *out,
-                        cudaStream_t st, float *h_dbg)
+// Argument block of the expert kernel for the configured shape.
+static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *shared_rowscale)
 {
     const coli_moe_shape &s = g.s;
     Workspace &w = g.ws;
-    const int T = n_tok, H = s.hidden, F = s.ffn, E = s.n_experts, k = s.top_k;
-    const int P = T * k;
-
-    LAUNCH_OK(launch_q8_0(x, (long)T * H, w.qx, w.dx, st));
-    LAUNCH_OK(launch_router_logits(x, T, H, router_w, E, w.logits, st));
-    LAUNCH_OK(launch_topk(w.logits, T, E, k, router_bias, s.routed_scale, w.idx, w.wts, st));
-    LAUNCH_OK(launch_dispatch(w.idx, T, k, E, w.counts, w.offsets, w.perm, w.inv, w.pos_token,
-                              w.tile_expert, w.tile_pos0, w.tile_m, w.n_tiles, w.status, st));
-
     ExpertArgs a{};
-    a.H = H; a.F = F; a.E = E; a.k = k; a.n_tok = T; a.P = P;
-    a.expert_w4 = expert_w4; a.expert_rs = expert_rowscale;
-    a.shared_w4 = shared_w4; a.shared_rs = shared_rowscale;
+    a.H = s.hidden; a.F = s.ffn; a.E = s.n_experts; a.k = s.top_k;
+    a.n_tok = T; a.P = T * s.top_k;
+    a.KC = stage_kc(s.hidden, s.ffn);
+    a.gate_up_only = 0;
+    a.expert_rs = expert_rowscale; a.shared_rs = shared_rowscale;
     a.qx = w.qx; a.dx = w.dx; a.pos_token = w.pos_token;
     a.tile_expert = w.tile_expert; a.tile_pos0 = w.tile_pos0; a.tile_m = w.tile_m;
     a.n_tiles = w.n_tiles;
-    a.qh = w.qh; a.dh = w.dh; a.h_dbg = h_dbg; a.y = w.y; a.status = w.status;
+    a.inv = w.inv; a.wts = w.wts;
+    a.qh = w.qh; a.dh = w.dh; a.h_dbg = nullptr; a.y = w.y; a.out = nullptr;
+    a.g_done = w.sync;
+    a.w_done = w.sync + g.max_tiles;
+    a.work_counter = w.sync + g.max_tiles + s.hidden / 64;
+    a.status = w.status;
+    return a;
+}
 
+// The forward body.
+static int forward_impl(const float *x, int n_tok, const float *router_w, const float *router_bias,
+                        const uint8_t *expert_w4, const float *expert_rowscale,
+                        const uint8_t *shared_w4, const float *shared_rowscale, float *out,
+                        cudaStream_t st)
+{
+    const coli_moe_shape &s = g.s;
+    Workspace &w = g.ws;
+    const int T = n_tok, H = s.hidden, E = s.n_experts, k = s.top_k;
+
+    ExpertMaps maps;
+    if (!expert_maps(expert_w4, E, shared_w4, &maps)) return COLI_E_CUDA;
+
+    if (T <= ROUTE_SMALL_MAX_T) {
+        RouteArgs r{};
+        r.x = x; r.T = T; r.H = H; r.E = E; r.k = k; r.routed_scale = s.routed_scale;
+        r.W = router_w; r.bias = router_bias;
+        r.qx = w.qx; r.dx = w.dx; r.logits = w.logits; r.idx = w.idx; r.wts = w.wts;
+        r.counts = w.counts; r.offsets = w.offsets; r.perm = w.perm; r.inv = w.inv;
+        r.pos_token = w.pos_token;
+        r.tile_expert = w.tile_expert; r.tile_pos0 = w.tile_pos0; r.tile_m = w.tile_m;
+        r.n_tiles = w.n_tiles; r.sync = w.sync; r.n_sync = w.n_sync;
+        r.route_counter = w.route_counter; r.status = w.status;
+        LAUNCH_OK(launch_route_small(r, st));
+    } else {
+        LAUNCH_OK(launch_q8_0(x, (long)T * H, w.qx, w.dx, st));
+        LAUNCH_OK(launch_router_logits(x, T, H, router_w, E, w.logits, st));
+        LAUNCH_OK(launch_topk(w.logits, T, E, k, router_bias, s.routed_scale, w.idx, w.wts, st));
+        LAUNCH_OK(launch_dispatch(w.idx, T, k, E, w.counts, w.offsets, w.perm, w.inv, w.pos_token,
+                                  w.tile_expert, w.tile_pos0, w.tile_m, w.n_tiles, w.sync, w.n_sync,
+                                  w.status, st));
+    }
+
+    ExpertArgs a = expert_args(T, expert_rowscale, shared_rowscale);
+    a.out = out;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (g.timing) {
         int r = timing_events(&e0, &e1);
         if (r != COLI_OK) return r;
         CUDA_OK(cudaEventRecord(e0, st));
     }
-    LAUNCH_OK(launch_gateup_gemv(a, g.num_sms, st));
-    LAUNCH_OK(launch_down_gemv(a, g.num_sms, st));
+    LAUNCH_OK(launch_experts(maps, a, g.num_sms, st));
     if (g.timing) CUDA_OK(cudaEventRecord(e1, st));
-    LAUNCH_OK(launch_combine(w.y, w.inv, w.wts, T, k, H, P, out, st));
     return COLI_OK;
 }
 
@@ -386,7 +494,7 @@ int coli_moe_layer_forward(const float *x, int n_tok, const float *router_w,
                                 shared_w4, shared_rowscale, out);
     if (st != COLI_OK || n_tok == 0) return st;
     return forward_impl(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
-                        shared_rowscale, out, (cudaStream_t)stream, nullptr);
+                        shared_rowscale, out, (cudaStream_t)stream);
 }
 
 int coli_moe_layer_forward_hostio(const float *x_host, int n_tok, const float *router_w,
@@ -403,7 +511,7 @@ int coli_moe_layer_forward_hostio(const float *x_host, int n_tok, const float *r
     const size_t bytes = (size_t)n_tok * g.s.hidden * sizeof(float);
     CUDA_OK(cudaMemcpyAsync(g.ws.x_io, x_host, bytes, cudaMemcpyHostToDevice, s));
     st = forward_impl(g.ws.x_io, n_tok, router_w, router_bias, expert_w4, expert_rowscale,
-                      shared_w4, shared_rowscale, g.ws.out_io, s, nullptr);
+                      shared_w4, shared_rowscale, g.ws.out_io, s);
     if (st != COLI_OK) return st;
     CUDA_OK(cudaMemcpyAsync(out_host, g.ws.out_io, bytes, cudaMemcpyDeviceToHost, s));
     CUDA_OK(cudaStreamSynchronize(s));
@@ -422,7 +530,7 @@ int coli_moe_dbg_forward_intermediates(const float *x, int n_tok, const float *r
     if (st != COLI_OK || n_tok == 0) return st;
     cudaStream_t s = (cudaStream_t)stream;
     st = forward_impl(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
-                      shared_rowscale, out, s, nullptr);
+                      shared_rowscale, out, s);
     if (st != COLI_OK) return st;
     const coli_moe_shape &sh = g.s;
     Workspace &w = g.ws;
@@ -448,16 +556,19 @@ int coli_moe_dbg_expert_hidden(const uint8_t *ew4, const float *ers, const int8_
     if (!aligned16(ew4) || !aligned16(qx)) return COLI_E_INVAL;
     cudaStream_t st = (cudaStream_t)stream;
     Workspace &w = g.ws;
+    ExpertMaps maps;
+    if (!expert_maps(ew4, 1, ew4, &maps)) return COLI_E_CUDA;
     LAUNCH_OK(launch_single_expert_tiles(n, w.pos_token, w.tile_expert, w.tile_pos0, w.tile_m,
-                                         w.n_tiles, st));
-    ExpertArgs a{};
-    a.H = s.hidden; a.F = s.ffn; a.E = 1; a.k = 1; a.n_tok = n; a.P = 0;
-    a.expert_w4 = ew4; a.expert_rs = ers; a.shared_w4 = ew4; a.shared_rs = ers;
-    a.qx = qx; a.dx = dx; a.pos_token = w.pos_token;
-    a.tile_expert = w.tile_expert; a.tile_pos0 = w.tile_pos0; a.tile_m = w.tile_m;
-    a.n_tiles = w.n_tiles;
-    a.qh = qh; a.dh = dh; a.h_dbg = h; a.y = w.y; a.status = w.status;
-    LAUNCH_OK(launch_gateup_gemv(a, g.num_sms, st));
+                                         w.n_tiles, w.sync, w.n_sync, st));
+    ExpertArgs a = expert_args(n, ers, ers);
+    a.E = 1;   // the one expert is tile expert 0, read through the routed map
+    a.k = 1;
+    a.P = 0;
+    a.qx = qx; a.dx = dx;
+    a.qh = qh; a.dh = dh; a.h_dbg = h;
+    a.gate_up_only = 1;
+    LAUNCH_OK(launch_experts(maps, a, g.num_sms, st));
+    g.maps_valid = false;   // the maps above describe a single expert
     return COLI_OK;
 }
 

@@ -1,0 +1,408 @@
+// k_experts.cu -- persistent expert kernel: gate/up with SiLU*up and Q8_0
+// requantisation of h, down, and the gate-weighted combine, in one launch.
+//
+// Method (int4 weights x Q8_0 int8 activations, int32 per 32-block, then F32
+// scaling; SwiGLU experts plus a shared expert): "colibri: a pure-C inference
+// engine ..." (discuss.pytorch.kr), section "Key features"; "Open-source engine
+// that ran 744B GLM-5.2 on a 25GB-RAM laptop" (jeff.news), section "Attention
+// and kernels"; "Colibri: an AI engine running a 744B model in 25GB of RAM"
+// (alphamatch.ai), section "Optimised integer kernels".
+//
+// Structure (one CTA per SM, 8 consumer warps + 1 producer warp):
+//   * Work units, claimed in increasing order from a global counter by the
+//     producer: first every gate/up unit (a tile of <= GEMV_MT tokens of one
+//     expert x 32 hidden units = 32 gate rows + 32 up rows), then every down
+//     unit (a tile x 64 output rows).
+//   * The producer streams each unit's weights through a ring of NSTAGE
+//     shared-memory stages with 3-D TMA tile loads (box = rows x 128 bytes of
+//     one expert, 128-byte swizzle, L2 evict-first); each stage completes on
+//     its mbarrier, consumers release it through a second mbarrier.
+//   * Consumers: 4 lanes per weight row, 2 blocks of 32 weights per lane per
+//     stage; dp4a block dots; the per-row F32 accumulation runs in block order
+//     (acc = fma(d_b, I_b, acc) for b ascending) on the row's first lane.
+//   * A down unit needs the h codes of its whole tile: it waits (bounded) on
+//     the tile's gate/up completion counter.  The last down unit to finish a
+//     64-row chunk (over all tiles) combines that chunk of the output.
+// Counters are zeroed by the dispatch step that precedes the launch.
+#include <cuda.h>
+
+#include "coli_common.cuh"
+#include "coli_internal.h"
+#include "tma.cuh"
+
+namespace coli {
+
+constexpr int NSTAGE = 12;
+constexpr int STAGE_ROWS = 64;
+constexpr int KC_MAX = 128;
+constexpr int STAGE_BYTES = STAGE_ROWS * KC_MAX;   // 8 KB
+constexpr int CONSUMER_WARPS = 8;
+constexpr int CONSUMERS = CONSUMER_WARPS * 32;
+constexpr int EXPERT_THREADS = CONSUMERS + 32;
+constexpr int BAR_CONSUMERS = 1;                   // named barrier id (0 = __syncthreads)
+constexpr uint64_t WAIT_NS = 2000000000ull;        // 2 s bound on every wait
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > WAIT_NS) return false;
+    }
+}
+
+struct ExpertSmem {
+    int stage_unit[NSTAGE];
+    int stage_k[NSTAGE];
+    int abort;
+    int combine;
+    int tok[GEMV_MT];
+    alignas(8) uint64_t full[NSTAGE];
+    alignas(8) uint64_t empty[NSTAGE];
+};
+
+size_t experts_smem_bytes(int H, int F)
+{
+    const int NB = (H > F ? H : F) / 32;
+    size_t act = (size_t)GEMV_MT * NB * (16 + 16 + 4 + 4);
+    size_t red = (size_t)GEMV_MT * 64 * 4;
+    return 1024 /*align slack*/ + (size_t)NSTAGE * STAGE_BYTES + act + red + sizeof(ExpertSmem);
+}
+
+// Split-form activations of one tile into shared memory (see block_dot).
+__device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const float *__restrict__ d,
+                                           int K, int m, const int *rows, int row_limit,
+                                           uint4 *xlo, uint4 *xhi, int *xcb, float *xd, int *status)
+{
+    const int NB = K / 32;
+    for (int i = threadIdx.x; i < GEMV_MT * NB; i += CONSUMERS) {
+        const int t = i / NB, b = i - t * NB;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        int sum = 0;
+        float dd = 0.0f;
+        if (t < m) {
+            const int row = rows[t];
+            if (row >= 0 && row < row_limit) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(q + (size_t)row * K + (size_t)b * 32);
+                split_block(__ldcg(src), __ldcg(src + 1), &lo, &hi, &sum);
+                dd = __ldcg(d + (size_t)row * NB + b);
+            } else {
+                set_status(status, ST_BAD_INDEX);
+            }
+        }
+        xlo[i] = lo;
+        xhi[i] = hi;
+        xcb[i] = MAGIC_I - 8 * sum;
+        xd[i] = dd;
+    }
+}
+
+// Integer dot of a block with the low and high nibbles accumulated apart:
+// the high nibbles are used in place (16 x nibble), so no shifts are needed.
+__device__ __forceinline__ int block_dot_i(uint4 w, uint4 lo, uint4 hi, int cb)
+{
+    int a = cb, h = 0;
+    a = dp4a_us(w.x & 0x0F0F0F0Fu, (int)lo.x, a);
+    h = dp4a_us(w.x & 0xF0F0F0F0u, (int)hi.x, h);
+    a = dp4a_us(w.y & 0x0F0F0F0Fu, (int)lo.y, a);
+    h = dp4a_us(w.y & 0xF0F0F0F0u, (int)hi.y, h);
+    a = dp4a_us(w.z & 0x0F0F0F0Fu, (int)lo.z, a);
+    h = dp4a_us(w.z & 0xF0F0F0F0u, (int)hi.z, h);
+    a = dp4a_us(w.w & 0x0F0F0F0Fu, (int)lo.w, a);
+    h = dp4a_us(w.w & 0xF0F0F0F0u, (int)hi.w, h);
+    return a + (h >> 4);     // = sum(nibble * x) - 8 * sum(x), exactly
+}
+
+__global__ void __launch_bounds__(EXPERT_THREADS, 1)
+k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *ring = smem;
+    const int NBmax = (a.H > a.F ? a.H : a.F) / 32;
+    uint4 *xlo = reinterpret_cast<uint4 *>(ring + NSTAGE * STAGE_BYTES);
+    uint4 *xhi = xlo + GEMV_MT * NBmax;
+    int *xcb = reinterpret_cast<int *>(xhi + GEMV_MT * NBmax);
+    float *xd = reinterpret_cast<float *>(xcb + GEMV_MT * NBmax);
+    float *red = xd + GEMV_MT * NBmax;
+    ExpertSmem &S = *reinterpret_cast<ExpertSmem *>(red + GEMV_MT * 64);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, F = a.F, KC = a.KC;
+    const int G = F / 32, CH = H / 64;
+    const int n_tiles = *a.n_tiles;
+    const long n_gu = (long)n_tiles * G;
+    const long total = a.gate_up_only ? n_gu : n_gu + (long)n_tiles * CH;
+    const int nst_gu = (H / 2) / KC, nst_dn = (F / 2) / KC;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], CONSUMER_WARPS);
+        }
+        S.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == CONSUMER_WARPS) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            prefetch_tmap(&maps.gu);
+            prefetch_tmap(&maps.dn);
+            prefetch_tmap(&maps.sgu);
+            prefetch_tmap(&maps.sdn);
+            const uint64_t pol = policy_evict_first();
+            long it = 0;
+            bool ok = true;
+            for (;;) {
+                const long u = atomicAdd(a.work_counter, 1);
+                const bool done = u >= total;
+                const bool gu = !done && u < n_gu;
+                int nst = done ? 1 : (gu ? nst_gu : nst_dn);
+                int e = 0, y0 = 0, tile = 0;
+                if (!done) {
+                    long v = gu ? u : u - n_gu;
+                    tile = (int)(gu ? v / G : v / CH);
+                    const int j = (int)(gu ? v - (long)tile * G : v - (long)tile * CH);
+                    e = a.tile_expert[tile];
+                    y0 = gu ? 32 * j : 64 * j;
+                }
+                const bool shared = (e == a.E);
+                for (int s = 0; s < nst; ++s, ++it) {
+                    const int slot = (int)(it % NSTAGE);
+                    const uint32_t round = (uint32_t)(it / NSTAGE);
+                    if (round > 0 && !mbar_wait_bounded(&S.empty[slot], (round - 1) & 1)) {
+                        set_status(a.status, ST_TIMEOUT);
+                        ok = false;
+                    }
+                    if (ok && S.abort) ok = false;
+                    if (done || !ok) {
+                        S.stage_unit[slot] = -1;
+                        mbar_arrive(&S.full[slot]);
+                        break;
+                    }
+                    S.stage_unit[slot] = (int)u;
+                    S.stage_k[slot] = s;
+                    unsigned char *dst = ring + slot * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&S.full[slot], STAGE_ROWS * KC);
+                    const int x = s * KC;
+                    if (gu) {
+                        const void *m = shared ? (const void *)&maps.sgu : (const void *)&maps.gu;
+                        const int z = shared ? 0 : e;
+                        tma_load_3d(dst, m, x, y0, z, &S.full[slot], pol);
+                        tma_load_3d(dst + 32 * KC, m, x, F + y0, z, &S.full[slot], pol);
+                    } else {
+                        const void *m = shared ? (const void *)&maps.sdn : (const void *)&maps.dn;
+                        tma_load_3d(dst, m, x, y0, shared ? 0 : e, &S.full[slot], pol);
+                    }
+                }
+                if (done || !ok) break;
+            }
+        }
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    const int r = 8 * warp + (lane >> 2);     // weight row of the stage owned by this lane's quad
+    const int q = lane & 3;
+    const int BPR = KC / 16;                  // 32-weight blocks per row per stage (8 or 4)
+    const int BPL = BPR / 4;                  // blocks per lane (2 or 1)
+    const bool swz = (KC == 128);
+
+    long it = 0;
+    float acc[GEMV_MT];
+    int tile = 0, m = 0, pos0 = 0, e = 0, j = 0, nst = 0;
+    bool gu = true;
+    const float *ers = nullptr;
+
+    for (;;) {
+        const int slot = (int)(it % NSTAGE);
+        const uint32_t round = (uint32_t)(it / NSTAGE);
+        if (!mbar_wait_bounded(&S.full[slot], round & 1)) {
+            set_status(a.status, ST_TIMEOUT);
+            S.abort = 1;
+            break;
+        }
+        const int u = S.stage_unit[slot];
+        const int s = S.stage_k[slot];
+        if (u < 0) break;
+        if (s == 0) {
+            // new unit: decode it and stage the activations of its tile
+            gu = u < n_gu;
+            const long v = gu ? u : u - n_gu;
+            tile = (int)(gu ? v / G : v / CH);
+            j = (int)(gu ? v - (long)tile * G : v - (long)tile * CH);
+            e = a.tile_expert[tile];
+            pos0 = a.tile_pos0[tile];
+            m = a.tile_m[tile];
+            nst = gu ? nst_gu : nst_dn;
+            ers = (e == a.E) ? a.shared_rs : a.expert_rs + (size_t)e * (2 * F + H);
+            if (threadIdx.x == 0) {
+                if (!gu) {
+                    // down needs the whole tile's h codes
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire_gpu(&a.g_done[tile]) < G) {
+                        if (globaltimer() - t0 > WAIT_NS) {
+                            set_status(a.status, ST_TIMEOUT);
+                            break;
+                        }
+                        nanosleep_ns(64);
+                    }
+                }
+                for (int t = 0; t < GEMV_MT; ++t)
+                    S.tok[t] = (t < m) ? (gu ? a.pos_token[pos0 + t] : pos0 + t) : 0;
+            }
+            named_barrier(BAR_CONSUMERS, CONSUMERS);
+            if (gu)
+                stage_acts(a.qx, a.dx, H, m, S.tok, a.n_tok, xlo, xhi, xcb, xd, a.status);
+            else
+                stage_acts(a.qh, a.dh, F, m, S.tok, a.P + a.n_tok, xlo, xhi, xcb, xd, a.status);
+            named_barrier(BAR_CONSUMERS, CONSUMERS);
+#pragma unroll
+            for (int t = 0; t < GEMV_MT; ++t) acc[t] = 0.0f;
+        }
+
+        // ---- one stage: rows r of the unit, K-chunk s ----
+        const int NB = gu ? H / 32 : F / 32;
+        const int b0 = s * BPR;
+        const unsigned char *rowp = ring + slot * STAGE_BYTES + r * KC;
+        uint4 wv[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (i < BPL) {
+                const int blk = q * BPL + i;
+                const int phys = swz ? (blk ^ (r & 7)) : blk;
+                wv[i] = *reinterpret_cast<const uint4 *>(rowp + phys * 16);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < GEMV_MT; ++t) {
+            if (t < m) {
+                int I[2] = {0, 0};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    if (i < BPL) {
+                        const int b = t * NB + b0 + q * BPL + i;
+                        I[i] = block_dot_i(wv[i], xlo[b], xhi[b], xcb[b]) - MAGIC_I;
+                    }
+                }
+                // |I| <= 8 * 127 * 32 < 2^15: two codes travel in one word
+                const int pk = (BPL == 2) ? (int)(((unsigned)I[0] & 0xFFFFu) | ((unsigned)I[1] << 16)) : I[0];
+                const int v1 = __shfl_down_sync(FULL, pk, 1);
+                const int v2 = __shfl_down_sync(FULL, pk, 2);
+                const int v3 = __shfl_down_sync(FULL, pk, 3);
+                if (q == 0) {
+                    const float *dt = xd + t * NB + b0;
+                    float c = acc[t];
+                    if (BPL == 2) {
+                        const int w4[4] = {pk, v1, v2, v3};
+#pragma unroll
+                        for (int l = 0; l < 4; ++l) {
+                            const int lo = (int)(short)(w4[l] & 0xFFFF);
+                            const int hi = w4[l] >> 16;
+                            c = __fmaf_rn(dt[2 * l], (float)lo, c);
+                            c = __fmaf_rn(dt[2 * l + 1], (float)hi, c);
+                        }
+                    } else {
+                        c = __fmaf_rn(dt[0], (float)pk, c);
+                        c = __fmaf_rn(dt[1], (float)v1, c);
+                        c = __fmaf_rn(dt[2], (float)v2, c);
+                        c = __fmaf_rn(dt[3], (float)v3, c);
+                    }
+                    acc[t] = c;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+        ++it;
+        if (s != nst - 1) continue;
+
+        // ---- unit epilogue ----
+        if (gu) {
+            if (q == 0)
+                for (int t = 0; t < m; ++t) red[t * 64 + r] = acc[t];
+            named_barrier(BAR_CONSUMERS, CONSUMERS);
+            if (warp < m) {
+                const int t = warp, i = 32 * j + lane, pos = pos0 + t;
+                const float gg = __fmul_rn(ers[i], red[t * 64 + lane]);
+                const float uu = __fmul_rn(ers[F + i], red[t * 64 + 32 + lane]);
+                const float h = __fmul_rn(__fmul_rn(gg, own_sigmoid(gg)), uu);
+                float dq;
+                const int qv = q8_0_lane(h, &dq);
+                a.qh[(size_t)pos * F + i] = (int8_t)qv;
+                if (lane == 0) a.dh[(size_t)pos * G + j] = dq;
+                if (a.h_dbg) a.h_dbg[(size_t)pos * F + i] = h;
+            }
+            named_barrier(BAR_CONSUMERS, CONSUMERS);
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomic_add_release_gpu(&a.g_done[tile], 1);
+            }
+        } else {
+            const int row = 64 * j + r;
+            if (q == 0)
+                for (int t = 0; t < m; ++t)
+                    a.y[(size_t)(pos0 + t) * H + row] = __fmul_rn(ers[2 * F + row], acc[t]);
+            named_barrier(BAR_CONSUMERS, CONSUMERS);
+            if (threadIdx.x == 0) {
+                __threadfence();
+                const int old = atomic_add_acq_rel_gpu(&a.w_done[j], 1);
+                S.combine = (old == n_tiles - 1);
+            }
+            named_barrier(BAR_CONSUMERS, CONSUMERS);
+            if (S.combine) {
+                // every tile's down rows of this chunk are written: combine them
+                __threadfence();
+                const int T = a.n_tok, k = a.k, P = a.P;
+                for (int i = threadIdx.x; i < T * 64; i += CONSUMERS) {
+                    const int t = i >> 6, col = 64 * j + (i & 63);
+                    float o = __ldcg(a.y + (size_t)(P + t) * H + col);
+                    for (int rr = 0; rr < k; ++rr) {
+                        const int pos = __ldcg(a.inv + (size_t)t * k + rr);
+                        if (pos < 0 || pos >= P) continue;
+                        o = __fmaf_rn(__ldcg(a.wts + (size_t)t * k + rr), __ldcg(a.y + (size_t)pos * H + col), o);
+                    }
+                    a.out[(size_t)t * H + col] = o;
+                }
+            }
+        }
+    }
+
+    // drain: if a wait gave up, wait (bounded) for copies still in flight into
+    // this block's ring before the block exits
+    if (S.abort && threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; ++i) {
+            const int slot = (int)(it % NSTAGE);
+            (void)mbar_wait_bounded(&S.full[slot], (uint32_t)(it / NSTAGE) & 1);
+            ++it;
+        }
+    }
+}
+
+int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
+{
+    static size_t configured = 0;
+    const size_t smem = experts_smem_bytes(a.H, a.F);
+    if (smem != configured) {
+        if (cudaFuncSetAttribute(k_experts, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        configured = smem;
+    }
+    k_experts<<<num_sms, EXPERT_THREADS, smem, st>>>(maps, a);
+    count_launch();
+    return 0;
+}
+
+}  // namespace coli

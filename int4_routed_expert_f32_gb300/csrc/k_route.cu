@@ -113,19 +113,20 @@ int launch_router_logits(const float *x, int T, int H, const float *W, int E, fl
 // ---------------------------------------------------------------------------
 constexpr int MAX_K = 16;
 
-__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int T, int E, int k,
-                                              const float *__restrict__ bias, float scale,
-                                              int32_t *__restrict__ idx, float *__restrict__ w)
+// Top-k of one token's logits by one warp; lane 0 receives the experts in
+// rank order (ce) and their sigma (cs), and returns S = sum of the chosen
+// sigma in rank order.
+__device__ __forceinline__ void warp_topk(const float *logits_row, int E, int k,
+                                          const float *__restrict__ bias, int (&ce)[MAX_K],
+                                          float (&cs)[MAX_K], float *S_out)
 {
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (t >= T) return;
     float sig[8], key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         int e = lane + 32 * i;
         if (e < E) {
-            sig[i] = own_sigmoid(logits[(size_t)t * E + e]);
+            sig[i] = own_sigmoid(__ldcg(logits_row + e));
             key[i] = __fadd_rn(sig[i], bias[e]);
         } else {
             sig[i] = 0.0f;
@@ -134,8 +135,6 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
     }
     unsigned taken = 0;
     float S = 0.0f;
-    int ce[MAX_K];
-    float cs[MAX_K];
 #pragma unroll
     for (int r = 0; r < MAX_K; ++r) {
         if (r < k) {
@@ -168,6 +167,19 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
             S = __fadd_rn(S, bs);
         }
     }
+    *S_out = S;
+}
+
+__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int T, int E, int k,
+                                              const float *__restrict__ bias, float scale,
+                                              int32_t *__restrict__ idx, float *__restrict__ w)
+{
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    int ce[MAX_K];
+    float cs[MAX_K], S;
+    warp_topk(logits + (size_t)t * E, E, k, bias, ce, cs, &S);
     if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < MAX_K; ++r)
@@ -203,21 +215,103 @@ int launch_topk(const float *logits, int T, int E, int k, const float *bias, flo
 constexpr int DISPATCH_THREADS = 1024;
 constexpr int MAX_E = 256;
 
+// Warp 0: exclusive scans of the per-expert counts and tile counts (E <= 256,
+// 8 per lane).  Writes counts/offsets (global), s_base/s_tile0 (shared) and
+// the total tile count (shared experts' tiles first).
+__device__ __forceinline__ void scan_experts(const int *s_cnt, int E, int T, int32_t *counts,
+                                             int32_t *offsets, int *s_base, int *s_tile0,
+                                             int *s_ntiles)
+{
+    const int lane = threadIdx.x & 31;
+    int v[8], nt[8], sum = 0, tsum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int e = lane * 8 + i;
+        v[i] = (e < E) ? s_cnt[e] : 0;
+        nt[i] = (v[i] + GEMV_MT - 1) / GEMV_MT;
+        sum += v[i];
+        tsum += nt[i];
+    }
+    int inc = sum, tinc = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int a = __shfl_up_sync(FULL, inc, o);
+        int b = __shfl_up_sync(FULL, tinc, o);
+        if (lane >= o) { inc += a; tinc += b; }
+    }
+    int run = inc - sum, trun = tinc - tsum;
+    const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int e = lane * 8 + i;
+        if (e < E) {
+            s_base[e] = run;
+            offsets[e] = run;
+            counts[e] = v[i];
+            s_tile0[e] = shared_tiles + trun;
+        }
+        run += v[i];
+        trun += nt[i];
+    }
+    if (lane == 31) {
+        offsets[E] = inc;
+        *s_ntiles = shared_tiles + tinc;
+    }
+}
+
+// All threads of the block: the tile list (shared expert's tiles, then each
+// routed expert's tokens in tiles of GEMV_MT) and pos_token of the shared rows.
+__device__ __forceinline__ void write_tiles(int T, int P, int E, const int *s_cnt, const int *s_tile0,
+                                            const int32_t *offsets_sh, int s_ntiles,
+                                            int32_t *pos_token, int32_t *tile_expert,
+                                            int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles)
+{
+    const int tid = threadIdx.x;
+    for (int t = tid; t < T; t += blockDim.x) pos_token[P + t] = t;
+    const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
+    for (int j = tid; j < shared_tiles; j += blockDim.x) {
+        tile_expert[j] = E;
+        tile_pos0[j] = P + j * GEMV_MT;
+        tile_m[j] = min(GEMV_MT, T - j * GEMV_MT);
+    }
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int cnt = s_cnt[e], t0 = s_tile0[e], off = offsets_sh[e];
+        for (int j = 0; j * GEMV_MT < cnt; ++j) {
+            tile_expert[t0 + j] = e;
+            tile_pos0[t0 + j] = off + j * GEMV_MT;
+            tile_m[t0 + j] = min(GEMV_MT, cnt - j * GEMV_MT);
+        }
+    }
+    if (tid == 0) *n_tiles = s_ntiles;
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch: one block of 1024 threads.  Pair p = t*k + r goes to position
+// offsets[e_p] + #{p' < p : e_p' = e_p} (a stable counting sort, so the
+// tokens of an expert stay in ascending order).  Pairs are ranked 1024 at a
+// time: warp-level match gives the rank inside a warp, a per-(warp, expert)
+// count table scanned across the 32 warps gives the rank inside the chunk,
+// and a running base per expert carries it across chunks.  All integer, no
+// order-dependent atomics.  Also emits pos_token, the tile list, and zeroes
+// the expert kernel's counters.
+// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(DISPATCH_THREADS) k_dispatch(
     const int32_t *__restrict__ idx, int T, int k, int E, int32_t *__restrict__ counts,
     int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
     int32_t *__restrict__ pos_token, int32_t *__restrict__ tile_expert,
     int32_t *__restrict__ tile_pos0, int32_t *__restrict__ tile_m, int32_t *__restrict__ n_tiles,
-    int *status)
+    int *sync, int n_sync, int *status)
 {
     __shared__ int s_cnt[MAX_E];
     __shared__ int s_base[MAX_E];
+    __shared__ int s_off[MAX_E];
     __shared__ int s_wc[32][MAX_E];
     __shared__ int s_tile0[MAX_E];
     __shared__ int s_ntiles;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = T * k;
 
+    for (int i = tid; i < n_sync; i += DISPATCH_THREADS) sync[i] = 0;
     if (tid < MAX_E) s_cnt[tid] = 0;
     __syncthreads();
     for (int p = tid; p < P; p += DISPATCH_THREADS) {
@@ -226,46 +320,9 @@ __global__ void __launch_bounds__(DISPATCH_THREADS) k_dispatch(
         else set_status(status, ST_BAD_INDEX);
     }
     __syncthreads();
-
-    // exclusive scan of the counts (E <= 256: 8 per lane of warp 0), and of the
-    // per-expert tile counts
-    if (warp == 0) {
-        int v[8], nt[8], sum = 0, tsum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int e = lane * 8 + i;
-            v[i] = (e < E) ? s_cnt[e] : 0;
-            nt[i] = (v[i] + GEMV_MT - 1) / GEMV_MT;
-            sum += v[i];
-            tsum += nt[i];
-        }
-        int inc = sum, tinc = tsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int a = __shfl_up_sync(FULL, inc, o);
-            int b = __shfl_up_sync(FULL, tinc, o);
-            if (lane >= o) { inc += a; tinc += b; }
-        }
-        int run = inc - sum, trun = tinc - tsum;
-        const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int e = lane * 8 + i;
-            if (e < E) {
-                s_base[e] = run;
-                offsets[e] = run;
-                counts[e] = v[i];
-                s_tile0[e] = shared_tiles + trun;
-            }
-            run += v[i];
-            trun += nt[i];
-        }
-        if (lane == 31) {
-            offsets[E] = inc;
-            s_ntiles = shared_tiles + tinc;
-        }
-    }
+    if (warp == 0) scan_experts(s_cnt, E, T, counts, offsets, s_base, s_tile0, &s_ntiles);
     __syncthreads();
+    if (tid < E) s_off[tid] = s_base[tid];
 
     for (int c0 = 0; c0 < P; c0 += DISPATCH_THREADS) {
         for (int i = tid; i < 32 * MAX_E; i += DISPATCH_THREADS) (&s_wc[0][0])[i] = 0;
@@ -299,39 +356,158 @@ __global__ void __launch_bounds__(DISPATCH_THREADS) k_dispatch(
         if (tid < E) s_base[tid] += chunk_total;
         __syncthreads();
     }
-
-    for (int t = tid; t < T; t += DISPATCH_THREADS) pos_token[P + t] = t;
-    const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
-    for (int j = tid; j < shared_tiles; j += DISPATCH_THREADS) {
-        tile_expert[j] = E;
-        tile_pos0[j] = P + j * GEMV_MT;
-        tile_m[j] = min(GEMV_MT, T - j * GEMV_MT);
-    }
-    if (tid < E) {
-        const int e = tid, cnt = s_cnt[e], t0 = s_tile0[e], off = offsets[e];
-        for (int j = 0; j * GEMV_MT < cnt; ++j) {
-            tile_expert[t0 + j] = e;
-            tile_pos0[t0 + j] = off + j * GEMV_MT;
-            tile_m[t0 + j] = min(GEMV_MT, cnt - j * GEMV_MT);
-        }
-    }
-    if (tid == 0) *n_tiles = s_ntiles;
+    write_tiles(T, P, E, s_cnt, s_tile0, s_off, s_ntiles, pos_token, tile_expert, tile_pos0,
+                tile_m, n_tiles);
 }
 
 int launch_dispatch(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets,
                     int32_t *perm, int32_t *inv, int32_t *pos_token, int32_t *tile_expert,
-                    int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles, int *status,
-                    cudaStream_t st)
+                    int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles, int *sync, int n_sync,
+                    int *status, cudaStream_t st)
 {
     k_dispatch<<<1, DISPATCH_THREADS, 0, st>>>(idx, T, k, E, counts, offsets, perm, inv, pos_token,
-                                               tile_expert, tile_pos0, tile_m, n_tiles, status);
+                                               tile_expert, tile_pos0, tile_m, n_tiles, sync, n_sync,
+                                               status);
+    count_launch();
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Small batches (T <= ROUTE_SMALL_MAX_T) route in a single launch of E blocks:
+// every block quantises a share of x and computes the logits of its expert
+// for all T tokens (same fixed order as k_router_logits); the last block to
+// finish (a completion counter) runs top-k, the stable dispatch of the
+// T*k <= 128 pairs, the tile list, and zeroes the expert kernel's counters.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = ra.T, H = ra.H, E = ra.E, k = ra.k;
+    const int e = blockIdx.x;
+
+    // 1. Q8_0 of x: warps of all blocks share the T*H/32 blocks
+    const long nblk = (long)T * H / 32;
+    for (long blk = (long)blockIdx.x * 8 + warp; blk < nblk; blk += (long)gridDim.x * 8) {
+        float d;
+        const int qv = q8_0_lane(ra.x[blk * 32 + lane], &d);
+        ra.qx[blk * 32 + lane] = (int8_t)qv;
+        if (lane == 0) ra.dx[blk] = d;
+    }
+
+    // 2. logits of expert e for every token
+    float acc[ROUTE_SMALL_MAX_T];
+#pragma unroll
+    for (int t = 0; t < ROUTE_SMALL_MAX_T; ++t) acc[t] = 0.0f;
+    const float4 *w4 = reinterpret_cast<const float4 *>(ra.W + (size_t)e * H);
+    for (int c = tid; c < H / 4; c += 256) {
+        const float4 wv = __ldg(w4 + c);
+#pragma unroll
+        for (int t = 0; t < ROUTE_SMALL_MAX_T; ++t) {
+            if (t < T) {
+                const float4 xv = __ldg(reinterpret_cast<const float4 *>(ra.x + (size_t)t * H) + c);
+                float p = acc[t];
+                p = __fmaf_rn(xv.x, wv.x, p);
+                p = __fmaf_rn(xv.y, wv.y, p);
+                p = __fmaf_rn(xv.z, wv.z, p);
+                p = __fmaf_rn(xv.w, wv.w, p);
+                acc[t] = p;
+            }
+        }
+    }
+    __shared__ float red[ROUTE_SMALL_MAX_T][8];
+#pragma unroll
+    for (int t = 0; t < ROUTE_SMALL_MAX_T; ++t) {
+        if (t < T) {
+            float v = acc[t];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(FULL, v, o));
+            if (lane == 0) red[t][warp] = v;
+        }
+    }
+    __syncthreads();
+    if (tid < T) {
+        float s8[8], tmp[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s8[w] = red[tid][w];
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) tmp[w] = __fadd_rn(s8[w], s8[w ^ o]);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s8[w] = tmp[w];
+        }
+        ra.logits[(size_t)tid * E + e] = s8[0];
+    }
+
+    // 3. the last block routes
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(ra.route_counter, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (tid == 0) *ra.route_counter = 0;
+
+    __shared__ int s_idx[ROUTE_SMALL_MAX_T * MAX_K];
+    __shared__ int s_cnt[MAX_E], s_base[MAX_E], s_tile0[MAX_E], s_off[MAX_E];
+    __shared__ int s_ntiles;
+    for (int i = tid; i < ra.n_sync; i += 256) ra.sync[i] = 0;
+    if (warp < T) {
+        int ce[MAX_K];
+        float cs[MAX_K], S;
+        warp_topk(ra.logits + (size_t)warp * E, E, k, ra.bias, ce, cs, &S);
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < MAX_K; ++r)
+                if (r < k) {
+                    s_idx[warp * k + r] = ce[r];
+                    ra.idx[(size_t)warp * k + r] = ce[r];
+                    ra.wts[(size_t)warp * k + r] = __fmul_rn(__fdiv_rn(cs[r], S), ra.routed_scale);
+                }
+        }
+    }
+    __syncthreads();
+    const int P = T * k;
+    for (int ee = tid; ee < MAX_E; ee += 256) {
+        int c = 0;
+        for (int p = 0; p < P; ++p) c += (s_idx[p] == ee);
+        s_cnt[ee] = (ee < E) ? c : 0;
+    }
+    if (tid < P && (s_idx[tid] < 0 || s_idx[tid] >= E)) set_status(ra.status, ST_BAD_INDEX);
+    __syncthreads();
+    if (warp == 0) scan_experts(s_cnt, E, T, ra.counts, ra.offsets, s_base, s_tile0, &s_ntiles);
+    __syncthreads();
+    if (tid < E) s_off[tid] = s_base[tid];
+    __syncthreads();
+    if (tid < P) {
+        const int ee = s_idx[tid];
+        if (ee >= 0 && ee < E) {
+            int rank = 0;
+            for (int p = 0; p < tid; ++p) rank += (s_idx[p] == ee);
+            const int pos = s_off[ee] + rank;
+            ra.perm[pos] = tid;
+            ra.inv[tid] = pos;
+            ra.pos_token[pos] = tid / k;
+        } else {
+            ra.inv[tid] = -1;
+        }
+    }
+    write_tiles(T, P, E, s_cnt, s_tile0, s_off, s_ntiles, ra.pos_token, ra.tile_expert,
+                ra.tile_pos0, ra.tile_m, ra.n_tiles);
+}
+
+int launch_route_small(const RouteArgs &r, cudaStream_t st)
+{
+    k_route_small<<<r.E, 256, 0, st>>>(r);
     count_launch();
     return 0;
 }
 
 // Tile list for a single expert (index 0) over positions 0..n-1.
 __global__ void k_single_expert_tiles(int n, int32_t *pos_token, int32_t *tile_expert,
-                                      int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles)
+                                      int32_t *tile_pos0, int32_t *tile_m, int32_t *n_tiles,
+                                      int *sync, int n_sync)
 {
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) pos_token[i] = i;
@@ -341,14 +517,16 @@ __global__ void k_single_expert_tiles(int n, int32_t *pos_token, int32_t *tile_e
         tile_pos0[i] = i * GEMV_MT;
         tile_m[i] = min(GEMV_MT, n - i * GEMV_MT);
     }
+    for (int j = i; j < n_sync; j += gridDim.x * blockDim.x) sync[j] = 0;
     if (i == 0) *n_tiles = nt;
 }
 
 int launch_single_expert_tiles(int n, int32_t *pos_token, int32_t *tile_expert, int32_t *tile_pos0,
-                               int32_t *tile_m, int32_t *n_tiles, cudaStream_t st)
+                               int32_t *tile_m, int32_t *n_tiles, int *sync, int n_sync,
+                               cudaStream_t st)
 {
     k_single_expert_tiles<<<(n + 255) / 256, 256, 0, st>>>(n, pos_token, tile_expert, tile_pos0,
-                                                          tile_m, n_tiles);
+                                                          tile_m, n_tiles, sync, n_sync);
     count_launch();
     return 0;
 }
