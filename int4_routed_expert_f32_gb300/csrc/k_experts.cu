@@ -9,17 +9,20 @@
 // (alphamatch.ai), section "Optimised integer kernels".
 //
 // Structure (one CTA per SM, 8 consumer warps + 1 producer warp):
-//   * Work units, claimed in increasing order from a global counter by the
-//     producer: first every gate/up unit (a tile of <= GEMV_MT tokens of one
+//   * Work units: every gate/up unit (a tile of <= GEMV_MT tokens of one
 //     expert x 32 hidden units = 32 gate rows + 32 up rows), then every down
-//     unit (a tile x 64 output rows).
+//     unit (a tile x 64 output rows).  Each block takes a contiguous share of
+//     the gate/up units and then of the down units (a static schedule known to
+//     producer and consumers alike).
 //   * The producer streams each unit's weights through a ring of NSTAGE
-//     shared-memory stages with 3-D TMA tile loads (box = rows x 128 bytes of
-//     one expert, 128-byte swizzle, L2 evict-first); each stage completes on
-//     its mbarrier, consumers release it through a second mbarrier.
-//   * Consumers: 4 lanes per weight row, 2 blocks of 32 weights per lane per
-//     stage; dp4a block dots; the per-row F32 accumulation runs in block order
-//     (acc = fma(d_b, I_b, acc) for b ascending) on the row's first lane.
+//     shared-memory stages with 3-D TMA tile loads.  A stage holds 64 weight
+//     rows x NSUB sub-chunks of 128 bytes (256 weights) each; a sub-chunk is
+//     one swizzled TMA box (128-byte swizzle), L2 evict-first.  Each stage
+//     completes on its mbarrier; consumers release it through a second one.
+//   * Consumers: a quad of lanes per weight row, lane q of the quad owns
+//     sub-chunk q (8 blocks of 32 weights); dp4a block dots.  The F32
+//     accumulation of the row runs in block order (acc = fma(d_b, I_b, acc),
+//     b ascending): lane 0 folds its 8 blocks, hands acc to lane 1, and so on.
 //   * A down unit needs the h codes of its whole tile: it waits (bounded) on
 //     the tile's gate/up completion counter.  The last down unit to finish a
 //     64-row chunk (over all tiles) combines that chunk of the output.
@@ -32,10 +35,12 @@
 
 namespace coli {
 
-constexpr int NSTAGE = 12;
+constexpr int NSTAGE = 4;
 constexpr int STAGE_ROWS = 64;
 constexpr int KC_MAX = 128;
-constexpr int STAGE_BYTES = STAGE_ROWS * KC_MAX;   // 8 KB
+constexpr int NSUB_MAX = 4;
+constexpr int SUB_BYTES = STAGE_ROWS * KC_MAX;      // 8 KB: one sub-chunk of 64 rows
+constexpr int STAGE_BYTES = NSUB_MAX * SUB_BYTES;   // 32 KB
 constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
 constexpr int EXPERT_THREADS = CONSUMERS + 32;
@@ -61,8 +66,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 }
 
 struct ExpertSmem {
-    int stage_unit[NSTAGE];
-    int stage_k[NSTAGE];
     int abort;
     int combine;
     int tok[GEMV_MT];
@@ -122,6 +125,9 @@ __device__ __forceinline__ int block_dot_i(uint4 w, uint4 lo, uint4 hi, int cb)
     return a + (h >> 4);     // = sum(nibble * x) - 8 * sum(x), exactly
 }
 
+// Largest of 4, 2, 1 dividing n.
+__device__ __forceinline__ int nsub_for(int n) { return (n % 4 == 0) ? 4 : (n % 2 == 0) ? 2 : 1; }
+
 __global__ void __launch_bounds__(EXPERT_THREADS, 1)
 k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 {
@@ -141,9 +147,14 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const int H = a.H, F = a.F, KC = a.KC;
     const int G = F / 32, CH = H / 64;
     const int n_tiles = *a.n_tiles;
-    const long n_gu = (long)n_tiles * G;
-    const long total = a.gate_up_only ? n_gu : n_gu + (long)n_tiles * CH;
-    const int nst_gu = (H / 2) / KC, nst_dn = (F / 2) / KC;
+    // sub-chunks per stage and stages per unit, for gate/up (K = H) and down (K = F)
+    const int nsub_gu = nsub_for((H / 2) / KC), nsub_dn = nsub_for((F / 2) / KC);
+    const int nst_gu = (H / 2) / (KC * nsub_gu), nst_dn = (F / 2) / (KC * nsub_dn);
+    // static schedule: this block's share of the gate/up units, then of the down units
+    const long NG = (long)n_tiles * G, NW = a.gate_up_only ? 0 : (long)n_tiles * CH;
+    const long g0 = NG * blockIdx.x / gridDim.x, g1 = NG * (blockIdx.x + 1) / gridDim.x;
+    const long w0 = NW * blockIdx.x / gridDim.x, w1 = NW * (blockIdx.x + 1) / gridDim.x;
+    const long n_units = (g1 - g0) + (w1 - w0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -164,50 +175,38 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             prefetch_tmap(&maps.sdn);
             const uint64_t pol = policy_evict_first();
             long it = 0;
-            bool ok = true;
-            for (;;) {
-                const long u = atomicAdd(a.work_counter, 1);
-                const bool done = u >= total;
-                const bool gu = !done && u < n_gu;
-                int nst = done ? 1 : (gu ? nst_gu : nst_dn);
-                int e = 0, y0 = 0, tile = 0;
-                if (!done) {
-                    long v = gu ? u : u - n_gu;
-                    tile = (int)(gu ? v / G : v / CH);
-                    const int j = (int)(gu ? v - (long)tile * G : v - (long)tile * CH);
-                    e = a.tile_expert[tile];
-                    y0 = gu ? 32 * j : 64 * j;
-                }
+            for (long i = 0; i < n_units && !S.abort; ++i) {
+                const bool gu = i < g1 - g0;
+                const long v = gu ? g0 + i : w0 + (i - (g1 - g0));
+                const int tile = (int)(gu ? v / G : v / CH);
+                const int j = (int)(gu ? v - (long)tile * G : v - (long)tile * CH);
+                const int e = __ldg(a.tile_expert + tile);
                 const bool shared = (e == a.E);
+                const int z = shared ? 0 : e;
+                const int nst = gu ? nst_gu : nst_dn, nsub = gu ? nsub_gu : nsub_dn;
+                const void *m = gu ? (shared ? (const void *)&maps.sgu : (const void *)&maps.gu)
+                                   : (shared ? (const void *)&maps.sdn : (const void *)&maps.dn);
                 for (int s = 0; s < nst; ++s, ++it) {
                     const int slot = (int)(it % NSTAGE);
                     const uint32_t round = (uint32_t)(it / NSTAGE);
                     if (round > 0 && !mbar_wait_bounded(&S.empty[slot], (round - 1) & 1)) {
                         set_status(a.status, ST_TIMEOUT);
-                        ok = false;
-                    }
-                    if (ok && S.abort) ok = false;
-                    if (done || !ok) {
-                        S.stage_unit[slot] = -1;
-                        mbar_arrive(&S.full[slot]);
+                        S.abort = 1;
                         break;
                     }
-                    S.stage_unit[slot] = (int)u;
-                    S.stage_k[slot] = s;
                     unsigned char *dst = ring + slot * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&S.full[slot], STAGE_ROWS * KC);
-                    const int x = s * KC;
-                    if (gu) {
-                        const void *m = shared ? (const void *)&maps.sgu : (const void *)&maps.gu;
-                        const int z = shared ? 0 : e;
-                        tma_load_3d(dst, m, x, y0, z, &S.full[slot], pol);
-                        tma_load_3d(dst + 32 * KC, m, x, F + y0, z, &S.full[slot], pol);
-                    } else {
-                        const void *m = shared ? (const void *)&maps.sdn : (const void *)&maps.dn;
-                        tma_load_3d(dst, m, x, y0, shared ? 0 : e, &S.full[slot], pol);
+                    mbar_arrive_expect_tx(&S.full[slot], STAGE_ROWS * KC * nsub);
+                    for (int c = 0; c < nsub; ++c) {
+                        const int x = (s * nsub + c) * KC;
+                        unsigned char *d = dst + c * SUB_BYTES;
+                        if (gu) {
+                            tma_load_3d(d, m, x, 32 * j, z, &S.full[slot], pol);
+                            tma_load_3d(d + 32 * KC, m, x, F + 32 * j, z, &S.full[slot], pol);
+                        } else {
+                            tma_load_3d(d, m, x, 64 * j, z, &S.full[slot], pol);
+                        }
                     }
                 }
-                if (done || !ok) break;
             }
         }
         return;
@@ -215,53 +214,40 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 
     // -------------------------------- consumers --------------------------------
     const int r = 8 * warp + (lane >> 2);     // weight row of the stage owned by this lane's quad
-    const int q = lane & 3;
-    const int BPR = KC / 16;                  // 32-weight blocks per row per stage (8 or 4)
-    const int BPL = BPR / 4;                  // blocks per lane (2 or 1)
+    const int q = lane & 3;                   // sub-chunk owned by this lane
+    const int BPS = KC / 16;                  // 32-weight blocks per sub-chunk row (8 or 4)
     const bool swz = (KC == 128);
 
     long it = 0;
-    float acc[GEMV_MT];
-    int tile = 0, m = 0, pos0 = 0, e = 0, j = 0, nst = 0;
-    bool gu = true;
-    const float *ers = nullptr;
+    int staged_tile = -1;
+    bool staged_gu = false;
+    for (long i = 0; i < n_units; ++i) {
+        const bool gu = i < g1 - g0;
+        const long v = gu ? g0 + i : w0 + (i - (g1 - g0));
+        const int tile = (int)(gu ? v / G : v / CH);
+        const int j = (int)(gu ? v - (long)tile * G : v - (long)tile * CH);
+        const int e = __ldg(a.tile_expert + tile);
+        const int pos0 = __ldg(a.tile_pos0 + tile);
+        const int m = __ldg(a.tile_m + tile);
+        const int nst = gu ? nst_gu : nst_dn, nsub = gu ? nsub_gu : nsub_dn;
+        const int NB = gu ? H / 32 : F / 32;
+        const float *ers = (e == a.E) ? a.shared_rs : a.expert_rs + (size_t)e * (2 * F + H);
 
-    for (;;) {
-        const int slot = (int)(it % NSTAGE);
-        const uint32_t round = (uint32_t)(it / NSTAGE);
-        if (!mbar_wait_bounded(&S.full[slot], round & 1)) {
-            set_status(a.status, ST_TIMEOUT);
-            S.abort = 1;
-            break;
-        }
-        const int u = S.stage_unit[slot];
-        const int s = S.stage_k[slot];
-        if (u < 0) break;
-        if (s == 0) {
-            // new unit: decode it and stage the activations of its tile
-            gu = u < n_gu;
-            const long v = gu ? u : u - n_gu;
-            tile = (int)(gu ? v / G : v / CH);
-            j = (int)(gu ? v - (long)tile * G : v - (long)tile * CH);
-            e = a.tile_expert[tile];
-            pos0 = a.tile_pos0[tile];
-            m = a.tile_m[tile];
-            nst = gu ? nst_gu : nst_dn;
-            ers = (e == a.E) ? a.shared_rs : a.expert_rs + (size_t)e * (2 * F + H);
+        if (tile != staged_tile || gu != staged_gu) {
+            // activations of the tile: x codes for gate/up, h codes for down
             if (threadIdx.x == 0) {
                 if (!gu) {
-                    // down needs the whole tile's h codes
                     const uint64_t t0 = globaltimer();
                     while (ld_acquire_gpu(&a.g_done[tile]) < G) {
                         if (globaltimer() - t0 > WAIT_NS) {
                             set_status(a.status, ST_TIMEOUT);
                             break;
                         }
-                        nanosleep_ns(64);
+                        nanosleep_ns(32);
                     }
                 }
                 for (int t = 0; t < GEMV_MT; ++t)
-                    S.tok[t] = (t < m) ? (gu ? a.pos_token[pos0 + t] : pos0 + t) : 0;
+                    S.tok[t] = (t < m) ? (gu ? __ldg(a.pos_token + pos0 + t) : pos0 + t) : 0;
             }
             named_barrier(BAR_CONSUMERS, CONSUMERS);
             if (gu)
@@ -269,65 +255,78 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             else
                 stage_acts(a.qh, a.dh, F, m, S.tok, a.P + a.n_tok, xlo, xhi, xcb, xd, a.status);
             named_barrier(BAR_CONSUMERS, CONSUMERS);
-#pragma unroll
-            for (int t = 0; t < GEMV_MT; ++t) acc[t] = 0.0f;
+            staged_tile = tile;
+            staged_gu = gu;
         }
 
-        // ---- one stage: rows r of the unit, K-chunk s ----
-        const int NB = gu ? H / 32 : F / 32;
-        const int b0 = s * BPR;
-        const unsigned char *rowp = ring + slot * STAGE_BYTES + r * KC;
-        uint4 wv[2];
+        float acc[GEMV_MT];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            if (i < BPL) {
-                const int blk = q * BPL + i;
-                const int phys = swz ? (blk ^ (r & 7)) : blk;
-                wv[i] = *reinterpret_cast<const uint4 *>(rowp + phys * 16);
+        for (int t = 0; t < GEMV_MT; ++t) acc[t] = 0.0f;
+        for (int s = 0; s < nst; ++s, ++it) {
+            const int slot = (int)(it % NSTAGE);
+            const uint32_t round = (uint32_t)(it / NSTAGE);
+            if (!mbar_wait_bounded(&S.full[slot], round & 1)) {
+                set_status(a.status, ST_TIMEOUT);
+                S.abort = 1;
+                goto drain;
             }
-        }
+            {
+                // this lane: row r, sub-chunk q -> blocks b0 .. b0 + BPS - 1
+                const bool active = q < nsub;
+                const int b0 = (s * nsub + q) * BPS;
+                const unsigned char *rowp = ring + slot * STAGE_BYTES + q * SUB_BYTES + r * KC;
+                // Visiting order rotated by 2q blocks keeps the four lanes of a
+                // quad on distinct shared-memory banks; wv[jj] / I[jj] hold
+                // block (jj + 2q) mod BPS.
+                const int rot = (2 * q) & (BPS - 1);
+                uint4 wv[8];
 #pragma unroll
-        for (int t = 0; t < GEMV_MT; ++t) {
-            if (t < m) {
-                int I[2] = {0, 0};
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    if (i < BPL) {
-                        const int b = t * NB + b0 + q * BPL + i;
-                        I[i] = block_dot_i(wv[i], xlo[b], xhi[b], xcb[b]) - MAGIC_I;
+                for (int jj = 0; jj < 8; ++jj) {
+                    if (active && jj < BPS) {
+                        const int blk = (jj + rot) & (BPS - 1);
+                        const int phys = swz ? (blk ^ (r & 7)) : blk;
+                        wv[jj] = *reinterpret_cast<const uint4 *>(rowp + phys * 16);
                     }
                 }
-                // |I| <= 8 * 127 * 32 < 2^15: two codes travel in one word
-                const int pk = (BPL == 2) ? (int)(((unsigned)I[0] & 0xFFFFu) | ((unsigned)I[1] << 16)) : I[0];
-                const int v1 = __shfl_down_sync(FULL, pk, 1);
-                const int v2 = __shfl_down_sync(FULL, pk, 2);
-                const int v3 = __shfl_down_sync(FULL, pk, 3);
-                if (q == 0) {
-                    const float *dt = xd + t * NB + b0;
-                    float c = acc[t];
-                    if (BPL == 2) {
-                        const int w4[4] = {pk, v1, v2, v3};
+#pragma unroll
+                for (int t = 0; t < GEMV_MT; ++t) {
+                    if (t < m) {
+                        int I[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            I[jj] = 0;
+                            if (active && jj < BPS) {
+                                const int xb = t * NB + b0 + ((jj + rot) & (BPS - 1));
+                                I[jj] = block_dot_i(wv[jj], xlo[xb], xhi[xb], xcb[xb]) - MAGIC_I;
+                            }
+                        }
+                        // in-order fold across the quad: lane 0, then 1, 2, 3
+                        float c = acc[t];
+                        const float *dt = xd + t * NB + b0;
 #pragma unroll
                         for (int l = 0; l < 4; ++l) {
-                            const int lo = (int)(short)(w4[l] & 0xFFFF);
-                            const int hi = w4[l] >> 16;
-                            c = __fmaf_rn(dt[2 * l], (float)lo, c);
-                            c = __fmaf_rn(dt[2 * l + 1], (float)hi, c);
+                            if (l > 0) c = __shfl_sync(FULL, c, (lane & ~3) | (l - 1));
+                            if (q == l && active) {
+                                // here q == l is a compile-time constant, so is the rotation
+                                if (BPS == 8) {
+#pragma unroll
+                                    for (int b = 0; b < 8; ++b)
+                                        c = __fmaf_rn(dt[b], (float)I[(b - 2 * l) & 7], c);
+                                } else {
+#pragma unroll
+                                    for (int b = 0; b < 4; ++b)
+                                        c = __fmaf_rn(dt[b], (float)I[(b - 2 * l) & 3], c);
+                                }
+                            }
                         }
-                    } else {
-                        c = __fmaf_rn(dt[0], (float)pk, c);
-                        c = __fmaf_rn(dt[1], (float)v1, c);
-                        c = __fmaf_rn(dt[2], (float)v2, c);
-                        c = __fmaf_rn(dt[3], (float)v3, c);
+                        // the quad's last active lane holds the row's running sum
+                        acc[t] = __shfl_sync(FULL, c, (lane & ~3) | (nsub - 1));
                     }
-                    acc[t] = c;
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[slot]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[slot]);
-        ++it;
-        if (s != nst - 1) continue;
 
         // ---- unit epilogue ----
         if (gu) {
@@ -335,15 +334,15 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 for (int t = 0; t < m; ++t) red[t * 64 + r] = acc[t];
             named_barrier(BAR_CONSUMERS, CONSUMERS);
             if (warp < m) {
-                const int t = warp, i = 32 * j + lane, pos = pos0 + t;
-                const float gg = __fmul_rn(ers[i], red[t * 64 + lane]);
-                const float uu = __fmul_rn(ers[F + i], red[t * 64 + 32 + lane]);
+                const int t = warp, ii = 32 * j + lane, pos = pos0 + t;
+                const float gg = __fmul_rn(ers[ii], red[t * 64 + lane]);
+                const float uu = __fmul_rn(ers[F + ii], red[t * 64 + 32 + lane]);
                 const float h = __fmul_rn(__fmul_rn(gg, own_sigmoid(gg)), uu);
                 float dq;
                 const int qv = q8_0_lane(h, &dq);
-                a.qh[(size_t)pos * F + i] = (int8_t)qv;
+                a.qh[(size_t)pos * F + ii] = (int8_t)qv;
                 if (lane == 0) a.dh[(size_t)pos * G + j] = dq;
-                if (a.h_dbg) a.h_dbg[(size_t)pos * F + i] = h;
+                if (a.h_dbg) a.h_dbg[(size_t)pos * F + ii] = h;
             }
             named_barrier(BAR_CONSUMERS, CONSUMERS);
             if (threadIdx.x == 0) {
@@ -366,8 +365,8 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 // every tile's down rows of this chunk are written: combine them
                 __threadfence();
                 const int T = a.n_tok, k = a.k, P = a.P;
-                for (int i = threadIdx.x; i < T * 64; i += CONSUMERS) {
-                    const int t = i >> 6, col = 64 * j + (i & 63);
+                for (int ii = threadIdx.x; ii < T * 64; ii += CONSUMERS) {
+                    const int t = ii >> 6, col = 64 * j + (ii & 63);
                     float o = __ldcg(a.y + (size_t)(P + t) * H + col);
                     for (int rr = 0; rr < k; ++rr) {
                         const int pos = __ldcg(a.inv + (size_t)t * k + rr);
@@ -379,10 +378,12 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             }
         }
     }
+    return;
 
-    // drain: if a wait gave up, wait (bounded) for copies still in flight into
-    // this block's ring before the block exits
-    if (S.abort && threadIdx.x == 0) {
+drain:
+    // a wait gave up: wait (bounded) for copies still in flight into this
+    // block's ring before the block exits
+    if (lane == 0 && warp == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
             const int slot = (int)(it % NSTAGE);
             (void)mbar_wait_bounded(&S.full[slot], (uint32_t)(it / NSTAGE) & 1);
