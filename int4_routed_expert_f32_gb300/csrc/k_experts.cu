@@ -24,8 +24,9 @@
 //     accumulation of the row runs in block order (acc = fma(d_b, I_b, acc),
 //     b ascending): lane 0 folds its 8 blocks, hands acc to lane 1, and so on.
 //   * A down unit needs the h codes of its whole tile: it waits (bounded) on
-//     the tile's gate/up completion counter.  The last down unit to finish a
-//     64-row chunk (over all tiles) combines that chunk of the output.
+//     the tile's gate/up completion counter.  Each 64-row output chunk is
+//     combined by the block that ran the chunk's down unit of the last tile,
+//     after (bounded) waiting for the chunk's down units of the other tiles.
 // Counters are zeroed by the dispatch step that precedes the launch.
 #include <cuda.h>
 
@@ -67,7 +68,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 
 struct ExpertSmem {
     int abort;
-    int combine;
     int tok[GEMV_MT];
     alignas(8) uint64_t full[NSTAGE];
     alignas(8) uint64_t empty[NSTAGE];
@@ -125,9 +125,84 @@ __device__ __forceinline__ int block_dot_i(uint4 w, uint4 lo, uint4 hi, int cb)
     return a + (h >> 4);     // = sum(nibble * x) - 8 * sum(x), exactly
 }
 
+// Integer block dots of one pipeline stage for this lane (row r, sub-chunk q):
+// dst[t][jj] = MAGIC_I + I(block b0 + (jj + rot) mod BPS, token t).  Waits for
+// the stage, and releases it once the dots are done.  False if the wait gave up.
+template <int MT>
+__device__ __forceinline__ bool stage_dots(uint64_t *full, uint64_t *empty, const unsigned char *ring,
+                                           long &it, const int (&woff)[8], const uint4 *xlo,
+                                           const uint4 *xhi, const int *xcb, int sub, int BPS, int rot,
+                                           int NB, int m, bool active, int lane, int (&dst)[MT][8])
+{
+    const int slot = (int)(it % NSTAGE);
+    const uint32_t round = (uint32_t)(it / NSTAGE);
+    if (!mbar_wait_bounded(&full[slot], round & 1)) return false;
+    const unsigned char *base = ring + slot * STAGE_BYTES;
+    uint4 wv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj)
+        if (active && jj < BPS) wv[jj] = *reinterpret_cast<const uint4 *>(base + woff[jj]);
+    const int b0 = sub * BPS;
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        if (t < m) {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                dst[t][jj] = MAGIC_I;
+                if (active && jj < BPS) {
+                    const int xb = t * NB + b0 + ((jj + rot) & (BPS - 1));
+                    dst[t][jj] = block_dot_i(wv[jj], xlo[xb], xhi[xb], xcb[xb]);
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    ++it;
+    return true;
+}
+
+// In-order F32 fold of one stage into acc: lane 0 of the quad folds its
+// sub-chunk's blocks, hands the running sum to lane 1, and so on.  dx points
+// at the scales of the stage's first block (token 0).
+template <int MT>
+__device__ __forceinline__ void stage_fold(const float *dx, int NB, int BPS, int nsub, int m, int q,
+                                           int lane, const int (&src)[MT][8], float (&acc)[MT])
+{
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        if (t < m) {
+            float c = acc[t];
+#pragma unroll
+            for (int l = 0; l < 4; ++l) {
+                if (l > 0) c = __shfl_sync(FULL, c, (lane & ~3) | (l - 1));
+                if (q == l && l < nsub) {
+                    // q == l is a compile-time constant here, so is the rotation
+                    const float *dt = dx + t * NB + l * BPS;
+                    if (BPS == 8) {
+                        const float4 d0 = *reinterpret_cast<const float4 *>(dt);
+                        const float4 d1 = *reinterpret_cast<const float4 *>(dt + 4);
+                        const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                        for (int b = 0; b < 8; ++b)
+                            c = __fmaf_rn(dd[b], __int_as_float(src[t][(b - 2 * l) & 7]) - MAGIC_F, c);
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            c = __fmaf_rn(dt[b], __int_as_float(src[t][(b - 2 * l) & 3]) - MAGIC_F, c);
+                    }
+                }
+            }
+            acc[t] = __shfl_sync(FULL, c, (lane & ~3) | 3);
+        }
+    }
+}
+
 // Largest of 4, 2, 1 dividing n.
 __device__ __forceinline__ int nsub_for(int n) { return (n % 4 == 0) ? 4 : (n % 2 == 0) ? 2 : 1; }
 
+// MT: bound on the tokens of any tile in this launch (1, 2 or 4; <= GEMV_MT).
+template <int MT>
 __global__ void __launch_bounds__(EXPERT_THREADS, 1)
 k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 {
@@ -217,11 +292,21 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const int q = lane & 3;                   // sub-chunk owned by this lane
     const int BPS = KC / 16;                  // 32-weight blocks per sub-chunk row (8 or 4)
     const bool swz = (KC == 128);
+    // Visiting order rotated by 2q blocks keeps the four lanes of a quad on
+    // distinct shared-memory banks: slot jj of this lane holds block (jj + rot).
+    const int rot = (2 * q) & (BPS - 1);
+    int woff[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+        const int blk = (jj + rot) & (BPS - 1);
+        woff[jj] = q * SUB_BYTES + r * KC + 16 * (swz ? (blk ^ (r & 7)) : blk);
+    }
 
     long it = 0;
     int staged_tile = -1;
     bool staged_gu = false;
-    for (long i = 0; i < n_units; ++i) {
+    bool aborted = false;
+    for (long i = 0; i < n_units && !aborted; ++i) {
         const bool gu = i < g1 - g0;
         const long v = gu ? g0 + i : w0 + (i - (g1 - g0));
         const int tile = (int)(gu ? v / G : v / CH);
@@ -232,6 +317,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         const int nst = gu ? nst_gu : nst_dn, nsub = gu ? nsub_gu : nsub_dn;
         const int NB = gu ? H / 32 : F / 32;
         const float *ers = (e == a.E) ? a.shared_rs : a.expert_rs + (size_t)e * (2 * F + H);
+        const bool active = q < nsub;
 
         if (tile != staged_tile || gu != staged_gu) {
             // activations of the tile: x codes for gate/up, h codes for down
@@ -246,7 +332,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                         nanosleep_ns(32);
                     }
                 }
-                for (int t = 0; t < GEMV_MT; ++t)
+                for (int t = 0; t < MT; ++t)
                     S.tok[t] = (t < m) ? (gu ? __ldg(a.pos_token + pos0 + t) : pos0 + t) : 0;
             }
             named_barrier(BAR_CONSUMERS, CONSUMERS);
@@ -259,74 +345,32 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             staged_gu = gu;
         }
 
-        float acc[GEMV_MT];
+        // Software pipeline over the unit's stages: the integer block dots of
+        // stage s+1 are issued next to the in-order F32 fold of stage s, and a
+        // ring slot is released as soon as its integer dots are done.
+        float acc[MT];
+        int Ic[MT][8];   // stage being folded: biased block dots (MAGIC_I + I)
+        int In[MT][8];   // next stage
 #pragma unroll
-        for (int t = 0; t < GEMV_MT; ++t) acc[t] = 0.0f;
-        for (int s = 0; s < nst; ++s, ++it) {
-            const int slot = (int)(it % NSTAGE);
-            const uint32_t round = (uint32_t)(it / NSTAGE);
-            if (!mbar_wait_bounded(&S.full[slot], round & 1)) {
-                set_status(a.status, ST_TIMEOUT);
-                S.abort = 1;
-                goto drain;
-            }
-            {
-                // this lane: row r, sub-chunk q -> blocks b0 .. b0 + BPS - 1
-                const bool active = q < nsub;
-                const int b0 = (s * nsub + q) * BPS;
-                const unsigned char *rowp = ring + slot * STAGE_BYTES + q * SUB_BYTES + r * KC;
-                // Visiting order rotated by 2q blocks keeps the four lanes of a
-                // quad on distinct shared-memory banks; wv[jj] / I[jj] hold
-                // block (jj + 2q) mod BPS.
-                const int rot = (2 * q) & (BPS - 1);
-                uint4 wv[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    if (active && jj < BPS) {
-                        const int blk = (jj + rot) & (BPS - 1);
-                        const int phys = swz ? (blk ^ (r & 7)) : blk;
-                        wv[jj] = *reinterpret_cast<const uint4 *>(rowp + phys * 16);
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < GEMV_MT; ++t) {
-                    if (t < m) {
-                        int I[8];
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            I[jj] = 0;
-                            if (active && jj < BPS) {
-                                const int xb = t * NB + b0 + ((jj + rot) & (BPS - 1));
-                                I[jj] = block_dot_i(wv[jj], xlo[xb], xhi[xb], xcb[xb]) - MAGIC_I;
-                            }
-                        }
-                        // in-order fold across the quad: lane 0, then 1, 2, 3
-                        float c = acc[t];
-                        const float *dt = xd + t * NB + b0;
-#pragma unroll
-                        for (int l = 0; l < 4; ++l) {
-                            if (l > 0) c = __shfl_sync(FULL, c, (lane & ~3) | (l - 1));
-                            if (q == l && active) {
-                                // here q == l is a compile-time constant, so is the rotation
-                                if (BPS == 8) {
-#pragma unroll
-                                    for (int b = 0; b < 8; ++b)
-                                        c = __fmaf_rn(dt[b], (float)I[(b - 2 * l) & 7], c);
-                                } else {
-#pragma unroll
-                                    for (int b = 0; b < 4; ++b)
-                                        c = __fmaf_rn(dt[b], (float)I[(b - 2 * l) & 3], c);
-                                }
-                            }
-                        }
-                        // the quad's last active lane holds the row's running sum
-                        acc[t] = __shfl_sync(FULL, c, (lane & ~3) | (nsub - 1));
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.empty[slot]);
+        for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+
+        // ping-pong between the two buffers, two stages per iteration
+#define COLI_DOTS(s_, dst_)                                                                     \
+    stage_dots<MT>(S.full, S.empty, ring, it, woff, xlo, xhi, xcb, (s_) * nsub + q, BPS, rot, NB, \
+                   m, active, lane, dst_)
+#define COLI_FOLD(s_, src_) \
+    stage_fold<MT>(xd + (s_) * nsub * BPS, NB, BPS, nsub, m, q, lane, src_, acc)
+        if (!COLI_DOTS(0, Ic)) { aborted = true; break; }
+        for (int s = 0; s < nst; s += 2) {
+            if (s + 1 < nst && !COLI_DOTS(s + 1, In)) { aborted = true; break; }
+            COLI_FOLD(s, Ic);
+            if (s + 1 >= nst) break;
+            if (s + 2 < nst && !COLI_DOTS(s + 2, Ic)) { aborted = true; break; }
+            COLI_FOLD(s + 1, In);
         }
+#undef COLI_DOTS
+#undef COLI_FOLD
+        if (aborted) break;
 
         // ---- unit epilogue ----
         if (gu) {
@@ -345,65 +389,83 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 if (a.h_dbg) a.h_dbg[(size_t)pos * F + ii] = h;
             }
             named_barrier(BAR_CONSUMERS, CONSUMERS);
-            if (threadIdx.x == 0) {
-                __threadfence();
-                atomic_add_release_gpu(&a.g_done[tile], 1);
-            }
+            if (threadIdx.x == 0) red_release_gpu(&a.g_done[tile], 1);
         } else {
             const int row = 64 * j + r;
             if (q == 0)
                 for (int t = 0; t < m; ++t)
                     a.y[(size_t)(pos0 + t) * H + row] = __fmul_rn(ers[2 * F + row], acc[t]);
             named_barrier(BAR_CONSUMERS, CONSUMERS);
-            if (threadIdx.x == 0) {
-                __threadfence();
-                const int old = atomic_add_acq_rel_gpu(&a.w_done[j], 1);
-                S.combine = (old == n_tiles - 1);
-            }
-            named_barrier(BAR_CONSUMERS, CONSUMERS);
-            if (S.combine) {
-                // every tile's down rows of this chunk are written: combine them
-                __threadfence();
-                const int T = a.n_tok, k = a.k, P = a.P;
-                for (int ii = threadIdx.x; ii < T * 64; ii += CONSUMERS) {
-                    const int t = ii >> 6, col = 64 * j + (ii & 63);
-                    float o = __ldcg(a.y + (size_t)(P + t) * H + col);
-                    for (int rr = 0; rr < k; ++rr) {
-                        const int pos = __ldcg(a.inv + (size_t)t * k + rr);
-                        if (pos < 0 || pos >= P) continue;
-                        o = __fmaf_rn(__ldcg(a.wts + (size_t)t * k + rr), __ldcg(a.y + (size_t)pos * H + col), o);
-                    }
-                    a.out[(size_t)t * H + col] = o;
-                }
-            }
+            if (threadIdx.x == 0) red_release_gpu(&a.w_done[j], 1);
         }
     }
-    return;
 
-drain:
-    // a wait gave up: wait (bounded) for copies still in flight into this
-    // block's ring before the block exits
-    if (lane == 0 && warp == 0) {
-        for (int i = 0; i < NSTAGE; ++i) {
-            const int slot = (int)(it % NSTAGE);
-            (void)mbar_wait_bounded(&S.full[slot], (uint32_t)(it / NSTAGE) & 1);
-            ++it;
+    if (aborted) {
+        set_status(a.status, ST_TIMEOUT);
+        S.abort = 1;
+        // wait (bounded) for copies still in flight into this block's ring
+        // before the block exits
+        if (threadIdx.x == 0)
+            for (int i = 0; i < NSTAGE; ++i, ++it)
+                (void)mbar_wait_bounded(&S.full[(int)(it % NSTAGE)], (uint32_t)(it / NSTAGE) & 1);
+        return;
+    }
+
+    // ---- combine: this block owns the chunks whose last-tile down unit it ran ----
+    if (!a.gate_up_only && n_tiles > 0) {
+        const long last0 = (long)(n_tiles - 1) * CH;
+        const long c0 = (w0 > last0 ? w0 : last0) - last0;
+        const long c1 = (w1 > last0 ? w1 : last0) - last0;
+        const int T = a.n_tok, k = a.k, P = a.P;
+        for (long c = c0; c < c1; ++c) {
+            if (threadIdx.x == 0) {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire_gpu(&a.w_done[c]) < n_tiles) {
+                    if (globaltimer() - t0 > WAIT_NS) {
+                        set_status(a.status, ST_TIMEOUT);
+                        break;
+                    }
+                    nanosleep_ns(32);
+                }
+            }
+            named_barrier(BAR_CONSUMERS, CONSUMERS);
+            for (int ii = threadIdx.x; ii < T * 64; ii += CONSUMERS) {
+                const int t = ii >> 6, col = 64 * (int)c + (ii & 63);
+                float o = __ldcg(a.y + (size_t)(P + t) * H + col);
+                for (int rr = 0; rr < k; ++rr) {
+                    const int pos = __ldcg(a.inv + (size_t)t * k + rr);
+                    if (pos < 0 || pos >= P) continue;
+                    o = __fmaf_rn(__ldcg(a.wts + (size_t)t * k + rr), __ldcg(a.y + (size_t)pos * H + col), o);
+                }
+                a.out[(size_t)t * H + col] = o;
+            }
         }
     }
 }
 
-int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
+template <int MT>
+static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
 {
     static size_t configured = 0;
     const size_t smem = experts_smem_bytes(a.H, a.F);
     if (smem != configured) {
-        if (cudaFuncSetAttribute(k_experts, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(k_experts<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
             return -1;
         configured = smem;
     }
-    k_experts<<<num_sms, EXPERT_THREADS, smem, st>>>(maps, a);
+    k_experts<MT><<<num_sms, EXPERT_THREADS, smem, st>>>(maps, a);
     count_launch();
     return 0;
+}
+
+int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
+{
+    // tiles hold at most min(T, GEMV_MT) tokens
+    const int mt = a.n_tok < GEMV_MT ? a.n_tok : GEMV_MT;
+    if (mt <= 1) return launch_experts_mt<1>(maps, a, num_sms, st);
+    if (mt <= 2) return launch_experts_mt<2>(maps, a, num_sms, st);
+    return launch_experts_mt<4>(maps, a, num_sms, st);
 }
 
 }  // namespace coli

@@ -108,6 +108,13 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v)
     return old;
 }
 
+// Release-ordered reduction without a return value (does not stall the thread
+// on the round trip).
+__device__ __forceinline__ void red_release_gpu(int *p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Named barrier for a subset of the block's warps.
 __device__ __forceinline__ void named_barrier(int id, int threads)
 {
