@@ -141,6 +141,18 @@ int coli_moe_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *
 int coli_moe_timing_enable(int on);
 int coli_moe_timing_read(double *ms_total, int *n_timed);
 
+/* Device-side event log of the expert kernel (tracing; off by default).
+ * coli_moe_trace_enable(n) allocates a log of n events per block (n <= 4096;
+ * 0 frees it and turns tracing off).  Each block writes, from its first
+ * consumer thread, events (globaltimer_ns << 8 | code, unit): 1 kernel start,
+ * 2 unit start, 3 activations staged, 4 unit done, 5 combine done, 6 exit;
+ * word 0 of a block's log counts its events.  coli_moe_trace_read()
+ * synchronises the device, copies the whole log (blocks x n x 2 u64) into
+ * `host` (capacity in u64 elements), clears it, and reports its shape. */
+int coli_moe_trace_enable(int events_per_block);
+int coli_moe_trace_read(unsigned long long *host, long long capacity, int *blocks,
+                        int *events_per_block);
+
 /* Number of kernels the library launched since the last call (then reset). */
 long long coli_moe_launch_count(void);
 

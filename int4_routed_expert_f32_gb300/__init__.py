@@ -26,7 +26,8 @@ EXPORTS = (
     "coli_moe_configure", "coli_moe_layer_forward", "coli_moe_layer_forward_hostio",
     "coli_moe_set_path", "coli_moe_get_device_status", "coli_moe_strerror", "coli_moe_release",
     "coli_moe_pack_int4", "coli_moe_timing_enable", "coli_moe_timing_read",
-    "coli_moe_launch_count", "coli_moe_dbg_quantize", "coli_moe_dbg_route",
+    "coli_moe_launch_count", "coli_moe_trace_enable", "coli_moe_trace_read",
+    "coli_moe_dbg_quantize", "coli_moe_dbg_route",
     "coli_moe_dbg_dispatch", "coli_moe_dbg_block_dots", "coli_moe_dbg_forward_intermediates",
     "coli_moe_dbg_expert_hidden",
 )
@@ -63,6 +64,9 @@ def _load():
         "coli_moe_timing_enable": ([i], i),
         "coli_moe_timing_read": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)], i),
         "coli_moe_launch_count": ([], ctypes.c_longlong),
+        "coli_moe_trace_enable": ([i], i),
+        "coli_moe_trace_read": ([P, ctypes.c_longlong, ctypes.POINTER(ctypes.c_int),
+                                 ctypes.POINTER(ctypes.c_int)], i),
         "coli_moe_dbg_quantize": ([P, i, P, P, P], i),
         "coli_moe_dbg_route": ([P, i, P, P, P, P, P, P], i),
         "coli_moe_dbg_dispatch": ([P, i, P, P, P, P, P], i),
@@ -171,6 +175,23 @@ def timing_read():
     n = ctypes.c_int(0)
     _check(_lib.coli_moe_timing_read(ctypes.byref(ms), ctypes.byref(n)), "timing_read")
     return ms.value, n.value
+
+
+def trace_enable(events_per_block: int):
+    _check(_lib.coli_moe_trace_enable(events_per_block), "trace_enable")
+
+
+def trace_read():
+    """Returns (events: uint64 [blocks][n][2], blocks, n); see the header."""
+    import numpy as np
+    nb, ne = ctypes.c_int(0), ctypes.c_int(0)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    cap = sms * 32 * 4096 * 2
+    buf = np.zeros(cap, np.uint64)
+    _check(_lib.coli_moe_trace_read(buf.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(nb),
+                                    ctypes.byref(ne)), "trace_read")
+    n = nb.value * ne.value * 2
+    return buf[:n].reshape(nb.value, ne.value, 2), nb.value, ne.value
 
 
 def launch_count() -> int:

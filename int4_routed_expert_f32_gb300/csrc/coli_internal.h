@@ -44,6 +44,8 @@ struct ExpertArgs {
     int *w_done;                    // [H/64] finished down units per row chunk
     int *work_counter;              // next unit to claim
     int *status;
+    unsigned long long *trace;      // optional per-block event log (null: off)
+    int trace_cap;                  // events per block
 };
 
 // Small-batch routing in one launch: Q8_0 of x, router logits, top-k, dispatch,

@@ -54,6 +54,9 @@ struct State {
     std::vector<cudaEvent_t> ev_pool;  // pairs (start, stop)
     int ev_used = 0;
     int max_tiles = 0;
+    unsigned long long *trace = nullptr;   // expert-kernel event log (device)
+    int trace_cap = 0;
+    int trace_blocks = 0;
     // tensor maps of the last weights seen (re-encoded when a pointer changes)
     ExpertMaps maps{};
     const void *maps_key[2] = {nullptr, nullptr};
@@ -288,6 +291,43 @@ long long coli_moe_launch_count(void)
     return n;
 }
 
+int coli_moe_trace_enable(int events_per_block)
+{
+    if (g.trace) {
+        cudaFree(g.trace);
+        g.trace = nullptr;
+        g.trace_cap = 0;
+    }
+    if (events_per_block <= 0) return COLI_OK;
+    if (events_per_block > 4096) return COLI_E_INVAL;
+    int dev = 0, sms = 0;
+    CUDA_OK(cudaGetDevice(&dev));
+    CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    g.trace_blocks = sms * 32;   // more than any expert-kernel grid
+    const size_t bytes = (size_t)g.trace_blocks * events_per_block * 2 * sizeof(unsigned long long);
+    if (cudaMalloc(&g.trace, bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        g.trace = nullptr;
+        return COLI_E_NOMEM;
+    }
+    CUDA_OK(cudaMemset(g.trace, 0, bytes));
+    g.trace_cap = events_per_block;
+    return COLI_OK;
+}
+
+int coli_moe_trace_read(unsigned long long *host, long long capacity, int *blocks, int *events_per_block)
+{
+    if (!g.trace) return COLI_E_INVAL;
+    const size_t n = (size_t)g.trace_blocks * g.trace_cap * 2;
+    if (!host || capacity < (long long)n || !blocks || !events_per_block) return COLI_E_INVAL;
+    CUDA_OK(cudaDeviceSynchronize());
+    CUDA_OK(cudaMemcpy(host, g.trace, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+    CUDA_OK(cudaMemset(g.trace, 0, n * sizeof(unsigned long long)));
+    *blocks = g.trace_blocks;
+    *events_per_block = g.trace_cap;
+    return COLI_OK;
+}
+
 int coli_moe_timing_enable(int on)
 {
     g.timing = on != 0;
@@ -436,6 +476,8 @@ static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *
     a.w_done = w.sync + g.max_tiles;
     a.work_counter = w.sync + g.max_tiles + s.hidden / 64;
     a.status = w.status;
+    a.trace = g.trace;
+    a.trace_cap = g.trace_cap;
     return a;
 }
 

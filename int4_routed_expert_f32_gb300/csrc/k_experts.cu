@@ -64,6 +64,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Optional event log: per block, trace_cap slots of (globaltimer << 8 | code)
+// followed by the unit; slot 0 counts the events.  Codes: 1 kernel start,
+// 2 unit start (first stage arrived), 3 activations staged, 4 unit done,
+// 5 combine done, 6 consumer exit.
+__device__ __forceinline__ void trace_event(const ExpertArgs &a, int code, long unit)
+{
+    if (!a.trace || threadIdx.x != 0) return;
+    unsigned long long *blk = a.trace + (size_t)blockIdx.x * a.trace_cap * 2;
+    const unsigned long long n = blk[0];
+    if ((long)n + 1 >= a.trace_cap) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    blk[2 * (n + 1)] = (t << 8) | (unsigned)code;
+    blk[2 * (n + 1) + 1] = (unsigned long long)unit;
+    blk[0] = n + 1;
+}
+
 // Bounded spin until *p >= target; false if it gave up.
 __device__ __forceinline__ bool wait_counter(const int *p, int target)
 {
@@ -261,6 +278,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     long it = 0;
     int staged_tile = -1;
     bool staged_gu = false;
+    trace_event(a, 1, -1);
     float acc[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
@@ -281,6 +299,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         if (u < 0) break;
         if (s == 0) {
             // new unit
+            trace_event(a, 2, u);
             decode_unit(u, n_gu, G, CH, &gu, &tile, &j);
             e = __ldg(a.tile_expert + tile);
             pos0 = __ldg(a.tile_pos0 + tile);
@@ -303,6 +322,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 named_barrier(BAR_CONSUMERS, CONSUMERS);
                 staged_tile = tile;
                 staged_gu = gu;
+                trace_event(a, 3, u);
             }
 #pragma unroll
             for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
@@ -367,6 +387,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 if (lane == 0) red_release_gpu(&a.g_done[tile], 1);
             }
             named_barrier(BAR_CONSUMERS, CONSUMERS);   // red[] is reused by the next unit
+            trace_event(a, 4, u);
         } else {
             const int row = 64 * j + r;
             const float sd = ers[2 * F + row];
@@ -395,9 +416,13 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                     }
                     a.out[(size_t)t * H + col] = o;
                 }
+                named_barrier(BAR_CONSUMERS, CONSUMERS);
+                trace_event(a, 5, u);
             }
+            trace_event(a, 4, u);
         }
     }
+    trace_event(a, 6, -1);
 
     if (S.abort && threadIdx.x == 0) {
         // a wait gave up: wait (bounded) for copies still in flight into this
