@@ -23,6 +23,7 @@ struct ExpertArgs {
     int n_tok;                      // T
     int P;                          // T * k (routed pairs); shared rows follow at P + t
     int KC;                         // bytes of a weight row per pipeline stage (128 or 64)
+    int nstage;                     // ring depth (set by the launcher)
     int gate_up_only;               // 1: stop after h (stage tests)
     const float *expert_rs;         // [E][2F+H]
     const float *shared_rs;         // [2F+H]

@@ -36,7 +36,7 @@
 
 namespace coli {
 
-constexpr int NSTAGE = 4;
+constexpr int NSTAGE_MAX = 16;
 constexpr int STAGE_ROWS = 64;
 constexpr int KC_MAX = 128;
 constexpr int STAGE_BYTES = STAGE_ROWS * KC_MAX;   // 8 KB
@@ -93,13 +93,13 @@ __device__ __forceinline__ bool wait_counter(const int *p, int target)
 }
 
 struct ExpertSmem {
-    int stage_unit[NSTAGE];     // unit of each ring slot (-1: no more work)
-    int stage_k[NSTAGE];        // stage index inside the unit
+    int stage_unit[NSTAGE_MAX];     // unit of each ring slot (-1: no more work)
+    int stage_k[NSTAGE_MAX];        // stage index inside the unit
     int abort;
     int combine;
-    int tok[GEMV_MT];
-    alignas(8) uint64_t full[NSTAGE];
-    alignas(8) uint64_t empty[NSTAGE];
+    int tok[GEMV_MT];               // rows of the activations being staged
+    alignas(8) uint64_t full[NSTAGE_MAX];
+    alignas(8) uint64_t empty[NSTAGE_MAX];
 };
 
 static size_t act_bytes(int H, int F, int mt)
@@ -108,41 +108,73 @@ static size_t act_bytes(int H, int F, int mt)
     return (size_t)mt * NB * (16 + 16 + 4 + 4);
 }
 
-size_t experts_smem_bytes_mt(int H, int F, int mt)
+size_t experts_smem_bytes_mt(int H, int F, int mt, int nstage)
 {
-    return 1024 /*align slack*/ + (size_t)NSTAGE * STAGE_BYTES + act_bytes(H, F, mt) +
+    return 1024 /*align slack*/ + (size_t)nstage * STAGE_BYTES + act_bytes(H, F, mt) +
            (size_t)mt * 32 * 4 + sizeof(ExpertSmem);
 }
 
-size_t experts_smem_bytes(int H, int F) { return experts_smem_bytes_mt(H, F, GEMV_MT); }
+// Ring depth: as deep as lets two blocks share an SM (a deep ring keeps the
+// producer streaming down-projection weights while the down units still wait
+// for their tiles' gate/up results).
+static int ring_stages(int H, int F, int mt)
+{
+    const size_t per_block = 110 * 1024;     // about half of the SM's shared memory
+    const size_t fixed = experts_smem_bytes_mt(H, F, mt, 0);
+    int n = fixed < per_block ? (int)((per_block - fixed) / STAGE_BYTES) : 2;
+    if (n > NSTAGE_MAX) n = NSTAGE_MAX;
+    if (n < 2) n = 2;
+    return n;
+}
+
+size_t experts_smem_bytes(int H, int F) { return experts_smem_bytes_mt(H, F, GEMV_MT, ring_stages(H, F, GEMV_MT)); }
 
 // Split-form activations of one tile into shared memory (see block_dot):
-// xlo/xhi/xcb/xd are [MT][NB].
+// xlo/xhi/xcb/xd are [MT][NB].  Loads are issued SU at a time per thread so
+// that a tile's staging costs about one L2 round trip.
 template <int MT>
 __device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const float *__restrict__ d,
                                            int K, int m, const int *rows, int row_limit,
                                            uint4 *xlo, uint4 *xhi, int *xcb, float *xd, int *status)
 {
+    constexpr int SU = 4;
     const int NB = K / 32;
-    for (int i = threadIdx.x; i < MT * NB; i += CONSUMERS) {
-        const int t = i / NB, b = i - t * NB;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-        int sum = 0;
-        float dd = 0.0f;
-        if (t < m) {
-            const int row = rows[t];
-            if (row >= 0 && row < row_limit) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(q + (size_t)row * K + (size_t)b * 32);
-                split_block(__ldcg(src), __ldcg(src + 1), &lo, &hi, &sum);
-                dd = __ldcg(d + (size_t)row * NB + b);
-            } else {
-                set_status(status, ST_BAD_INDEX);
+    for (int i0 = threadIdx.x; i0 < MT * NB; i0 += CONSUMERS * SU) {
+        uint4 va[SU], vb[SU];
+        float vd[SU];
+#pragma unroll
+        for (int uu = 0; uu < SU; ++uu) {
+            const int i = i0 + uu * CONSUMERS;
+            va[uu] = vb[uu] = make_uint4(0, 0, 0, 0);
+            vd[uu] = 0.0f;
+            if (i < MT * NB) {
+                const int t = i / NB, b = i - t * NB;
+                if (t < m) {
+                    const int row = rows[t];
+                    if (row >= 0 && row < row_limit) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(q + (size_t)row * K + (size_t)b * 32);
+                        va[uu] = __ldcg(src);
+                        vb[uu] = __ldcg(src + 1);
+                        vd[uu] = __ldcg(d + (size_t)row * NB + b);
+                    } else {
+                        set_status(status, ST_BAD_INDEX);
+                    }
+                }
             }
         }
-        xlo[i] = lo;
-        xhi[i] = hi;
-        xcb[i] = MAGIC_I - 8 * sum;
-        xd[i] = dd;
+#pragma unroll
+        for (int uu = 0; uu < SU; ++uu) {
+            const int i = i0 + uu * CONSUMERS;
+            if (i < MT * NB) {
+                uint4 lo, hi;
+                int sum;
+                split_block(va[uu], vb[uu], &lo, &hi, &sum);
+                xlo[i] = lo;
+                xhi[i] = hi;
+                xcb[i] = MAGIC_I - 8 * sum;
+                xd[i] = vd[uu];
+            }
+        }
     }
 }
 
@@ -183,7 +215,8 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *ring = smem;
     const int NBmax = (a.H > a.F ? a.H : a.F) / 32;
-    uint4 *xlo = reinterpret_cast<uint4 *>(ring + NSTAGE * STAGE_BYTES);
+    const int nstage = a.nstage;
+    uint4 *xlo = reinterpret_cast<uint4 *>(ring + nstage * STAGE_BYTES);
     uint4 *xhi = xlo + MT * NBmax;
     int *xcb = reinterpret_cast<int *>(xhi + MT * NBmax);
     float *xd = reinterpret_cast<float *>(xcb + MT * NBmax);
@@ -199,7 +232,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const int nst_gu = (H / 2) / KC, nst_dn = (F / 2) / KC;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < nstage; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], CONSUMER_WARPS);
         }
@@ -216,7 +249,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             prefetch_tmap(&maps.sgu);
             prefetch_tmap(&maps.sdn);
             const uint64_t pol = policy_evict_first();
-            long it = 0;
+            int slot = 0;
+            uint32_t phase = 0;       // parity of the ring's current round
+            bool first_round = true;
             long u = atomicAdd(a.work_counter, 1);
             for (;;) {
                 const bool done = u >= total || S.abort;
@@ -234,10 +269,8 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                                    : (shared ? (const void *)&maps.sdn : (const void *)&maps.dn);
                 const int z = shared ? 0 : e;
                 bool stop = false;
-                for (int s = 0; s < nst; ++s, ++it) {
-                    const int slot = (int)(it % NSTAGE);
-                    const uint32_t round = (uint32_t)(it / NSTAGE);
-                    if (round > 0 && !mbar_wait_bounded(&S.empty[slot], (round - 1) & 1)) {
+                for (int s = 0; s < nst; ++s) {
+                    if (!first_round && !mbar_wait_bounded(&S.empty[slot], phase ^ 1)) {
                         set_status(a.status, ST_TIMEOUT);
                         S.abort = 1;
                         stop = true;
@@ -259,6 +292,11 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                     } else {
                         tma_load_3d(dst, m, x, 64 * j, z, &S.full[slot], pol);
                     }
+                    if (++slot == nstage) {
+                        slot = 0;
+                        phase ^= 1;
+                        first_round = false;
+                    }
                 }
                 if (stop) break;
                 u = u_next;
@@ -275,9 +313,13 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) woff[jj] = r * KC + 16 * (swz ? (jj ^ (r & 7)) : jj);
 
-    long it = 0;
-    int staged_tile = -1;
-    bool staged_gu = false;
+    int slot = 0;
+    uint32_t phase = 0;
+    int staged_tile = -1;            // tile whose h codes are staged (down units)
+    int staged_tok[GEMV_MT];         // tokens whose x codes are staged (gate/up units)
+    int staged_m = -1;
+#pragma unroll
+    for (int t = 0; t < GEMV_MT; ++t) staged_tok[t] = -1;
     trace_event(a, 1, -1);
     float acc[MT];
 #pragma unroll
@@ -287,9 +329,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const float *ers = nullptr;
 
     for (;;) {
-        const int slot = (int)(it % NSTAGE);
-        const uint32_t round = (uint32_t)(it / NSTAGE);
-        if (!mbar_wait_bounded(&S.full[slot], round & 1)) {
+        if (!mbar_wait_bounded(&S.full[slot], phase)) {
             set_status(a.status, ST_TIMEOUT);
             S.abort = 1;
             break;
@@ -307,8 +347,18 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             nst = gu ? nst_gu : nst_dn;
             NB = gu ? H / 32 : F / 32;
             ers = (e == a.E) ? a.shared_rs : a.expert_rs + (size_t)e * (2 * F + H);
-            if (tile != staged_tile || gu != staged_gu) {
-                // activations of the tile: x codes for gate/up, h codes for down
+            // activations: x codes of the tile's tokens for gate/up (kept while
+            // the token set is unchanged), h codes of the tile for down
+            bool restage;
+            if (gu) {
+                restage = (m != staged_m) || staged_tile >= 0;
+#pragma unroll
+                for (int t = 0; t < GEMV_MT; ++t)
+                    if (t < m && __ldg(a.pos_token + pos0 + t) != staged_tok[t]) restage = true;
+            } else {
+                restage = (tile != staged_tile);
+            }
+            if (restage) {
                 if (threadIdx.x == 0) {
                     if (!gu && !wait_counter(&a.g_done[tile], G)) set_status(a.status, ST_TIMEOUT);
                     for (int t = 0; t < GEMV_MT; ++t)
@@ -319,9 +369,11 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                     stage_acts<MT>(a.qx, a.dx, H, m, S.tok, a.n_tok, xlo, xhi, xcb, xd, a.status);
                 else
                     stage_acts<MT>(a.qh, a.dh, F, m, S.tok, a.P + a.n_tok, xlo, xhi, xcb, xd, a.status);
+#pragma unroll
+                for (int t = 0; t < GEMV_MT; ++t) staged_tok[t] = gu ? S.tok[t] : -1;
+                staged_m = gu ? m : -1;
+                staged_tile = gu ? -1 : tile;
                 named_barrier(BAR_CONSUMERS, CONSUMERS);
-                staged_tile = tile;
-                staged_gu = gu;
                 trace_event(a, 3, u);
             }
 #pragma unroll
@@ -357,7 +409,10 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
-        ++it;
+        if (++slot == nstage) {
+            slot = 0;
+            phase ^= 1;
+        }
         if (s != nst - 1) continue;
 
         // ---- unit epilogue ----
@@ -427,17 +482,24 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     if (S.abort && threadIdx.x == 0) {
         // a wait gave up: wait (bounded) for copies still in flight into this
         // block's ring before the block exits
-        for (int i = 0; i < NSTAGE; ++i, ++it)
-            (void)mbar_wait_bounded(&S.full[(int)(it % NSTAGE)], (uint32_t)(it / NSTAGE) & 1);
+        for (int i = 0; i < nstage; ++i) {
+            (void)mbar_wait_bounded(&S.full[slot], phase);
+            if (++slot == nstage) {
+                slot = 0;
+                phase ^= 1;
+            }
+        }
     }
 }
 
 template <int MT>
-static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
+static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int num_sms, cudaStream_t st)
 {
     static size_t configured = 0;
     static int blocks_per_sm = 0;
-    const size_t smem = experts_smem_bytes_mt(a.H, a.F, MT);
+    ExpertArgs a = a_in;
+    a.nstage = ring_stages(a.H, a.F, MT);
+    const size_t smem = experts_smem_bytes_mt(a.H, a.F, MT, a.nstage);
     if (smem != configured) {
         if (cudaFuncSetAttribute(k_experts<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
