@@ -67,7 +67,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 // Optional event log: per block, trace_cap slots of (globaltimer << 8 | code)
 // followed by the unit; slot 0 counts the events.  Codes: 1 kernel start,
 // 2 unit start (first stage arrived), 3 activations staged, 4 unit done,
-// 5 combine done, 6 consumer exit.
+// 5 combine done, 6 consumer exit, 7 consumer time waiting for data (the
+// unit field holds nanoseconds); the producer's waiting time for free ring
+// slots is code 8 in the block's last slot.
 __device__ __forceinline__ void trace_event(const ExpertArgs &a, int code, long unit)
 {
     if (!a.trace || threadIdx.x != 0) return;
@@ -210,9 +212,10 @@ template <int MT>
 __global__ void __launch_bounds__(EXPERT_THREADS)
 k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled TMA boxes, by pointer arithmetic on
+    // the shared array itself so that every access stays a shared-memory access
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char *ring = smem;
     const int NBmax = (a.H > a.F ? a.H : a.F) / 32;
     const int nstage = a.nstage;
@@ -249,6 +252,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             prefetch_tmap(&maps.sgu);
             prefetch_tmap(&maps.sdn);
             const uint64_t pol = policy_evict_first();
+            unsigned long long waited = 0;      // traced: time spent waiting for free slots
             int slot = 0;
             uint32_t phase = 0;       // parity of the ring's current round
             bool first_round = true;
@@ -270,7 +274,10 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 const int z = shared ? 0 : e;
                 bool stop = false;
                 for (int s = 0; s < nst; ++s) {
-                    if (!first_round && !mbar_wait_bounded(&S.empty[slot], phase ^ 1)) {
+                    const unsigned long long w0 = a.trace ? globaltimer() : 0;
+                    const bool got = first_round || mbar_wait_bounded(&S.empty[slot], phase ^ 1);
+                    if (a.trace) waited += globaltimer() - w0;
+                    if (!got) {
                         set_status(a.status, ST_TIMEOUT);
                         S.abort = 1;
                         stop = true;
@@ -301,6 +308,12 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 if (stop) break;
                 u = u_next;
             }
+            if (a.trace) {
+                // the producer's lane logs its waiting time in the block's last slot
+                unsigned long long *blk = a.trace + (size_t)blockIdx.x * a.trace_cap * 2;
+                blk[2 * (a.trace_cap - 1)] = (waited << 8) | 8u;
+                blk[2 * (a.trace_cap - 1) + 1] = 0;
+            }
         }
         return;
     }
@@ -328,8 +341,12 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     int tile = 0, j = 0, e = 0, pos0 = 0, m = 0, nst = 0, NB = 0;
     const float *ers = nullptr;
 
+    unsigned long long full_wait = 0;    // traced: time spent waiting for filled slots
     for (;;) {
-        if (!mbar_wait_bounded(&S.full[slot], phase)) {
+        const unsigned long long fw0 = a.trace ? globaltimer() : 0;
+        const bool got = mbar_wait_bounded(&S.full[slot], phase);
+        if (a.trace) full_wait += globaltimer() - fw0;
+        if (!got) {
             set_status(a.status, ST_TIMEOUT);
             S.abort = 1;
             break;
@@ -478,6 +495,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         }
     }
     trace_event(a, 6, -1);
+    trace_event(a, 7, (long)full_wait);
 
     if (S.abort && threadIdx.x == 0) {
         // a wait gave up: wait (bounded) for copies still in flight into this
