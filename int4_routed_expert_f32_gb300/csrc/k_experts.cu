@@ -14,16 +14,18 @@
 //     every gate/up unit (a tile of <= GEMV_MT tokens of one expert x 32
 //     hidden units = 32 gate rows + 32 up rows), then every down unit (a tile x
 //     64 output rows).
-//   * The producer streams a unit's 64 weight rows through a ring of NSTAGE
-//     stages with 3-D TMA tile loads: a stage is 64 rows x 128 bytes (256
-//     weights of each row), one swizzled box (128-byte swizzle), L2
-//     evict-first.  Each stage completes on its mbarrier; the consumers
-//     release it through a second one.
-//   * Consumer lane r owns weight row r: per stage it reads its row's 8 blocks
-//     of 32 weights (the swizzle keeps the 32 lanes on distinct banks), does
-//     the dp4a block dots and folds them into its F32 accumulator in block
-//     order, acc = fma(d_b, I_b, acc): the row's whole dot product lives in one
-//     lane, so the order is the fixed ascending one without any exchange.
+//   * The producer streams a unit's 64 weight rows through a ring of stages
+//     with 3-D TMA tile loads: a stage is 64 rows x 256 bytes (512 weights of
+//     each row) as two swizzled boxes of 64 rows x 128 bytes (128-byte
+//     swizzle), L2 evict-first.  Each stage completes on its mbarrier; the
+//     consumers release it through a second one.
+//   * Consumer lane r owns weight row r: per stage it reads its row's 16
+//     blocks of 32 weights (the swizzle keeps the 32 lanes on distinct banks),
+//     does the dp4a block dots and folds them into its F32 accumulator in
+//     block order, acc = fma(d_b, I_b, acc): the row's whole dot product lives
+//     in one lane, so the order is the fixed ascending one without any
+//     exchange.  Sixteen independent block dots per stage give each warp
+//     enough instruction-level parallelism; a few blocks per SM hide the rest.
 //   * A down unit needs the h codes of its whole tile: it waits (bounded) on
 //     the tile's gate/up completion counter.  The block that finishes the last
 //     down unit of a 64-row output chunk (over all tiles) combines the chunk.
@@ -39,7 +41,9 @@ namespace coli {
 constexpr int NSTAGE_MAX = 16;
 constexpr int STAGE_ROWS = 64;
 constexpr int KC_MAX = 128;
-constexpr int STAGE_BYTES = STAGE_ROWS * KC_MAX;   // 8 KB
+constexpr int NSUB_MAX = 2;                        // TMA boxes along K per stage
+constexpr int SUB_BYTES = STAGE_ROWS * KC_MAX;     // 8 KB: one box of 64 rows x 128 B
+constexpr int STAGE_BYTES = NSUB_MAX * SUB_BYTES;  // 16 KB
 constexpr int CONSUMER_WARPS = 2;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;     // one lane per stage row
 constexpr int EXPERT_THREADS = CONSUMERS + 32;
@@ -116,18 +120,9 @@ size_t experts_smem_bytes_mt(int H, int F, int mt, int nstage)
            (size_t)mt * 32 * 4 + sizeof(ExpertSmem);
 }
 
-// Ring depth: as deep as lets two blocks share an SM (a deep ring keeps the
-// producer streaming down-projection weights while the down units still wait
-// for their tiles' gate/up results).
-static int ring_stages(int H, int F, int mt)
-{
-    const size_t per_block = 110 * 1024;     // about half of the SM's shared memory
-    const size_t fixed = experts_smem_bytes_mt(H, F, mt, 0);
-    int n = fixed < per_block ? (int)((per_block - fixed) / STAGE_BYTES) : 2;
-    if (n > NSTAGE_MAX) n = NSTAGE_MAX;
-    if (n < 2) n = 2;
-    return n;
-}
+// Ring depth.  More blocks per SM help more than deeper rings: each block's
+// consumers drain a bounded rate, so four 16 KB stages per block suffice.
+static int ring_stages(int, int, int) { return 4; }
 
 size_t experts_smem_bytes(int H, int F) { return experts_smem_bytes_mt(H, F, GEMV_MT, ring_stages(H, F, GEMV_MT)); }
 
@@ -185,16 +180,16 @@ __device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const f
 // Returns MAGIC_I + I when cb = MAGIC_I - 8 * sum(x).
 __device__ __forceinline__ int block_dot_i(uint4 w, uint4 lo, uint4 hi, int cb)
 {
-    int a = cb, h = 0;
-    a = dp4a_us(w.x & 0x0F0F0F0Fu, (int)lo.x, a);
-    h = dp4a_us(w.x & 0xF0F0F0F0u, (int)hi.x, h);
-    a = dp4a_us(w.y & 0x0F0F0F0Fu, (int)lo.y, a);
-    h = dp4a_us(w.y & 0xF0F0F0F0u, (int)hi.y, h);
-    a = dp4a_us(w.z & 0x0F0F0F0Fu, (int)lo.z, a);
-    h = dp4a_us(w.z & 0xF0F0F0F0u, (int)hi.z, h);
-    a = dp4a_us(w.w & 0x0F0F0F0Fu, (int)lo.w, a);
-    h = dp4a_us(w.w & 0xF0F0F0F0u, (int)hi.w, h);
-    return a + (h >> 4);
+    // four short chains instead of two long ones
+    int a0 = dp4a_us(w.x & 0x0F0F0F0Fu, (int)lo.x, cb);
+    int a1 = dp4a_us(w.y & 0x0F0F0F0Fu, (int)lo.y, 0);
+    int h0 = dp4a_us(w.x & 0xF0F0F0F0u, (int)hi.x, 0);
+    int h1 = dp4a_us(w.y & 0xF0F0F0F0u, (int)hi.y, 0);
+    a0 = dp4a_us(w.z & 0x0F0F0F0Fu, (int)lo.z, a0);
+    a1 = dp4a_us(w.w & 0x0F0F0F0Fu, (int)lo.w, a1);
+    h0 = dp4a_us(w.z & 0xF0F0F0F0u, (int)hi.z, h0);
+    h1 = dp4a_us(w.w & 0xF0F0F0F0u, (int)hi.w, h1);
+    return (a0 + a1) + ((h0 + h1) >> 4);
 }
 
 // Decode unit u: gate/up units first (tile-major), then down units.
@@ -232,7 +227,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const int n_tiles = *a.n_tiles;
     const long n_gu = (long)n_tiles * G;
     const long total = a.gate_up_only ? n_gu : n_gu + (long)n_tiles * CH;
-    const int nst_gu = (H / 2) / KC, nst_dn = (F / 2) / KC;
+    // boxes along K per stage (2 when the row's box count is even)
+    const int nsub_gu = (((H / 2) / KC) % 2 == 0) ? 2 : 1, nsub_dn = (((F / 2) / KC) % 2 == 0) ? 2 : 1;
+    const int nst_gu = (H / 2) / (KC * nsub_gu), nst_dn = (F / 2) / (KC * nsub_dn);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstage; ++s) {
@@ -268,6 +265,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 // claim the next unit early: its round trip overlaps this one's copies
                 const long u_next = done ? total : atomicAdd(a.work_counter, 1);
                 const int nst = done ? 1 : (gu ? nst_gu : nst_dn);
+                const int nsub = gu ? nsub_gu : nsub_dn;
                 const bool shared = (e == a.E);
                 const void *m = gu ? (shared ? (const void *)&maps.sgu : (const void *)&maps.gu)
                                    : (shared ? (const void *)&maps.sdn : (const void *)&maps.dn);
@@ -291,13 +289,16 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                     S.stage_unit[slot] = (int)u;
                     S.stage_k[slot] = s;
                     unsigned char *dst = ring + slot * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&S.full[slot], STAGE_ROWS * KC);
-                    const int x = s * KC;
-                    if (gu) {
-                        tma_load_3d(dst, m, x, 32 * j, z, &S.full[slot], pol);
-                        tma_load_3d(dst + 32 * KC, m, x, F + 32 * j, z, &S.full[slot], pol);
-                    } else {
-                        tma_load_3d(dst, m, x, 64 * j, z, &S.full[slot], pol);
+                    mbar_arrive_expect_tx(&S.full[slot], STAGE_ROWS * KC * nsub);
+                    for (int c = 0; c < nsub; ++c) {
+                        const int x = (s * nsub + c) * KC;
+                        unsigned char *d = dst + c * SUB_BYTES;
+                        if (gu) {
+                            tma_load_3d(d, m, x, 32 * j, z, &S.full[slot], pol);
+                            tma_load_3d(d + 32 * KC, m, x, F + 32 * j, z, &S.full[slot], pol);
+                        } else {
+                            tma_load_3d(d, m, x, 64 * j, z, &S.full[slot], pol);
+                        }
                     }
                     if (++slot == nstage) {
                         slot = 0;
@@ -338,7 +339,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
     bool gu = true;
-    int tile = 0, j = 0, e = 0, pos0 = 0, m = 0, nst = 0, NB = 0;
+    int tile = 0, j = 0, e = 0, pos0 = 0, m = 0, nst = 0, NB = 0, nsub = 1;
     const float *ers = nullptr;
 
     unsigned long long full_wait = 0;    // traced: time spent waiting for filled slots
@@ -362,6 +363,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             pos0 = __ldg(a.tile_pos0 + tile);
             m = __ldg(a.tile_m + tile);
             nst = gu ? nst_gu : nst_dn;
+            nsub = gu ? nsub_gu : nsub_dn;
             NB = gu ? H / 32 : F / 32;
             ers = (e == a.E) ? a.shared_rs : a.expert_rs + (size_t)e * (2 * F + H);
             // activations: x codes of the tile's tokens for gate/up (kept while
@@ -397,30 +399,38 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
         }
 
-        // ---- one stage: this lane's row, blocks b0 .. b0 + BPS - 1, in order ----
+        // ---- one stage: this lane's row, blocks b0 .. b0 + nsub * BPS - 1, in order ----
         {
             const unsigned char *base = ring + slot * STAGE_BYTES;
-            uint4 wv[8];
+            uint4 wv[NSUB_MAX][8];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                if (jj < BPS) wv[jj] = *reinterpret_cast<const uint4 *>(base + woff[jj]);
-            const int b0 = s * BPS;
+            for (int c = 0; c < NSUB_MAX; ++c)
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    if (c < nsub && jj < BPS)
+                        wv[c][jj] = *reinterpret_cast<const uint4 *>(base + c * SUB_BYTES + woff[jj]);
+            const int b0 = s * nsub * BPS;
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 if (t < m) {
-                    int I[8];
+                    int I[NSUB_MAX][8];
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj)
-                        if (jj < BPS) {
-                            const int xb = t * NB + b0 + jj;
-                            I[jj] = block_dot_i(wv[jj], xlo[xb], xhi[xb], xcb[xb]);
-                        }
+                    for (int c = 0; c < NSUB_MAX; ++c)
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            if (c < nsub && jj < BPS) {
+                                const int xb = t * NB + b0 + c * BPS + jj;
+                                I[c][jj] = block_dot_i(wv[c][jj], xlo[xb], xhi[xb], xcb[xb]);
+                            }
                     const float *dt = xd + t * NB + b0;
-                    float c = acc[t];
+                    float cacc = acc[t];
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj)
-                        if (jj < BPS) c = __fmaf_rn(dt[jj], __int_as_float(I[jj]) - MAGIC_F, c);
-                    acc[t] = c;
+                    for (int c = 0; c < NSUB_MAX; ++c)
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            if (c < nsub && jj < BPS)
+                                cacc = __fmaf_rn(dt[c * BPS + jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
+                    acc[t] = cacc;
                 }
             }
         }
