@@ -192,6 +192,44 @@ __device__ __forceinline__ int block_dot_i(uint4 w, uint4 lo, uint4 hi, int cb)
     return (a0 + a1) + ((h0 + h1) >> 4);
 }
 
+// One stage for this lane's row: the NSUB x BPS block dots of every token,
+// then their in-order fold into acc.  All trip counts are compile-time
+// constants, so the block dots form one straight-line region the scheduler
+// can interleave.
+template <int MT, int NSUB, int BPS>
+__device__ __forceinline__ void stage_rows(const unsigned char *base, const int (&woff)[8], const uint4 *xlo,
+                                           const uint4 *xhi, const int *xcb, const float *xd, int NB,
+                                           int b0, int m, float (&acc)[MT])
+{
+    uint4 wv[NSUB][BPS];
+#pragma unroll
+    for (int c = 0; c < NSUB; ++c)
+#pragma unroll
+        for (int jj = 0; jj < BPS; ++jj)
+            wv[c][jj] = *reinterpret_cast<const uint4 *>(base + c * SUB_BYTES + woff[jj]);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        if (t < m) {
+            const int xb0 = t * NB + b0;
+            int I[NSUB][BPS];
+#pragma unroll
+            for (int c = 0; c < NSUB; ++c)
+#pragma unroll
+                for (int jj = 0; jj < BPS; ++jj) {
+                    const int xb = xb0 + c * BPS + jj;
+                    I[c][jj] = block_dot_i(wv[c][jj], xlo[xb], xhi[xb], xcb[xb]);
+                }
+            float cacc = acc[t];
+#pragma unroll
+            for (int c = 0; c < NSUB; ++c)
+#pragma unroll
+                for (int jj = 0; jj < BPS; ++jj)
+                    cacc = __fmaf_rn(xd[xb0 + c * BPS + jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
+            acc[t] = cacc;
+        }
+    }
+}
+
 // Decode unit u: gate/up units first (tile-major), then down units.
 __device__ __forceinline__ void decode_unit(long u, long n_gu, int G, int CH, bool *gu, int *tile, int *j)
 {
@@ -203,7 +241,8 @@ __device__ __forceinline__ void decode_unit(long u, long n_gu, int G, int CH, bo
 }
 
 // MT: bound on the tokens of any tile in this launch (1, 2 or 4; <= GEMV_MT).
-template <int MT>
+// BPS: 32-weight blocks per 128- or 64-byte box row (8 or 4).
+template <int MT, int BPS>
 __global__ void __launch_bounds__(EXPERT_THREADS)
 k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 {
@@ -321,7 +360,6 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 
     // -------------------------------- consumers --------------------------------
     const int r = threadIdx.x;                // this lane's weight row in the stage (0..63)
-    const int BPS = KC / 16;                  // 32-weight blocks per row per stage (8 or 4)
     const bool swz = (KC == 128);
     int woff[8];
 #pragma unroll
@@ -402,37 +440,11 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         // ---- one stage: this lane's row, blocks b0 .. b0 + nsub * BPS - 1, in order ----
         {
             const unsigned char *base = ring + slot * STAGE_BYTES;
-            uint4 wv[NSUB_MAX][8];
-#pragma unroll
-            for (int c = 0; c < NSUB_MAX; ++c)
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    if (c < nsub && jj < BPS)
-                        wv[c][jj] = *reinterpret_cast<const uint4 *>(base + c * SUB_BYTES + woff[jj]);
             const int b0 = s * nsub * BPS;
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                if (t < m) {
-                    int I[NSUB_MAX][8];
-#pragma unroll
-                    for (int c = 0; c < NSUB_MAX; ++c)
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj)
-                            if (c < nsub && jj < BPS) {
-                                const int xb = t * NB + b0 + c * BPS + jj;
-                                I[c][jj] = block_dot_i(wv[c][jj], xlo[xb], xhi[xb], xcb[xb]);
-                            }
-                    const float *dt = xd + t * NB + b0;
-                    float cacc = acc[t];
-#pragma unroll
-                    for (int c = 0; c < NSUB_MAX; ++c)
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj)
-                            if (c < nsub && jj < BPS)
-                                cacc = __fmaf_rn(dt[c * BPS + jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
-                    acc[t] = cacc;
-                }
-            }
+            if (nsub == 2)
+                stage_rows<MT, 2, BPS>(base, woff, xlo, xhi, xcb, xd, NB, b0, m, acc);
+            else
+                stage_rows<MT, 1, BPS>(base, woff, xlo, xhi, xcb, xd, NB, b0, m, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -520,7 +532,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     }
 }
 
-template <int MT>
+template <int MT, int BPS>
 static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int num_sms, cudaStream_t st)
 {
     static size_t configured = 0;
@@ -529,28 +541,35 @@ static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int
     a.nstage = ring_stages(a.H, a.F, MT);
     const size_t smem = experts_smem_bytes_mt(a.H, a.F, MT, a.nstage);
     if (smem != configured) {
-        if (cudaFuncSetAttribute(k_experts<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        if (cudaFuncSetAttribute(k_experts<MT, BPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return -1;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k_experts<MT>, EXPERT_THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k_experts<MT, BPS>, EXPERT_THREADS,
                                                           smem) != cudaSuccess ||
             blocks_per_sm < 1)
             return -1;
         configured = smem;
     }
     // every block must be resident: down units wait on gate/up units of others
-    k_experts<MT><<<num_sms * blocks_per_sm, EXPERT_THREADS, smem, st>>>(maps, a);
+    k_experts<MT, BPS><<<num_sms * blocks_per_sm, EXPERT_THREADS, smem, st>>>(maps, a);
     count_launch();
     return 0;
 }
 
-int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
+template <int BPS>
+static int launch_experts_bps(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
 {
     // tiles hold at most min(T, GEMV_MT) tokens
     const int mt = a.n_tok < GEMV_MT ? a.n_tok : GEMV_MT;
-    if (mt <= 1) return launch_experts_mt<1>(maps, a, num_sms, st);
-    if (mt <= 2) return launch_experts_mt<2>(maps, a, num_sms, st);
-    return launch_experts_mt<4>(maps, a, num_sms, st);
+    if (mt <= 1) return launch_experts_mt<1, BPS>(maps, a, num_sms, st);
+    if (mt <= 2) return launch_experts_mt<2, BPS>(maps, a, num_sms, st);
+    return launch_experts_mt<4, BPS>(maps, a, num_sms, st);
+}
+
+int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
+{
+    if (a.KC == 128) return launch_experts_bps<8>(maps, a, num_sms, st);
+    return launch_experts_bps<4>(maps, a, num_sms, st);
 }
 
 }  // namespace coli
