@@ -30,6 +30,8 @@
 //     the tile's gate/up completion counter.  The block that finishes the last
 //     down unit of a 64-row output chunk (over all tiles) combines the chunk.
 // Counters are zeroed by the dispatch step that precedes the launch.
+#include <cstdlib>
+
 #include <cuda.h>
 
 #include "coli_common.cuh"
@@ -121,8 +123,18 @@ size_t experts_smem_bytes_mt(int H, int F, int mt, int nstage)
 }
 
 // Ring depth.  More blocks per SM help more than deeper rings: each block's
-// consumers drain a bounded rate, so four 16 KB stages per block suffice.
-static int ring_stages(int, int, int) { return 4; }
+// consumers drain a bounded rate.  COLI_MOE_RING_STAGES (2..16) overrides the
+// default for tuning.
+static int ring_stages(int, int, int)
+{
+    static int n = 0;
+    if (n == 0) {
+        const char *env = getenv("COLI_MOE_RING_STAGES");
+        const int v = env ? atoi(env) : 0;
+        n = (v >= 2 && v <= NSTAGE_MAX) ? v : 3;
+    }
+    return n;
+}
 
 size_t experts_smem_bytes(int H, int F) { return experts_smem_bytes_mt(H, F, GEMV_MT, ring_stages(H, F, GEMV_MT)); }
 
