@@ -203,8 +203,6 @@ def run(args):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    coli.timing_read()
-    coli.timing_enable(True)
     coli.launch_count()
     if world > 1:
         dist.barrier()
@@ -219,14 +217,24 @@ def run(args):
     if world > 1:
         dist.barrier()
     launches = coli.launch_count()
-    coli.timing_enable(False)
-    k_ms, k_n = coli.timing_read()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = float(sum(step_ms))
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
+
+    # dominant-kernel timing: the library records events around the expert
+    # kernel; they serialise it behind routing, so this is a separate pass over
+    # the same inputs
+    coli.timing_read()
+    coli.timing_enable(True)
+    for s in range(args.steps):
+        flush.zero_()
+        fwd(args.warmup + s)
+    torch.cuda.synchronize()
+    coli.timing_enable(False)
+    k_ms, k_n = coli.timing_read()
     status = coli.get_device_status()
 
     # end to end through the host-I/O entry point: pinned host x in, host out
@@ -262,7 +270,7 @@ def run(args):
         "config": workload_config(wl),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,
-                     "kernel": "expert gate/up + down (k_gateup_gemv, k_down_gemv)",
+                     "kernel": "k_experts (gate/up + SiLU*up requant + down + combine), timed alone",
                      "algorithmic_bytes_per_launch": bytes_per_fwd,
                      "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} hbm_gbs"},
         "weight_gbs_layer": bytes_per_fwd / (total_ms / args.steps * 1e-3) / 1e9,

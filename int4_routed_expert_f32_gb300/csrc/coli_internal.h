@@ -44,6 +44,9 @@ struct ExpertArgs {
     int *g_done;                    // [n_tiles] finished gate/up units per tile
     int *w_done;                    // [H/64] finished down units per row chunk
     int *work_counter;              // next unit to claim
+    int *blocks_done;               // blocks that finished (the last one resets)
+    int *sync_base;                 // all of the above counters, n_sync ints
+    int n_sync;
     int *status;
     unsigned long long *trace;      // optional per-block event log (null: off)
     int trace_cap;                  // events per block

@@ -236,7 +236,7 @@ int coli_moe_configure(const coli_moe_shape *s)
         {(void **)&w.tile_pos0, tiles * 4},
         {(void **)&w.tile_m, tiles * 4},
         {(void **)&w.n_tiles, 4},
-        {(void **)&w.sync, (tiles + H / 64 + 1) * 4},
+        {(void **)&w.sync, (tiles + H / 64 + 2) * 4},
         {(void **)&w.route_counter, 4},
         {(void **)&w.qh, R * F},
         {(void **)&w.dh, R * (F / 32) * 4},
@@ -264,7 +264,7 @@ int coli_moe_configure(const coli_moe_shape *s)
         return cuda_fail(cudaErrorUnknown);
     }
     CUDA_OK(cudaDeviceSynchronize());
-    w.n_sync = (int)(tiles + H / 64 + 1);
+    w.n_sync = (int)(tiles + H / 64 + 2);
     g.ws = w;
     g.max_tiles = (int)tiles;
     g.maps_valid = false;
@@ -475,6 +475,9 @@ static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *
     a.g_done = w.sync;
     a.w_done = w.sync + g.max_tiles;
     a.work_counter = w.sync + g.max_tiles + s.hidden / 64;
+    a.blocks_done = a.work_counter + 1;
+    a.sync_base = w.sync;
+    a.n_sync = w.n_sync;
     a.status = w.status;
     a.trace = g.trace;
     a.trace_cap = g.trace_cap;

@@ -29,7 +29,11 @@
 //   * A down unit needs the h codes of its whole tile: it waits (bounded) on
 //     the tile's gate/up completion counter.  The block that finishes the last
 //     down unit of a 64-row output chunk (over all tiles) combines the chunk.
-// Counters are zeroed by the dispatch step that precedes the launch.
+//   * Launched as a programmatic dependent of the routing kernel: set-up
+//     overlaps routing, and every thread waits for the routing grid
+//     (griddepcontrol.wait) before reading its results.  The counters start at
+//     zero (configure) and the last block to exit zeroes them for the next
+//     launch.
 #include <cstdlib>
 
 #include <cuda.h>
@@ -275,9 +279,6 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, F = a.F, KC = a.KC;
     const int G = F / 32, CH = H / 64;
-    const int n_tiles = *a.n_tiles;
-    const long n_gu = (long)n_tiles * G;
-    const long total = a.gate_up_only ? n_gu : n_gu + (long)n_tiles * CH;
     // boxes along K per stage (2 when the row's box count is even)
     const int nsub_gu = (((H / 2) / KC) % 2 == 0) ? 2 : 1, nsub_dn = (((F / 2) / KC) % 2 == 0) ? 2 : 1;
     const int nst_gu = (H / 2) / (KC * nsub_gu), nst_dn = (F / 2) / (KC * nsub_dn);
@@ -290,15 +291,22 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         S.abort = 0;
         fence_barrier_init();
     }
+    if (threadIdx.x == 32 * CONSUMER_WARPS) {
+        prefetch_tmap(&maps.gu);
+        prefetch_tmap(&maps.dn);
+        prefetch_tmap(&maps.sgu);
+        prefetch_tmap(&maps.sdn);
+    }
     __syncthreads();
+    // routing results (tile list, activations) are complete past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_tiles = *a.n_tiles;
+    const long n_gu = (long)n_tiles * G;
+    const long total = a.gate_up_only ? n_gu : n_gu + (long)n_tiles * CH;
 
     if (warp == CONSUMER_WARPS) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
-            prefetch_tmap(&maps.gu);
-            prefetch_tmap(&maps.dn);
-            prefetch_tmap(&maps.sgu);
-            prefetch_tmap(&maps.sdn);
             const uint64_t pol = policy_evict_first();
             unsigned long long waited = 0;      // traced: time spent waiting for free slots
             int slot = 0;
@@ -542,6 +550,23 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             }
         }
     }
+
+    // the last block out zeroes the counters for the next launch
+    named_barrier(BAR_CONSUMERS, CONSUMERS);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        S.combine = (atomic_add_acq_rel_gpu(a.blocks_done, 1) == (int)gridDim.x - 1);
+    }
+    named_barrier(BAR_CONSUMERS, CONSUMERS);
+    if (S.combine) {
+        for (int i = threadIdx.x; i < a.n_sync; i += CONSUMERS)
+            if (a.sync_base + i != a.blocks_done) a.sync_base[i] = 0;
+        named_barrier(BAR_CONSUMERS, CONSUMERS);
+        if (threadIdx.x == 0) {
+            __threadfence();
+            *a.blocks_done = 0;
+        }
+    }
 }
 
 template <int MT, int BPS>
@@ -563,7 +588,17 @@ static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int
         configured = smem;
     }
     // every block must be resident: down units wait on gate/up units of others
-    k_experts<MT, BPS><<<num_sms * blocks_per_sm, EXPERT_THREADS, smem, st>>>(maps, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms * blocks_per_sm);
+    cfg.blockDim = dim3(EXPERT_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_experts<MT, BPS>, maps, a) != cudaSuccess) return -1;
     count_launch();
     return 0;
 }

@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = ra.T, H = ra.H, E = ra.E, k = ra.k;
     const int e = blockIdx.x;
+    // the expert kernel may start launching now; it waits for this grid's
+    // results (griddepcontrol.wait) before reading any of them
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // 1. Q8_0 of x: warps of all blocks share the T*H/32 blocks
     const long nblk = (long)T * H / 32;
@@ -394,22 +397,40 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
         if (lane == 0) ra.dx[blk] = d;
     }
 
-    // 2. logits of expert e for every token
+    // 2. logits of expert e for every token (each thread's weight chunks are
+    //    loaded together, LG at a time, so the row costs one or two round trips)
     float acc[ROUTE_SMALL_MAX_T];
 #pragma unroll
     for (int t = 0; t < ROUTE_SMALL_MAX_T; ++t) acc[t] = 0.0f;
     const float4 *w4 = reinterpret_cast<const float4 *>(ra.W + (size_t)e * H);
-    for (int c = tid; c < H / 4; c += 256) {
-        const float4 wv = __ldg(w4 + c);
+    constexpr int LG = 8;
+    for (int c0 = tid; c0 < H / 4; c0 += 256 * LG) {
+        float4 wv[LG];
+#pragma unroll
+        for (int u = 0; u < LG; ++u) {
+            const int c = c0 + 256 * u;
+            wv[u] = (c < H / 4) ? __ldg(w4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
         for (int t = 0; t < ROUTE_SMALL_MAX_T; ++t) {
             if (t < T) {
-                const float4 xv = __ldg(reinterpret_cast<const float4 *>(ra.x + (size_t)t * H) + c);
+                const float4 *x4 = reinterpret_cast<const float4 *>(ra.x + (size_t)t * H);
+                float4 xv[LG];
+#pragma unroll
+                for (int u = 0; u < LG; ++u) {
+                    const int c = c0 + 256 * u;
+                    xv[u] = (c < H / 4) ? __ldg(x4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
                 float p = acc[t];
-                p = __fmaf_rn(xv.x, wv.x, p);
-                p = __fmaf_rn(xv.y, wv.y, p);
-                p = __fmaf_rn(xv.z, wv.z, p);
-                p = __fmaf_rn(xv.w, wv.w, p);
+#pragma unroll
+                for (int u = 0; u < LG; ++u) {
+                    if (c0 + 256 * u < H / 4) {      // chunks ascending, elements ascending
+                        p = __fmaf_rn(xv[u].x, wv[u].x, p);
+                        p = __fmaf_rn(xv[u].y, wv[u].y, p);
+                        p = __fmaf_rn(xv[u].z, wv[u].z, p);
+                        p = __fmaf_rn(xv[u].w, wv[u].w, p);
+                    }
+                }
                 acc[t] = p;
             }
         }
@@ -452,7 +473,6 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     __shared__ int s_idx[ROUTE_SMALL_MAX_T * MAX_K];
     __shared__ int s_cnt[MAX_E], s_base[MAX_E], s_tile0[MAX_E], s_off[MAX_E];
     __shared__ int s_ntiles;
-    for (int i = tid; i < ra.n_sync; i += 256) ra.sync[i] = 0;
     if (warp < T) {
         int ce[MAX_K];
         float cs[MAX_K], S;
