@@ -297,7 +297,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="decode", choices=["decode", "verify", "prefill", "profile"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "verify", "prefill", "profile", "route_profile"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-forwards", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

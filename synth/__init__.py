@@ -97,6 +97,10 @@ WORKLOADS = {
     # the decode shape with 16 routed experts (~0.3 GB resident): a small case of
     # the same kernels for profiler captures; one forward still reads 170 MB
     "profile": Workload("profile", 6144, 2048, 16, 8, 1, 1),
+    # the decode router's exact shape (hidden 6144, 256 experts, top-8, 1 token)
+    # with a small expert FFN (~0.6 GB resident): a small case for capturing the
+    # routing kernel
+    "route_profile": Workload("route_profile", 6144, 256, 256, 8, 1, 1),
     "sweep": Workload("sweep", 6144, 2048, 256, 8, 128, 100, zipf_beta=ZIPF_BETA, layers=8,
                       layer_corr=SWEEP_LAYER_CORR, batches=(1, 8, 32, 128)),
 }
