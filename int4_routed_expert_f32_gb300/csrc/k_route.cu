@@ -113,12 +113,13 @@ int launch_router_logits(const float *x, int T, int H, const float *W, int E, fl
 // ---------------------------------------------------------------------------
 constexpr int MAX_K = 16;
 
-// Top-k of one token's logits by one warp; lane 0 receives the experts in
-// rank order (ce) and their sigma (cs), and returns S = sum of the chosen
-// sigma in rank order.
-__device__ __forceinline__ void warp_topk(const float *logits_row, int E, int k,
-                                          const float *__restrict__ bias, int (&ce)[MAX_K],
-                                          float (&cs)[MAX_K], float *S_out)
+// Top-k of one token's logits by one warp.  Lane 0 writes the experts in rank
+// order to idx_out[0..k) and their sigma to sig_out[0..k); every lane returns
+// S = the sum of the chosen sigma in rank order.  The rounds are a rolled
+// loop: this runs once per token at the end of routing, where a compact body
+// matters more than unrolling.
+__device__ __noinline__ float warp_topk(const float *logits_row, int E, int k,
+                                        const float *__restrict__ bias, int *idx_out, float *sig_out)
 {
     const int lane = threadIdx.x & 31;
     float sig[8], key[8];
@@ -135,58 +136,55 @@ __device__ __forceinline__ void warp_topk(const float *logits_row, int E, int k,
     }
     unsigned taken = 0;
     float S = 0.0f;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        float bv = -__int_as_float(0x7f800000);
+        int be = INT_MAX;
+        float bs = 0.0f;
 #pragma unroll
-    for (int r = 0; r < MAX_K; ++r) {
-        if (r < k) {
-            float bv = -__int_as_float(0x7f800000);
-            int be = INT_MAX;
-            float bs = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && (key[i] > bv || be == INT_MAX)) {
-                    bv = key[i];
-                    be = e;
-                    bs = sig[i];
-                }
+        for (int i = 0; i < 8; ++i) {
+            int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (key[i] > bv || be == INT_MAX)) {
+                bv = key[i];
+                be = e;
+                bs = sig[i];
             }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                float ov = __shfl_xor_sync(FULL, bv, o);
-                int oe = __shfl_xor_sync(FULL, be, o);
-                float os = __shfl_xor_sync(FULL, bs, o);
-                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                    bs = os;
-                }
-            }
-            if (be != INT_MAX && (be & 31) == lane) taken |= 1u << (be >> 5);
-            ce[r] = (be == INT_MAX) ? -1 : be;
-            cs[r] = bs;
-            S = __fadd_rn(S, bs);
         }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            float ov = __shfl_xor_sync(FULL, bv, o);
+            int oe = __shfl_xor_sync(FULL, be, o);
+            float os = __shfl_xor_sync(FULL, bs, o);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+                bs = os;
+            }
+        }
+        if (be != INT_MAX && (be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == 0) {
+            idx_out[r] = (be == INT_MAX) ? -1 : be;
+            sig_out[r] = bs;
+        }
+        S = __fadd_rn(S, bs);
     }
-    *S_out = S;
+    return S;
 }
 
 __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int T, int E, int k,
                                               const float *__restrict__ bias, float scale,
                                               int32_t *__restrict__ idx, float *__restrict__ w)
 {
+    __shared__ int s_idx[8][MAX_K];
+    __shared__ float s_sig[8][MAX_K];
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (t >= T) return;
-    int ce[MAX_K];
-    float cs[MAX_K], S;
-    warp_topk(logits + (size_t)t * E, E, k, bias, ce, cs, &S);
-    if (lane == 0) {
-#pragma unroll
-        for (int r = 0; r < MAX_K; ++r)
-            if (r < k) {
-                idx[(size_t)t * k + r] = ce[r];
-                w[(size_t)t * k + r] = __fmul_rn(__fdiv_rn(cs[r], S), scale);
-            }
+    const float S = warp_topk(logits + (size_t)t * E, E, k, bias, s_idx[warp], s_sig[warp]);
+    __syncwarp();
+    if (lane < k) {
+        idx[(size_t)t * k + lane] = s_idx[warp][lane];
+        w[(size_t)t * k + lane] = __fmul_rn(__fdiv_rn(s_sig[warp][lane], S), scale);
     }
 }
 
@@ -471,20 +469,17 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     if (tid == 0) *ra.route_counter = 0;
 
     __shared__ int s_idx[ROUTE_SMALL_MAX_T * MAX_K];
+    __shared__ float s_sig[ROUTE_SMALL_MAX_T * MAX_K];
     __shared__ int s_cnt[MAX_E], s_base[MAX_E], s_tile0[MAX_E], s_off[MAX_E];
     __shared__ int s_ntiles;
     if (warp < T) {
-        int ce[MAX_K];
-        float cs[MAX_K], S;
-        warp_topk(ra.logits + (size_t)warp * E, E, k, ra.bias, ce, cs, &S);
-        if (lane == 0) {
-#pragma unroll
-            for (int r = 0; r < MAX_K; ++r)
-                if (r < k) {
-                    s_idx[warp * k + r] = ce[r];
-                    ra.idx[(size_t)warp * k + r] = ce[r];
-                    ra.wts[(size_t)warp * k + r] = __fmul_rn(__fdiv_rn(cs[r], S), ra.routed_scale);
-                }
+        const float S = warp_topk(ra.logits + (size_t)warp * E, E, k, ra.bias, s_idx + warp * k,
+                                  s_sig + warp * k);
+        __syncwarp();
+        if (lane < k) {
+            ra.idx[(size_t)warp * k + lane] = s_idx[warp * k + lane];
+            ra.wts[(size_t)warp * k + lane] =
+                __fmul_rn(__fdiv_rn(s_sig[warp * k + lane], S), ra.routed_scale);
         }
     }
     __syncthreads();
