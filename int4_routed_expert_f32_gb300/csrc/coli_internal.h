@@ -71,6 +71,7 @@ struct RouteArgs {
     int n_sync;
     int *route_counter;             // blocks finished (reset by the last block)
     int *status;
+    unsigned long long *trace;      // optional phase log of the routing tail (null: off)
 };
 constexpr int ROUTE_SMALL_MAX_T = 8;
 

@@ -507,6 +507,8 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
         r.tile_expert = w.tile_expert; r.tile_pos0 = w.tile_pos0; r.tile_m = w.tile_m;
         r.n_tiles = w.n_tiles; r.sync = w.sync; r.n_sync = w.n_sync;
         r.route_counter = w.route_counter; r.status = w.status;
+        // routing-tail phase stamps go to the last block's slots of the trace log
+        r.trace = g.trace ? g.trace + (size_t)(g.trace_blocks - 1) * g.trace_cap * 2 : nullptr;
         LAUNCH_OK(launch_route_small(r, st));
     } else {
         LAUNCH_OK(launch_q8_0(x, (long)T * H, w.qx, w.dx, st));

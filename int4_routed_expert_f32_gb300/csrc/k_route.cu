@@ -460,11 +460,21 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
 
     // 3. the last block routes
     __shared__ int s_last;
+    unsigned long long *tr = ra.trace;
+    auto stamp = [&](int i) {
+        if (tr && tid == 0) {
+            unsigned long long t;
+            asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+            tr[i] = t;
+        }
+    };
+    stamp(0 + 16 * (blockIdx.x == 0));
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = (atomicAdd(ra.route_counter, 1) == (int)gridDim.x - 1);
     __syncthreads();
     if (!s_last) return;
+    stamp(1);
     __threadfence();
     if (tid == 0) *ra.route_counter = 0;
 
@@ -483,6 +493,7 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
         }
     }
     __syncthreads();
+    stamp(2);
     const int P = T * k;
     for (int ee = tid; ee < MAX_E; ee += 256) {
         int c = 0;
@@ -491,10 +502,12 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     }
     if (tid < P && (s_idx[tid] < 0 || s_idx[tid] >= E)) set_status(ra.status, ST_BAD_INDEX);
     __syncthreads();
+    stamp(3);
     if (warp == 0) scan_experts(s_cnt, E, T, ra.counts, ra.offsets, s_base, s_tile0, &s_ntiles);
     __syncthreads();
     if (tid < E) s_off[tid] = s_base[tid];
     __syncthreads();
+    stamp(4);
     if (tid < P) {
         const int ee = s_idx[tid];
         if (ee >= 0 && ee < E) {
@@ -508,8 +521,11 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
             ra.inv[tid] = -1;
         }
     }
+    stamp(5);
     write_tiles(T, P, E, s_cnt, s_tile0, s_off, s_ntiles, ra.pos_token, ra.tile_expert,
                 ra.tile_pos0, ra.tile_m, ra.n_tiles);
+    __syncthreads();
+    stamp(6);
 }
 
 int launch_route_small(const RouteArgs &r, cudaStream_t st)
