@@ -171,6 +171,51 @@ __device__ __noinline__ float warp_topk(const float *logits_row, int E, int k,
     return S;
 }
 
+// Top-k selection for one token by one warp over keys already in shared
+// memory (key = sigma + bias; taken experts are overwritten with -inf).
+// Lane 0 writes the experts in rank order to idx_out and their sigma to
+// sig_out; returns S = sum of the chosen sigma in rank order.  Every loop is
+// rolled: this runs once per token, on code no other block has fetched, so a
+// small body beats unrolling.
+__device__ __noinline__ float warp_select(float *key, const float *sig, int E, int k, int *idx_out,
+                                          float *sig_out)
+{
+    const int lane = threadIdx.x & 31;
+    float S = 0.0f;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        float bv = -__int_as_float(0x7f800000);
+        int be = INT_MAX;
+#pragma unroll 1
+        for (int e = lane; e < E; e += 32) {
+            const float v = key[e];
+            if (v != -__int_as_float(0x7f800000) && (be == INT_MAX || v > bv)) {
+                bv = v;
+                be = e;
+            }
+        }
+#pragma unroll 1
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(FULL, bv, o);
+            const int oe = __shfl_xor_sync(FULL, be, o);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        const float bs = (be == INT_MAX) ? 0.0f : sig[be];
+        __syncwarp();
+        if (lane == 0) {
+            idx_out[r] = (be == INT_MAX) ? -1 : be;
+            sig_out[r] = bs;
+            if (be != INT_MAX) key[be] = -__int_as_float(0x7f800000);
+        }
+        __syncwarp();
+        S = __fadd_rn(S, bs);
+    }
+    return S;
+}
+
 __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int T, int E, int k,
                                               const float *__restrict__ bias, float scale,
                                               int32_t *__restrict__ idx, float *__restrict__ w)
@@ -216,22 +261,22 @@ constexpr int MAX_E = 256;
 // Warp 0: exclusive scans of the per-expert counts and tile counts (E <= 256,
 // 8 per lane).  Writes counts/offsets (global), s_base/s_tile0 (shared) and
 // the total tile count (shared experts' tiles first).
-__device__ __forceinline__ void scan_experts(const int *s_cnt, int E, int T, int32_t *counts,
-                                             int32_t *offsets, int *s_base, int *s_tile0,
-                                             int *s_ntiles)
+__device__ __noinline__ void scan_experts(const int *s_cnt, int E, int T, int32_t *counts,
+                                          int32_t *offsets, int *s_base, int *s_tile0,
+                                          int *s_ntiles)
 {
+    // rolled loops: runs once per forward on code no other warp has fetched
     const int lane = threadIdx.x & 31;
-    int v[8], nt[8], sum = 0, tsum = 0;
-#pragma unroll
+    int sum = 0, tsum = 0;
+#pragma unroll 1
     for (int i = 0; i < 8; ++i) {
-        int e = lane * 8 + i;
-        v[i] = (e < E) ? s_cnt[e] : 0;
-        nt[i] = (v[i] + GEMV_MT - 1) / GEMV_MT;
-        sum += v[i];
-        tsum += nt[i];
+        const int e = lane * 8 + i;
+        const int v = (e < E) ? s_cnt[e] : 0;
+        sum += v;
+        tsum += (v + GEMV_MT - 1) / GEMV_MT;
     }
     int inc = sum, tinc = tsum;
-#pragma unroll
+#pragma unroll 1
     for (int o = 1; o < 32; o <<= 1) {
         int a = __shfl_up_sync(FULL, inc, o);
         int b = __shfl_up_sync(FULL, tinc, o);
@@ -239,17 +284,18 @@ __device__ __forceinline__ void scan_experts(const int *s_cnt, int E, int T, int
     }
     int run = inc - sum, trun = tinc - tsum;
     const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < 8; ++i) {
-        int e = lane * 8 + i;
+        const int e = lane * 8 + i;
+        const int v = (e < E) ? s_cnt[e] : 0;
         if (e < E) {
             s_base[e] = run;
             offsets[e] = run;
-            counts[e] = v[i];
+            counts[e] = v;
             s_tile0[e] = shared_tiles + trun;
         }
-        run += v[i];
-        trun += nt[i];
+        run += v;
+        trun += (v + GEMV_MT - 1) / GEMV_MT;
     }
     if (lane == 31) {
         offsets[E] = inc;
@@ -482,9 +528,18 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     __shared__ float s_sig[ROUTE_SMALL_MAX_T * MAX_K];
     __shared__ int s_cnt[MAX_E], s_base[MAX_E], s_tile0[MAX_E], s_off[MAX_E];
     __shared__ int s_ntiles;
+    __shared__ float s_key[ROUTE_SMALL_MAX_T][MAX_E], s_sg[ROUTE_SMALL_MAX_T][MAX_E];
+    // sigma and selection key of every (token, expert), all threads at once
+#pragma unroll 1
+    for (int i = tid; i < T * E; i += 256) {
+        const int t = i / E, ee = i - t * E;
+        const float sg = own_sigmoid(__ldcg(ra.logits + (size_t)t * E + ee));
+        s_sg[t][ee] = sg;
+        s_key[t][ee] = __fadd_rn(sg, ra.bias[ee]);
+    }
+    __syncthreads();
     if (warp < T) {
-        const float S = warp_topk(ra.logits + (size_t)warp * E, E, k, ra.bias, s_idx + warp * k,
-                                  s_sig + warp * k);
+        const float S = warp_select(s_key[warp], s_sg[warp], E, k, s_idx + warp * k, s_sig + warp * k);
         __syncwarp();
         if (lane < k) {
             ra.idx[(size_t)warp * k + lane] = s_idx[warp * k + lane];
