@@ -538,13 +538,34 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
         s_key[t][ee] = __fadd_rn(sg, ra.bias[ee]);
     }
     __syncthreads();
-    if (warp < T) {
-        const float S = warp_select(s_key[warp], s_sg[warp], E, k, s_idx + warp * k, s_sig + warp * k);
-        __syncwarp();
-        if (lane < k) {
-            ra.idx[(size_t)warp * k + lane] = s_idx[warp * k + lane];
-            ra.wts[(size_t)warp * k + lane] =
-                __fmul_rn(__fdiv_rn(s_sig[warp * k + lane], S), ra.routed_scale);
+    // Top-k by rank: expert e of token t ranks below every expert with a
+    // larger key, and below equal keys of lower index (lowest-index ties);
+    // it is selected, at position rank, iff rank < k.
+#pragma unroll 1
+    for (int i = tid; i < T * E; i += 256) {
+        const int t = i / E, ee = i - t * E;
+        const float ke = s_key[t][ee];
+        int rank = 0;
+#pragma unroll 4
+        for (int e2 = 0; e2 < E; ++e2) {
+            const float k2 = s_key[t][e2];
+            rank += (k2 > ke) | ((k2 == ke) & (e2 < ee));
+        }
+        if (rank < k) {
+            s_idx[t * k + rank] = ee;
+            s_sig[t * k + rank] = s_sg[t][ee];
+        }
+    }
+    __syncthreads();
+    if (tid < T) {
+        // S = sum of the chosen sigma in rank order, then the weights
+        float S = 0.0f;
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) S = __fadd_rn(S, s_sig[tid * k + r]);
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) {
+            ra.idx[(size_t)tid * k + r] = s_idx[tid * k + r];
+            ra.wts[(size_t)tid * k + r] = __fmul_rn(__fdiv_rn(s_sig[tid * k + r], S), ra.routed_scale);
         }
     }
     __syncthreads();
@@ -558,7 +579,34 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     if (tid < P && (s_idx[tid] < 0 || s_idx[tid] >= E)) set_status(ra.status, ST_BAD_INDEX);
     __syncthreads();
     stamp(3);
-    if (warp == 0) scan_experts(s_cnt, E, T, ra.counts, ra.offsets, s_base, s_tile0, &s_ntiles);
+    {
+        // exclusive scans of the counts and tile counts: one expert per thread,
+        // warp scans plus a scan of the eight warp totals
+        __shared__ int s_wsum[8], s_wtsum[8];
+        const int v = (tid < E) ? s_cnt[tid] : 0;
+        const int nt = (v + GEMV_MT - 1) / GEMV_MT;
+        int inc = v, tinc = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(FULL, inc, o), b = __shfl_up_sync(FULL, tinc, o);
+            if (lane >= o) { inc += a; tinc += b; }
+        }
+        if (lane == 31) { s_wsum[warp] = inc; s_wtsum[warp] = tinc; }
+        __syncthreads();
+        int base = 0, tbase = 0;
+        for (int w2 = 0; w2 < warp; ++w2) { base += s_wsum[w2]; tbase += s_wtsum[w2]; }
+        const int shared_tiles = (T + GEMV_MT - 1) / GEMV_MT;
+        if (tid < E) {
+            s_base[tid] = base + inc - v;
+            ra.offsets[tid] = base + inc - v;
+            ra.counts[tid] = v;
+            s_tile0[tid] = shared_tiles + tbase + tinc - nt;
+        }
+        if (tid == 255) {
+            ra.offsets[E] = base + inc;
+            s_ntiles = shared_tiles + tbase + tinc;
+        }
+    }
     __syncthreads();
     if (tid < E) s_off[tid] = s_base[tid];
     __syncthreads();
