@@ -156,6 +156,31 @@ int coli_moe_trace_read(unsigned long long *host, long long capacity, int *block
 /* Number of kernels the library launched since the last call (then reset). */
 long long coli_moe_launch_count(void);
 
+/* ---- routing without any device allocation --------------------------------
+ * This entry point has no counterpart in the colibri pages: it is a service
+ * for callers that must not allocate device memory (code running under
+ * another runtime's allocator or memory pool, processes whose device memory is
+ * fully reserved up front, serving loops that forbid allocation).  It runs
+ * the same router as coli_moe_layer_forward (logits in the fixed F32 order,
+ * sigmoid, +bias for selection, top-k with lowest-index ties, weights
+ * sigma_r / sum(sigma_sel) * routed_scale) with the shape passed in `s`
+ * (s->ffn and s->max_tok are ignored), and needs no coli_moe_configure().
+ *   x [n_tok][H] F32 (16-byte aligned), router_w [E][H] F32 (16-byte
+ *   aligned), router_bias [E] F32; outputs idx [n_tok][k] int32 (rank order)
+ *   and w [n_tok][k] F32, all device pointers owned by the caller.
+ * Its scratch (the logits) is a file-scope device array for at most
+ * COLI_STATIC_MAX_TOK tokens and 256 experts, held on every GPU that loads the
+ * library until exit; larger n_tok or E return COLI_E_INVAL.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current, so make that first call before any stream capture.  All
+ * calls share the one array: calls that overlap on the GPU (different
+ * streams, or different host threads) race on it. */
+#define COLI_STATIC_MAX_TOK 64
+int coli_moe_route_noalloc(const coli_moe_shape *s, const float *x, int n_tok,
+                           const float *router_w, const float *router_bias, int32_t *idx, float *w,
+                           void *stream);
+
 /* ---- stage entry points (tests; same conventions, configured shape) ------- */
 
 /* Q8_0 of n floats (n % 32 == 0): q [n] int8, d [n/32] F32 (same rule as the

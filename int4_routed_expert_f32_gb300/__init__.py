@@ -29,7 +29,7 @@ EXPORTS = (
     "coli_moe_launch_count", "coli_moe_trace_enable", "coli_moe_trace_read",
     "coli_moe_dbg_quantize", "coli_moe_dbg_route",
     "coli_moe_dbg_dispatch", "coli_moe_dbg_block_dots", "coli_moe_dbg_forward_intermediates",
-    "coli_moe_dbg_expert_hidden",
+    "coli_moe_dbg_expert_hidden", "coli_moe_route_noalloc",
 )
 
 
@@ -73,6 +73,7 @@ def _load():
         "coli_moe_dbg_block_dots": ([P, i, i, P, P, P], i),
         "coli_moe_dbg_forward_intermediates": ([P, i, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P], i),
         "coli_moe_dbg_expert_hidden": ([P, P, P, P, i, P, P, P, P], i),
+        "coli_moe_route_noalloc": ([ctypes.POINTER(_Shape), P, i, P, P, P, P, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -196,6 +197,25 @@ def trace_read():
 
 def launch_count() -> int:
     return int(_lib.coli_moe_launch_count())
+
+
+STATIC_MAX_TOK = 64
+
+
+def route_noalloc(x, router_w, router_bias, hidden, n_experts, top_k, routed_scale, idx=None, w=None,
+                  stream=None):
+    """Router for callers that cannot allocate device memory (see the header):
+    no configure() needed; scratch is a static device array of the library.
+    ``idx``/``w`` may be given pre-allocated by the caller."""
+    T = x.shape[0]
+    s = _Shape(hidden, 0, n_experts, top_k, routed_scale, 0)
+    if idx is None:
+        idx = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    if w is None:
+        w = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    _check(_lib.coli_moe_route_noalloc(ctypes.byref(s), _ptr(x), T, _ptr(router_w), _ptr(router_bias),
+                                       _ptr(idx), _ptr(w), _stream(stream)), "route_noalloc")
+    return idx, w
 
 
 # ---- stage entry points ---------------------------------------------------- #
