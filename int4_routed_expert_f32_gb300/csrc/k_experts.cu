@@ -143,12 +143,13 @@ static int ring_stages(int, int, int)
 size_t experts_smem_bytes(int H, int F) { return experts_smem_bytes_mt(H, F, GEMV_MT, ring_stages(H, F, GEMV_MT)); }
 
 // Split-form activations of one tile into shared memory (see block_dot):
-// xlo/xhi/xcb/xd are [MT][NB].  Loads are issued SU at a time per thread so
+// xlo/xhi/xcd are [MT][NB]; xcd holds (MAGIC_I - 8 * sum of the codes, the
+// block's F32 scale bits) so one 8-byte load serves both.  Loads are issued SU at a time per thread so
 // that a tile's staging costs about one L2 round trip.
 template <int MT>
 __device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const float *__restrict__ d,
                                            int K, int m, const int *rows, int row_limit,
-                                           uint4 *xlo, uint4 *xhi, int *xcb, float *xd, int *status)
+                                           uint4 *xlo, uint4 *xhi, int2 *xcd, int *status)
 {
     constexpr int SU = 4;
     const int NB = K / 32;
@@ -184,8 +185,7 @@ __device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const f
                 split_block(va[uu], vb[uu], &lo, &hi, &sum);
                 xlo[i] = lo;
                 xhi[i] = hi;
-                xcb[i] = MAGIC_I - 8 * sum;
-                xd[i] = vd[uu];
+                xcd[i] = make_int2(MAGIC_I - 8 * sum, __float_as_int(vd[uu]));
             }
         }
     }
@@ -214,8 +214,8 @@ __device__ __forceinline__ int block_dot_i(uint4 w, uint4 lo, uint4 hi, int cb)
 // can interleave.
 template <int MT, int NSUB, int BPS>
 __device__ __forceinline__ void stage_rows(const unsigned char *base, const int (&woff)[8], const uint4 *xlo,
-                                           const uint4 *xhi, const int *xcb, const float *xd, int NB,
-                                           int b0, int m, float (&acc)[MT])
+                                           const uint4 *xhi, const int2 *xcd, int NB, int b0, int m,
+                                           float (&acc)[MT])
 {
     uint4 wv[NSUB][BPS];
 #pragma unroll
@@ -228,19 +228,22 @@ __device__ __forceinline__ void stage_rows(const unsigned char *base, const int 
         if (t < m) {
             const int xb0 = t * NB + b0;
             int I[NSUB][BPS];
+            float dd[NSUB][BPS];
 #pragma unroll
             for (int c = 0; c < NSUB; ++c)
 #pragma unroll
                 for (int jj = 0; jj < BPS; ++jj) {
                     const int xb = xb0 + c * BPS + jj;
-                    I[c][jj] = block_dot_i(wv[c][jj], xlo[xb], xhi[xb], xcb[xb]);
+                    const int2 cd = xcd[xb];
+                    I[c][jj] = block_dot_i(wv[c][jj], xlo[xb], xhi[xb], cd.x);
+                    dd[c][jj] = __int_as_float(cd.y);
                 }
             float cacc = acc[t];
 #pragma unroll
             for (int c = 0; c < NSUB; ++c)
 #pragma unroll
                 for (int jj = 0; jj < BPS; ++jj)
-                    cacc = __fmaf_rn(xd[xb0 + c * BPS + jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
+                    cacc = __fmaf_rn(dd[c][jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
             acc[t] = cacc;
         }
     }
@@ -271,9 +274,8 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const int nstage = a.nstage;
     uint4 *xlo = reinterpret_cast<uint4 *>(ring + nstage * STAGE_BYTES);
     uint4 *xhi = xlo + MT * NBmax;
-    int *xcb = reinterpret_cast<int *>(xhi + MT * NBmax);
-    float *xd = reinterpret_cast<float *>(xcb + MT * NBmax);
-    float *red = xd + MT * NBmax;     // [MT][32] up-row sums
+    int2 *xcd = reinterpret_cast<int2 *>(xhi + MT * NBmax);
+    float *red = reinterpret_cast<float *>(xcd + MT * NBmax);     // [MT][32] up-row sums
     ExpertSmem &S = *reinterpret_cast<ExpertSmem *>(red + MT * 32);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -443,9 +445,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 }
                 named_barrier(BAR_CONSUMERS, CONSUMERS);
                 if (gu)
-                    stage_acts<MT>(a.qx, a.dx, H, m, S.tok, a.n_tok, xlo, xhi, xcb, xd, a.status);
+                    stage_acts<MT>(a.qx, a.dx, H, m, S.tok, a.n_tok, xlo, xhi, xcd, a.status);
                 else
-                    stage_acts<MT>(a.qh, a.dh, F, m, S.tok, a.P + a.n_tok, xlo, xhi, xcb, xd, a.status);
+                    stage_acts<MT>(a.qh, a.dh, F, m, S.tok, a.P + a.n_tok, xlo, xhi, xcd, a.status);
 #pragma unroll
                 for (int t = 0; t < GEMV_MT; ++t) staged_tok[t] = gu ? S.tok[t] : -1;
                 staged_m = gu ? m : -1;
@@ -462,9 +464,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             const unsigned char *base = ring + slot * STAGE_BYTES;
             const int b0 = s * nsub * BPS;
             if (nsub == 2)
-                stage_rows<MT, 2, BPS>(base, woff, xlo, xhi, xcb, xd, NB, b0, m, acc);
+                stage_rows<MT, 2, BPS>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
             else
-                stage_rows<MT, 1, BPS>(base, woff, xlo, xhi, xcb, xd, NB, b0, m, acc);
+                stage_rows<MT, 1, BPS>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
