@@ -50,11 +50,10 @@ constexpr int KC_MAX = 128;
 constexpr int NSUB_MAX = 2;                        // TMA boxes along K per stage
 constexpr int SUB_BYTES = STAGE_ROWS * KC_MAX;     // 8 KB: one box of 64 rows x 128 B
 constexpr int STAGE_BYTES = NSUB_MAX * SUB_BYTES;  // 16 KB
-constexpr int CONSUMER_WARPS = 4;
-constexpr int CONSUMERS = CONSUMER_WARPS * 32;     // two warp pairs, one lane per row in each
+constexpr int CONSUMER_WARPS = 2;
+constexpr int CONSUMERS = CONSUMER_WARPS * 32;     // one lane per stage row
 constexpr int EXPERT_THREADS = CONSUMERS + 32;
-constexpr int BAR_CONSUMERS = 1;                   // named barrier ids (0 = __syncthreads)
-constexpr int BAR_PAIRS = 2;
+constexpr int BAR_CONSUMERS = 1;                   // named barrier id (0 = __syncthreads)
 constexpr uint64_t WAIT_NS = 2000000000ull;        // 2 s bound on every wait
 
 __device__ __forceinline__ uint64_t globaltimer()
@@ -123,9 +122,8 @@ static size_t act_bytes(int H, int F, int mt)
 
 size_t experts_smem_bytes_mt(int H, int F, int mt, int nstage)
 {
-    // ring, activations, up-row sums, the pair hand-off tile [2][mt][64][8], control
     return 1024 /*align slack*/ + (size_t)nstage * STAGE_BYTES + act_bytes(H, F, mt) +
-           (size_t)mt * 32 * 4 + (size_t)2 * mt * 64 * 8 * 4 + sizeof(ExpertSmem);
+           (size_t)mt * 32 * 4 + sizeof(ExpertSmem);
 }
 
 // Ring depth.  More blocks per SM help more than deeper rings: each block's
@@ -251,70 +249,6 @@ __device__ __forceinline__ void stage_rows(const unsigned char *base, const int 
     }
 }
 
-// One stage for this lane's row, sub-box `half` of the two: the warp pair of
-// sub-box 1 computes its block dots and hands them over through `hand`
-// ([MT][64][8], this stage's parity); the pair of sub-box 0 computes its own,
-// waits for the hand-off, and folds all 16 in block order.
-template <int MT, int BPS>
-__device__ __forceinline__ void stage_rows_split(const unsigned char *base, const int (&woff)[8],
-                                                 const uint4 *xlo, const uint4 *xhi, const int2 *xcd,
-                                                 int NB, int b0, int m, int half, int r, int *hand,
-                                                 float (&acc)[MT])
-{
-    uint4 wv[BPS];
-#pragma unroll
-    for (int jj = 0; jj < BPS; ++jj)
-        wv[jj] = *reinterpret_cast<const uint4 *>(base + half * SUB_BYTES + woff[jj]);
-    int I[MT][BPS];
-    float dd[MT][BPS];
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-        if (t < m) {
-            const int xb0 = t * NB + b0 + half * BPS;
-#pragma unroll
-            for (int jj = 0; jj < BPS; ++jj) {
-                const int2 cd = xcd[xb0 + jj];
-                I[t][jj] = block_dot_i(wv[jj], xlo[xb0 + jj], xhi[xb0 + jj], cd.x);
-                dd[t][jj] = __int_as_float(cd.y);
-            }
-        }
-    }
-    if (half == 1) {
-#pragma unroll
-        for (int t = 0; t < MT; ++t)
-            if (t < m) {
-                int4 *h4 = reinterpret_cast<int4 *>(hand + (t * 64 + r) * 8);
-                h4[0] = make_int4(I[t][0], I[t][1], I[t][2], I[t][3]);
-                if (BPS == 8) h4[1] = make_int4(I[t][4 % BPS], I[t][5 % BPS], I[t][6 % BPS], I[t][7 % BPS]);
-            }
-    }
-    named_barrier(BAR_PAIRS, CONSUMERS);
-    if (half == 0) {
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-            if (t < m) {
-                const int4 *h4 = reinterpret_cast<const int4 *>(hand + (t * 64 + r) * 8);
-                int I2[BPS];
-                const int4 q0 = h4[0];
-                I2[0] = q0.x; I2[1 % BPS] = q0.y; I2[2 % BPS] = q0.z; I2[3 % BPS] = q0.w;
-                if (BPS == 8) {
-                    const int4 q1 = h4[1];
-                    I2[4 % BPS] = q1.x; I2[5 % BPS] = q1.y; I2[6 % BPS] = q1.z; I2[7 % BPS] = q1.w;
-                }
-                const int2 *cd2 = xcd + t * NB + b0 + BPS;
-                float c = acc[t];
-#pragma unroll
-                for (int jj = 0; jj < BPS; ++jj)
-                    c = __fmaf_rn(dd[t][jj], __int_as_float(I[t][jj]) - MAGIC_F, c);
-#pragma unroll
-                for (int jj = 0; jj < BPS; ++jj)
-                    c = __fmaf_rn(__int_as_float(cd2[jj].y), __int_as_float(I2[jj]) - MAGIC_F, c);
-                acc[t] = c;
-            }
-        }
-    }
-}
-
 // Decode unit u: gate/up units first (tile-major), then down units.
 __device__ __forceinline__ void decode_unit(long u, long n_gu, int G, int CH, bool *gu, int *tile, int *j)
 {
@@ -342,8 +276,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     uint4 *xhi = xlo + MT * NBmax;
     int2 *xcd = reinterpret_cast<int2 *>(xhi + MT * NBmax);
     float *red = reinterpret_cast<float *>(xcd + MT * NBmax);     // [MT][32] up-row sums
-    int *hand = reinterpret_cast<int *>(red + MT * 32);            // [2][MT][64][8]
-    ExpertSmem &S = *reinterpret_cast<ExpertSmem *>(hand + 2 * MT * 64 * 8);
+    ExpertSmem &S = *reinterpret_cast<ExpertSmem *>(red + MT * 32);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, F = a.F, KC = a.KC;
@@ -448,10 +381,8 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     }
 
     // -------------------------------- consumers --------------------------------
-    const int r = threadIdx.x & 63;           // this lane's weight row in the stage (0..63)
-    const int half = threadIdx.x >> 6;        // warp pair: sub-box 0 (folds) or 1 (hands over)
+    const int r = threadIdx.x;                // this lane's weight row in the stage (0..63)
     const bool swz = (KC == 128);
-    uint32_t hand_par = 0;
     int woff[8];
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) woff[jj] = r * KC + 16 * (swz ? (jj ^ (r & 7)) : jj);
@@ -532,13 +463,10 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         {
             const unsigned char *base = ring + slot * STAGE_BYTES;
             const int b0 = s * nsub * BPS;
-            if (nsub == 2) {
-                stage_rows_split<MT, BPS>(base, woff, xlo, xhi, xcd, NB, b0, m, half, r,
-                                          hand + hand_par * (MT * 64 * 8), acc);
-                hand_par ^= 1;
-            } else if (half == 0) {
+            if (nsub == 2)
+                stage_rows<MT, 2, BPS>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
+            else
                 stage_rows<MT, 1, BPS>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
-            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -550,7 +478,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 
         // ---- unit epilogue ----
         if (gu) {
-            // pair 0 holds the sums: rows 0..31 gate rows 32j.., rows 32..63 the matching up rows
+            // rows 0..31: gate rows 32j.., rows 32..63: the matching up rows
             if (warp == 1)
                 for (int t = 0; t < m; ++t) red[t * 32 + lane] = acc[t];
             named_barrier(BAR_CONSUMERS, CONSUMERS);
@@ -578,12 +506,10 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             trace_event(a, 4, u);
         } else {
             const int row = 64 * j + r;
-            if (half == 0) {
-                const float sd = ers[2 * F + row];
+            const float sd = ers[2 * F + row];
 #pragma unroll
-                for (int t = 0; t < MT; ++t)
-                    if (t < m) a.y[(size_t)(pos0 + t) * H + row] = __fmul_rn(sd, acc[t]);
-            }
+            for (int t = 0; t < MT; ++t)
+                if (t < m) a.y[(size_t)(pos0 + t) * H + row] = __fmul_rn(sd, acc[t]);
             named_barrier(BAR_CONSUMERS, CONSUMERS);
             if (threadIdx.x == 0) {
                 __threadfence();
