@@ -67,11 +67,11 @@ typedef struct {
     int max_tok;         /* largest n_tok any later call will pass             */
 } coli_moe_shape;
 
-/* Execution path of the expert matmuls. */
+/* Execution path of the expert matmuls.  Both give bit-identical results. */
 typedef enum {
-    COLI_PATH_AUTO = 0,  /* per-expert choice by tokens routed to the expert   */
-    COLI_PATH_GEMV = 1,  /* streaming int4 x int8 dp4a kernels for every expert */
-    COLI_PATH_GEMM = 2   /* tensor-core grouped GEMM for every routed expert    */
+    COLI_PATH_AUTO = 0,  /* per forward: GEMM when n_tok >= the threshold       */
+    COLI_PATH_GEMV = 1,  /* streaming int4 x int8 dp4a kernels (decode batches) */
+    COLI_PATH_GEMM = 2   /* tcgen05 grouped GEMM over the batch union (prefill) */
 } coli_path;
 
 /* Validate `s`, remember it and allocate the library-owned workspace for up to
@@ -110,8 +110,13 @@ int coli_moe_layer_forward_hostio(const float *x_host, int n_tok,
                                   float *out_host, void *stream);
 
 /* Choose the expert-matmul path for later forwards (default COLI_PATH_AUTO).
- * `gemm_min_tokens`: with COLI_PATH_AUTO, an expert receiving at least this many
- * tokens uses the grouped GEMM (<= 0 keeps the built-in threshold). */
+ * `gemm_min_tokens`: with COLI_PATH_AUTO, a forward of at least this many
+ * tokens runs the grouped tensor-core GEMM (the batch union of all experts:
+ * gather of the activation codes by dispatch position, gate/up GEMM with
+ * SiLU*up and Q8_0 of h, down GEMM, combine), a smaller one the streaming GEMV
+ * kernel; <= 0 keeps the built-in threshold (COLI_GEMM_MIN_TOKENS).  Returns
+ * COLI_E_INVAL for an unknown path.  Takes effect at the next forward. */
+#define COLI_GEMM_MIN_TOKENS 64
 int coli_moe_set_path(int path, int gemm_min_tokens);
 
 /* Synchronise `stream`, then read and clear the device status word.

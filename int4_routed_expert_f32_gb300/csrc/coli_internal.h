@@ -52,6 +52,35 @@ struct ExpertArgs {
     int trace_cap;                  // events per block
 };
 
+// Tensor maps of one grouped-GEMM launch: the bf16 activation codes by
+// dispatch position (2-D, box 64 x 128, 128-byte swizzle) and the packed
+// weight rows of the routed experts and of the shared expert (3-D, box
+// 32 bytes x 64 or 128 rows x 1, no swizzle).
+struct GemmMaps {
+    CUtensorMap act;
+    CUtensorMap w;
+    CUtensorMap sw;
+};
+
+// Argument block of the grouped-GEMM kernels (gate/up and down).
+struct GemmArgs {
+    int H, F, E, T;
+    const int32_t *n_items;          // device scalar
+    const int32_t *item_expert;      // [n_items] expert (E = shared)
+    const int32_t *item_pos0;        // [n_items] first dispatch position
+    const int32_t *item_m;           // [n_items] positions in the item (1..128)
+    const int32_t *pos_token;        // [P+T]
+    const float *dx;                 // [T][H/32] activation block scales
+    const float *expert_rs;          // [E][2F+H]
+    const float *shared_rs;          // [2F+H]
+    int8_t *qh;                      // [P+T][F] requantised hidden, by position
+    float *dh;                       // [P+T][F/32]
+    uint16_t *qhb;                   // [P+T][F] the same codes as bf16 (down-GEMM operand)
+    float *h_dbg;                    // optional [P+T][F]
+    float *y;                        // [P+T][H]
+    int *status;
+};
+
 // Small-batch routing in one launch: Q8_0 of x, router logits, top-k, dispatch,
 // tile list, and zeroing of the expert kernel's counters.
 struct RouteArgs {
@@ -103,5 +132,17 @@ int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cud
 int launch_gather_pairs(const int32_t *inv, int T, int k, int P, const int8_t *qh, const float *dh,
                         const float *y, int F, int H, int8_t *qh_out, float *dh_out, float *y_out,
                         cudaStream_t st);
+
+// Grouped tensor-core path.
+int max_gemm_items(int T, int k, int E);
+int gemm_tile_rows();
+size_t gemm_smem_bytes();
+int launch_gather_x(const int8_t *qx, const int32_t *pos_token, const int32_t *offsets, int E, int P, int R,
+                    int T, int H, uint16_t *xg, int *status, cudaStream_t st);
+int launch_gemm_items(const int32_t *counts, const int32_t *offsets, int E, int T, int P, int32_t *item_expert,
+                      int32_t *item_pos0, int32_t *item_m, int32_t *n_items, cudaStream_t st);
+int launch_gemm(bool gateup, const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st);
+int launch_combine(const float *y, const int32_t *inv, const float *wts, int T, int k, int P, int H, float *out,
+                   cudaStream_t st);
 
 }  // namespace coli

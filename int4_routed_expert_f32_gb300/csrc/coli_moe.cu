@@ -6,8 +6,12 @@
 //   logits in the fixed F32 order, sigmoid/top-k/renormalisation, the stable
 //   token->expert dispatch and the tile list;
 //   routing, T > 8: k_q8_0, k_router_logits, k_topk, k_dispatch;
-//   experts: one persistent launch (k_experts): gate/up + SiLU*up + Q8_0 of h,
-//   down, and the gate-weighted combine with the shared expert.
+//   experts, streaming path (decode batches): one persistent launch
+//   (k_experts): gate/up + SiLU*up + Q8_0 of h, down, and the gate-weighted
+//   combine with the shared expert;
+//   experts, grouped tensor-core path (prefill batches): k_gather_x (bf16
+//   codes by dispatch position), k_gemm_items (tiles of 128 positions per
+//   expert), k_gemm<gate/up> (+ SiLU*up + Q8_0 of h), k_gemm<down>, k_combine.
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -40,6 +44,11 @@ struct Workspace {
     float *y = nullptr;
     float *x_io = nullptr, *out_io = nullptr;
     int *status = nullptr;
+    // grouped tensor-core path
+    uint16_t *xg = nullptr;          // [R'][H] bf16 codes of x by dispatch position
+    uint16_t *qhb = nullptr;         // [R'][F] bf16 codes of h by dispatch position
+    int32_t *item_expert = nullptr, *item_pos0 = nullptr, *item_m = nullptr, *n_items = nullptr;
+    int rows_alloc = 0;              // R' = max(P + T, 128) rows of xg and qhb
 };
 
 struct State {
@@ -61,6 +70,11 @@ struct State {
     ExpertMaps maps{};
     const void *maps_key[2] = {nullptr, nullptr};
     bool maps_valid = false;
+    // grouped-GEMM maps: activations (fixed workspace buffers) and weights
+    CUtensorMap act_x{}, act_h{};
+    GemmMaps gemm_gu{}, gemm_dn{};
+    const void *gemm_key[2] = {nullptr, nullptr};
+    bool gemm_valid = false;
 };
 
 static State g;
@@ -164,6 +178,44 @@ static bool expert_maps(const uint8_t *ew4, int E, const uint8_t *sw4, ExpertMap
     return true;
 }
 
+// 2-D map over bf16 codes [rows][K] with 128-byte swizzle, box 64 x 128.
+static bool encode_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {K * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Weight maps of the grouped GEMM: 32 bytes (64 weights) of a row per stage,
+// 64 rows per box for gate/up (two boxes: gate rows, then the matching up
+// rows), 128 rows for down.
+static bool gemm_weight_maps(const uint8_t *ew4, int E, const uint8_t *sw4)
+{
+    if (g.gemm_valid && g.gemm_key[0] == ew4 && g.gemm_key[1] == sw4) return true;
+    const uint64_t H = g.s.hidden, F = g.s.ffn, stride = 3 * F * H / 2;
+    GemmMaps gu{}, dn{};
+    bool ok = encode_rows(&gu.w, ew4, H / 2, 2 * F, (uint64_t)E, stride, 64, 32) &&
+              encode_rows(&gu.sw, sw4, H / 2, 2 * F, 1, stride, 64, 32) &&
+              encode_rows(&dn.w, ew4 + F * H, F / 2, H, (uint64_t)E, stride, 128, 32) &&
+              encode_rows(&dn.sw, sw4 + F * H, F / 2, H, 1, stride, 128, 32);
+    if (!ok) return false;
+    gu.act = g.act_x;
+    dn.act = g.act_h;
+    g.gemm_gu = gu;
+    g.gemm_dn = dn;
+    g.gemm_key[0] = ew4;
+    g.gemm_key[1] = sw4;
+    g.gemm_valid = true;
+    return true;
+}
+
 static int check_shape(const coli_moe_shape *s)
 {
     if (!s) return COLI_E_INVAL;
@@ -218,6 +270,8 @@ int coli_moe_configure(const coli_moe_shape *s)
     const size_t E = (size_t)s->n_experts, k = (size_t)s->top_k;
     const size_t P = T * k, R = P + T;
     const size_t tiles = (size_t)max_gemv_tiles((int)T, (int)k, (int)E);
+    const size_t items = (size_t)max_gemm_items((int)T, (int)k, (int)E);
+    const size_t Ra = R > 128 ? R : 128;
     // carve one allocation; every piece 256-byte aligned
     struct Piece { void **dst; size_t bytes; };
     Workspace w;
@@ -244,6 +298,12 @@ int coli_moe_configure(const coli_moe_shape *s)
         {(void **)&w.x_io, T * H * 4},
         {(void **)&w.out_io, T * H * 4},
         {(void **)&w.status, 4},
+        {(void **)&w.xg, Ra * H * 2},
+        {(void **)&w.qhb, Ra * F * 2},
+        {(void **)&w.item_expert, items * 4},
+        {(void **)&w.item_pos0, items * 4},
+        {(void **)&w.item_m, items * 4},
+        {(void **)&w.n_items, 4},
     };
     size_t total = 0;
     for (auto &p : pieces) total += align_up(p.bytes, 256);
@@ -265,6 +325,12 @@ int coli_moe_configure(const coli_moe_shape *s)
     }
     CUDA_OK(cudaDeviceSynchronize());
     w.n_sync = (int)(tiles + H / 64 + 2);
+    w.rows_alloc = (int)Ra;
+    if (!encode_act(&g.act_x, w.xg, H, Ra) || !encode_act(&g.act_h, w.qhb, F, Ra)) {
+        cudaFree(base);
+        return COLI_E_CUDA;
+    }
+    g.gemm_valid = false;
     g.ws = w;
     g.max_tiles = (int)tiles;
     g.maps_valid = false;
@@ -278,7 +344,6 @@ int coli_moe_configure(const coli_moe_shape *s)
 int coli_moe_set_path(int path, int gemm_min_tokens)
 {
     if (path < COLI_PATH_AUTO || path > COLI_PATH_GEMM) return COLI_E_INVAL;
-    if (path == COLI_PATH_GEMM) return COLI_E_UNIMPL;
     g.path = path;
     g.gemm_min_tokens = gemm_min_tokens;
     return COLI_OK;
@@ -494,8 +559,14 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
     Workspace &w = g.ws;
     const int T = n_tok, H = s.hidden, E = s.n_experts, k = s.top_k;
 
+    const int thr = g.gemm_min_tokens > 0 ? g.gemm_min_tokens : COLI_GEMM_MIN_TOKENS;
+    const bool use_gemm = g.path == COLI_PATH_GEMM || (g.path == COLI_PATH_AUTO && T >= thr);
     ExpertMaps maps;
-    if (!expert_maps(expert_w4, E, shared_w4, &maps)) return COLI_E_CUDA;
+    if (use_gemm) {
+        if (!gemm_weight_maps(expert_w4, E, shared_w4)) return COLI_E_CUDA;
+    } else if (!expert_maps(expert_w4, E, shared_w4, &maps)) {
+        return COLI_E_CUDA;
+    }
 
     if (T <= ROUTE_SMALL_MAX_T) {
         RouteArgs r{};
@@ -519,9 +590,33 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
                                   w.status, st));
     }
 
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (use_gemm) {
+        const int P = T * k, F = s.ffn;
+        LAUNCH_OK(launch_gather_x(w.qx, w.pos_token, w.offsets, E, P, P + T, T, H, w.xg, w.status, st));
+        LAUNCH_OK(launch_gemm_items(w.counts, w.offsets, E, T, P, w.item_expert, w.item_pos0, w.item_m,
+                                    w.n_items, st));
+        GemmArgs ga{};
+        ga.H = H; ga.F = F; ga.E = E; ga.T = T;
+        ga.n_items = w.n_items; ga.item_expert = w.item_expert; ga.item_pos0 = w.item_pos0;
+        ga.item_m = w.item_m; ga.pos_token = w.pos_token; ga.dx = w.dx;
+        ga.expert_rs = expert_rowscale; ga.shared_rs = shared_rowscale;
+        ga.qh = w.qh; ga.dh = w.dh; ga.qhb = w.qhb; ga.h_dbg = nullptr; ga.y = w.y;
+        ga.status = w.status;
+        if (g.timing) {
+            int r = timing_events(&e0, &e1);
+            if (r != COLI_OK) return r;
+            CUDA_OK(cudaEventRecord(e0, st));
+        }
+        LAUNCH_OK(launch_gemm(true, g.gemm_gu, ga, g.num_sms, st));
+        if (g.timing) CUDA_OK(cudaEventRecord(e1, st));
+        LAUNCH_OK(launch_gemm(false, g.gemm_dn, ga, g.num_sms, st));
+        LAUNCH_OK(launch_combine(w.y, w.inv, w.wts, T, k, P, H, out, st));
+        return COLI_OK;
+    }
+
     ExpertArgs a = expert_args(T, expert_rowscale, shared_rowscale);
     a.out = out;
-    cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (g.timing) {
         int r = timing_events(&e0, &e1);
         if (r != COLI_OK) return r;

@@ -1,0 +1,630 @@
+// k_gemm.cu -- grouped expert GEMM on the 5th-generation tensor cores
+// (tcgen05 MMA, TMEM accumulators, TMA-staged operands) for batches in which
+// experts receive many tokens (prefill, large verify batches): the batch-union
+// MoE of "Colibri: an AI engine running a 744B model in 25GB of RAM"
+// (alphamatch.ai), section "Technical excellence", with the integer block dot
+// products of "colibri: a pure-C inference engine ..." (discuss.pytorch.kr),
+// section "Key features".
+//
+// Exactness.  The method multiplies int4 weights (-8..7) by int8 activations
+// (-127..127) and sums each 32-element block in int32.  Both factors are exact
+// in bf16, every product is exact, and a 32-term block sum (|sum| < 2^15) is
+// exact in an F32 accumulator, so tcgen05.mma.kind::f16 on bf16 operands
+// produces exactly the integers I_b.  (There is no kind::i8 on sm_103a.)  Each
+// Q8_0 block gets its own TMEM accumulator (two K=16 MMAs), and the drain
+// folds the blocks into F32 in ascending order, acc = fma(d_b, I_b, acc), the
+// same operation sequence as the GEMV kernel and the CPU oracle, so the result
+// is bit-identical to both.
+//
+// Tile.  M = 128 dispatch positions (rows of operand A: the gathered bf16
+// codes of one expert's tokens), N = 128 weight rows (gate/up: 64 gate rows
+// and the 64 matching up rows; down: 128 output rows), K = 64 per pipeline
+// stage (two blocks).  A drain thread owns one token row and 64 columns, so
+// the per-(token, block) scale is one scalar, and SiLU(gate)*up and the Q8_0
+// requantisation of h stay inside threads.
+//
+// Warp roles (14 warps, one CTA per SM, persistent over units):
+//   0      TMA producer (activation tile + packed weight rows)
+//   1      MMA issuer, owner of the TMEM allocation
+//   2..5   weight converters: packed int4 -> bf16 in the 128-byte-swizzled
+//          K-major layout the MMA reads
+//   6..13  drain + epilogue; warp w reads TMEM lanes 32*(w%4).. and the
+//          column half (w-6)/4
+//
+// Element order inside each 8-element K chunk, for both operands:
+// (k0, k2, k4, k6, k1, k3, k5, k7).  It is what splitting the packed bytes
+// into low and high nibbles gives without shuffling; the gathered activations
+// are written in the same order (one fixed permutation of K applied to both
+// operands leaves every dot product unchanged).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "coli_common.cuh"
+#include "coli_internal.h"
+#include "tma.cuh"
+
+namespace coli {
+
+constexpr int GM = 128;                 // positions per tile (MMA M)
+constexpr int GN = 128;                 // weight rows per tile (MMA N)
+constexpr int GK = 64;                  // K per stage (two Q8_0 blocks)
+constexpr int G_STAGES = 4;
+constexpr int G_NACC = 4;               // TMEM accumulators (one per block in flight)
+constexpr int A_BYTES = GM * GK * 2;    // 16 KB bf16, swizzled
+constexpr int B_BYTES = GN * GK * 2;    // 16 KB bf16, swizzled
+constexpr int RAW_BYTES = GN * GK / 2;  // 4 KB packed int4
+constexpr int XCH_LD = 65;              // padded row of the gate/up exchange tile
+constexpr int G_CONV_WARPS = 4;
+constexpr int G_DRAIN_WARPS = 8;
+constexpr int G_THREADS = 32 * (2 + G_CONV_WARPS + G_DRAIN_WARPS);
+constexpr int G_TMEM_COLS = G_NACC * GN;
+constexpr int BAR_DRAIN = 3;
+constexpr uint64_t G_WAIT_NS = 2000000000ull;
+
+static_assert(G_TMEM_COLS <= 512, "TMEM has 512 columns");
+
+__device__ __forceinline__ uint64_t g_timer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded mbarrier wait that also gives up as soon as another warp aborted.
+__device__ __forceinline__ bool g_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = g_timer();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (g_timer() - t0 > G_WAIT_NS) return false;
+    }
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart, descriptor version 1.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> F32, both operands K-major, M = GM, N = GN.
+constexpr uint32_t UMMA_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GN >> 3) << 17) |
+                                ((uint32_t)(GM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem, uint64_t da, uint64_t db, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(tmem), "l"(da), "l"(db), "r"(UMMA_IDESC), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes (one F32 per lane and column).
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(addr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Eight int8 codes (natural order, little-endian in c) -> 16 bytes of bf16 in
+// chunk order (k0, k2, k4, k6, k1, k3, k5, k7).  |code| <= 127 is exact in bf16.
+__device__ __forceinline__ uint4 codes_to_bf16_chunk(uint2 c)
+{
+    const uint32_t lo = __byte_perm(c.x, c.y, 0x6420), hi = __byte_perm(c.x, c.y, 0x7531);
+    const uint32_t src[2] = {lo, hi};
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const float a = (float)(int8_t)(src[h] >> (16 * p));
+            const float b = (float)(int8_t)(src[h] >> (16 * p + 8));
+            w[2 * h + p] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 4 bytes of packed nibbles (8 weights; element 2i in the low nibble of byte
+// i) -> 16 bytes of bf16 (nibble - 8) in chunk order.  The bf16 pattern 0x43nn
+// (nn < 16) is 128 + nn; subtracting 136 leaves nn - 8 exactly.
+__device__ __forceinline__ uint4 nibbles_to_bf16_chunk(uint32_t w)
+{
+    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t C = 0x43434343u;
+    uint32_t o[4] = {__byte_perm(lo, C, 0x4140), __byte_perm(lo, C, 0x4342), __byte_perm(hi, C, 0x4140),
+                     __byte_perm(hi, C, 0x4342)};
+    const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&o[i]);
+        v = __hsub2(v, bias);
+        o[i] = *reinterpret_cast<uint32_t *>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------------------
+// Gather: the bf16 chunk-ordered codes of every used dispatch position (the A
+// operand of the gate/up GEMM).  Positions [offsets[E], P) hold no pair (an
+// invalid expert index) and are skipped.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_gather_x(const int8_t *__restrict__ qx,
+                                                  const int32_t *__restrict__ pos_token,
+                                                  const int32_t *__restrict__ offsets, int E, int P, int R,
+                                                  int T, int H, uint16_t *__restrict__ xg, int *status)
+{
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;   // one 8-element chunk
+    const int per = H / 8;
+    if (i >= (long)R * per) return;
+    const int pos = (int)(i / per), c = (int)(i - (long)pos * per);
+    if (pos < P && pos >= offsets[E]) return;
+    const int tok = pos_token[pos];
+    if (tok < 0 || tok >= T) {
+        set_status(status, ST_BAD_INDEX);
+        return;
+    }
+    const uint2 codes = *reinterpret_cast<const uint2 *>(qx + (size_t)tok * H + (size_t)c * 8);
+    reinterpret_cast<uint4 *>(xg + (size_t)pos * H)[c] = codes_to_bf16_chunk(codes);
+}
+
+// GEMM work items: each expert's dispatch positions in tiles of GM, the shared
+// expert (rows P .. P+T-1) first, then routed experts in ascending id.
+__global__ void k_gemm_items(const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int E,
+                             int T, int P, int32_t *item_expert, int32_t *item_pos0, int32_t *item_m,
+                             int32_t *n_items)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int n = 0;
+    for (int p = 0; p < T; p += GM) {
+        item_expert[n] = E;
+        item_pos0[n] = P + p;
+        item_m[n] = min(GM, T - p);
+        ++n;
+    }
+    for (int e = 0; e < E; ++e)
+        for (int p = 0; p < counts[e]; p += GM) {
+            item_expert[n] = e;
+            item_pos0[n] = offsets[e] + p;
+            item_m[n] = min(GM, counts[e] - p);
+            ++n;
+        }
+    *n_items = n;
+}
+
+// Combine: out[t] = y[shared row of t], then + w_r * y[pair (t, r)] for the
+// ranks r in order, one fused multiply-add each (the method's weighted sum of
+// the shared expert and the k routed experts).
+__global__ void __launch_bounds__(256) k_combine(const float *__restrict__ y, const int32_t *__restrict__ inv,
+                                                 const float *__restrict__ wts, int T, int k, int P, int H,
+                                                 float *__restrict__ out)
+{
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;   // 4 columns
+    const int per = H / 4;
+    if (i >= (long)T * per) return;
+    const int t = (int)(i / per), c = (int)(i - (long)t * per);
+    float4 o = reinterpret_cast<const float4 *>(y + (size_t)(P + t) * H)[c];
+    for (int r = 0; r < k; ++r) {
+        const int pos = inv[(size_t)t * k + r];
+        if (pos < 0 || pos >= P) continue;
+        const float w = wts[(size_t)t * k + r];
+        const float4 v = reinterpret_cast<const float4 *>(y + (size_t)pos * H)[c];
+        o.x = __fmaf_rn(w, v.x, o.x);
+        o.y = __fmaf_rn(w, v.y, o.y);
+        o.z = __fmaf_rn(w, v.z, o.z);
+        o.w = __fmaf_rn(w, v.w, o.w);
+    }
+    reinterpret_cast<float4 *>(out + (size_t)t * H)[c] = o;
+}
+
+struct GemmSmem {
+    alignas(8) uint64_t full[G_STAGES];      // activation tile + packed weights landed (TMA)
+    alignas(8) uint64_t conv[G_STAGES];      // weights converted to bf16
+    alignas(8) uint64_t empty[G_STAGES];     // the stage's MMAs completed
+    alignas(8) uint64_t tfull[G_NACC];       // a block's accumulator is ready
+    alignas(8) uint64_t tempty[G_NACC];      // a block's accumulator was read
+    uint32_t tmem_base;
+    int abort;
+};
+
+size_t gemm_smem_bytes()
+{
+    return 1024 + (size_t)G_STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + (size_t)GM * XCH_LD * 4 +
+           sizeof(GemmSmem);
+}
+
+// GATEUP: A = gathered x codes (K = H), B = gate/up rows; epilogue SiLU*up and
+// Q8_0 of h.  Otherwise A = h codes (K = F), B = down rows; epilogue y.
+template <bool GATEUP>
+__global__ void __launch_bounds__(G_THREADS, 1)
+k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char *sA = smem;                                   // [G_STAGES][A_BYTES]
+    unsigned char *sB = sA + G_STAGES * A_BYTES;                // [G_STAGES][B_BYTES]
+    unsigned char *sRaw = sB + G_STAGES * B_BYTES;              // [G_STAGES][RAW_BYTES]
+    float *xch = reinterpret_cast<float *>(sRaw + G_STAGES * RAW_BYTES);   // [GM][XCH_LD]
+    GemmSmem &S = *reinterpret_cast<GemmSmem *>(xch + GM * XCH_LD);
+    volatile int *abort = &S.abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = g.H, F = g.F;
+    const int K = GATEUP ? H : F;
+    const int nst = K / GK;                         // stages per unit
+    const int nb = K / 32;                          // blocks per unit
+    const int per_item = GATEUP ? F / 64 : H / GN;  // weight tiles per item
+    const long n_units = (long)(*g.n_items) * per_item;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G_STAGES; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.conv[s], G_CONV_WARPS);
+            mbar_init(&S.empty[s], 1);
+        }
+        for (int b = 0; b < G_NACC; ++b) {
+            mbar_init(&S.tfull[b], 1);
+            mbar_init(&S.tempty[b], G_DRAIN_WARPS);
+        }
+        S.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&maps.act);
+        prefetch_tmap(&maps.w);
+        prefetch_tmap(&maps.sw);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&S.tmem_base)), "r"(G_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            long sc = 0;   // stages issued
+            for (long u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+                const int item = (int)(u / per_item), j = (int)(u - (long)item * per_item);
+                const int e = g.item_expert[item], pos0 = g.item_pos0[item];
+                const bool shared = (e == g.E);
+                const void *wmap = shared ? (const void *)&maps.sw : (const void *)&maps.w;
+                const int z = shared ? 0 : e;
+                for (int s = 0; s < nst; ++s, ++sc) {
+                    const int slot = (int)(sc % G_STAGES);
+                    const long rnd = sc / G_STAGES;
+                    if (rnd > 0 && !g_wait(&S.empty[slot], (uint32_t)((rnd - 1) & 1), abort)) {
+                        if (!*abort) set_status(g.status, ST_TIMEOUT);
+                        *abort = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&S.full[slot], A_BYTES + RAW_BYTES);
+                    tma_load_2d(sA + slot * A_BYTES, &maps.act, s * GK, pos0, &S.full[slot]);
+                    unsigned char *raw = sRaw + slot * RAW_BYTES;
+                    if (GATEUP) {
+                        tma_load_3d(raw, wmap, s * (GK / 2), 64 * j, z, &S.full[slot], pol);
+                        tma_load_3d(raw + 64 * (GK / 2), wmap, s * (GK / 2), F + 64 * j, z, &S.full[slot], pol);
+                    } else {
+                        tma_load_3d(raw, wmap, s * (GK / 2), GN * j, z, &S.full[slot], pol);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            long sc = 0, bc = 0;   // stages consumed, blocks accumulated
+            for (long u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+                for (int s = 0; s < nst && !*abort; ++s, ++sc) {
+                    const int slot = (int)(sc % G_STAGES);
+                    const uint32_t par = (uint32_t)((sc / G_STAGES) & 1);
+                    if (!g_wait(&S.full[slot], par, abort) || !g_wait(&S.conv[slot], par, abort)) {
+                        if (!*abort) set_status(g.status, ST_TIMEOUT);
+                        *abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + slot * A_BYTES), b0 = smem_u32(sB + slot * B_BYTES);
+                    for (int blk = 0; blk < 2; ++blk, ++bc) {
+                        const int acc = (int)(bc % G_NACC);
+                        const long use = bc / G_NACC;
+                        if (use > 0 && !g_wait(&S.tempty[acc], (uint32_t)((use - 1) & 1), abort)) {
+                            if (!*abort) set_status(g.status, ST_TIMEOUT);
+                            *abort = 1;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem + (uint32_t)(acc * GN);
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            const uint32_t off = (uint32_t)(blk * 64 + ks * 32);
+                            umma_bf16(d, umma_desc(a0 + off), umma_desc(b0 + off), (uint32_t)ks);
+                        }
+                        umma_commit(&S.tfull[acc]);
+                    }
+                    umma_commit(&S.empty[slot]);   // the stage's operands may be overwritten
+                }
+            }
+            // the last commit to `empty` must land before the CTA exits
+            if (sc > 0 && !*abort) {
+                const long last = sc - 1;
+                if (!g_wait(&S.empty[last % G_STAGES], (uint32_t)((last / G_STAGES) & 1), abort)) {
+                    set_status(g.status, ST_TIMEOUT);
+                    *abort = 1;
+                }
+            }
+        }
+    } else if (warp < 2 + G_CONV_WARPS) {
+        // ------------------------------ converters ------------------------------
+        // packed weights [GN rows][GK/2 bytes] -> bf16 [GN][GK] in the swizzled layout
+        const int ct = threadIdx.x - 64;            // 0 .. 127
+        long sc = 0;
+        for (long u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+            for (int s = 0; s < nst; ++s, ++sc) {
+                const int slot = (int)(sc % G_STAGES);
+                const uint32_t par = (uint32_t)((sc / G_STAGES) & 1);
+                const bool ok = __all_sync(FULL, g_wait(&S.full[slot], par, abort));
+                if (!ok) {
+                    if (lane == 0) {
+                        if (!*abort) set_status(g.status, ST_TIMEOUT);
+                        *abort = 1;
+                    }
+                    break;
+                }
+                const unsigned char *raw = sRaw + slot * RAW_BYTES;
+                unsigned char *bt = sB + slot * B_BYTES;
+                // 256 (row, block) pieces of 16 bytes per stage, two per thread
+#pragma unroll
+                for (int pi = 0; pi < 2; ++pi) {
+                    const int piece = ct + 128 * pi;
+                    const int n = piece >> 1, blk = piece & 1;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(raw + n * (GK / 2) + blk * 16);
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int c = blk * 4 + q;   // 8-element chunk along K
+                        *reinterpret_cast<uint4 *>(bt + n * 128 + ((c ^ (n & 7)) << 4)) =
+                            nibbles_to_bf16_chunk(wv[q]);
+                    }
+                }
+                fence_proxy_async_shared();   // generic-proxy writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.conv[slot]);
+            }
+        }
+    } else {
+        // ------------------------------ drain / epilogue ------------------------------
+        // Every drain warp walks the same units and blocks (also after an
+        // abort, without touching data) so that the named barriers below
+        // always see all of them.
+        const int dw = warp - (2 + G_CONV_WARPS);    // 0 .. 7
+        const int quad = warp & 3;                   // TMEM lanes 32*quad ..
+        const int chalf = dw >> 2;                   // columns 64*chalf ..
+        const int row = 32 * quad + lane;            // position row of the tile
+        long bc = 0;
+        for (long u = blockIdx.x; u < n_units; u += gridDim.x) {
+            const int item = (int)(u / per_item), j = (int)(u - (long)item * per_item);
+            const int e = g.item_expert[item], pos0 = g.item_pos0[item], m = g.item_m[item];
+            const bool active = 32 * quad < m;       // warp-uniform: any valid row in this quad
+            const bool valid = row < m;
+            const int pos = pos0 + (valid ? row : 0);
+            const float *dsc;
+            if (GATEUP) {
+                int tok = valid ? g.pos_token[pos] : 0;
+                if (tok < 0 || tok >= g.T) tok = 0;   // flagged by the gather kernel
+                dsc = g.dx + (size_t)tok * (H / 32);
+            } else {
+                dsc = g.dh + (size_t)pos * (F / 32);
+            }
+            float2 acc[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.0f, 0.0f);
+            float dnext = valid ? __ldg(dsc) : 0.0f;
+            for (int b = 0; b < nb; ++b, ++bc) {
+                const float db = dnext;
+                if (b + 1 < nb) dnext = valid ? __ldg(dsc + b + 1) : 0.0f;
+                const int a = (int)(bc % G_NACC);
+                const uint32_t par = (uint32_t)((bc / G_NACC) & 1);
+                const bool ok = !*abort && __all_sync(FULL, g_wait(&S.tfull[a], par, abort));
+                if (ok) {
+                    tc_fence_after();
+                    if (active) {
+                        const uint32_t base =
+                            tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(a * GN + 64 * chalf);
+                        const float2 d2 = make_float2(db, db);
+                        float v[32];
+                        tmem_ld32(base, v);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) acc[c] = __ffma2_rn(d2, make_float2(v[2 * c], v[2 * c + 1]), acc[c]);
+                        tmem_ld32(base + 32, v);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            acc[16 + c] = __ffma2_rn(d2, make_float2(v[2 * c], v[2 * c + 1]), acc[16 + c]);
+                    }
+                    tc_fence_before();
+                } else if (lane == 0) {
+                    if (!*abort) set_status(g.status, ST_TIMEOUT);
+                    *abort = 1;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.tempty[a]);
+            }
+            const bool live = !*abort;
+            // ---- epilogue ----
+            const float *ers = (e == g.E) ? g.shared_rs : g.expert_rs + (size_t)e * (2 * F + H);
+            if (GATEUP) {
+                // columns 0..63: gate rows 64j.., columns 64..127: the matching up rows
+                if (chalf == 1 && live && active) {
+                    const float *su = ers + F + 64 * j;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        xch[row * XCH_LD + 2 * c] = __fmul_rn(su[2 * c], acc[c].x);
+                        xch[row * XCH_LD + 2 * c + 1] = __fmul_rn(su[2 * c + 1], acc[c].y);
+                    }
+                }
+                named_barrier(BAR_DRAIN, 32 * G_DRAIN_WARPS);
+                if (chalf == 0 && live && valid) {
+                    const float *sg = ers + 64 * j;
+#pragma unroll
+                    for (int grp = 0; grp < 2; ++grp) {
+                        float h[32];
+                        float amax = 0.0f;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int col = 32 * grp + c;
+                            const float gv = (c & 1) ? acc[col >> 1].y : acc[col >> 1].x;
+                            const float gg = __fmul_rn(sg[col], gv);
+                            const float uu = xch[row * XCH_LD + col];
+                            h[c] = __fmul_rn(__fmul_rn(gg, own_sigmoid(gg)), uu);
+                            amax = fmaxf(amax, fabsf(h[c]));
+                        }
+                        const float dq = __fdiv_rn(amax, 127.0f);
+                        const float id = (dq != 0.0f) ? __fdiv_rn(1.0f, dq) : 0.0f;
+                        uint32_t qw[8];
+#pragma unroll
+                        for (int w4 = 0; w4 < 8; ++w4) {
+                            uint32_t word = 0;
+#pragma unroll
+                            for (int bb = 0; bb < 4; ++bb) {
+                                int q = __float2int_rn(__fmul_rn(h[4 * w4 + bb], id));
+                                q = max(-127, min(127, q));
+                                word |= ((uint32_t)q & 0xFFu) << (8 * bb);
+                            }
+                            qw[w4] = word;
+                        }
+                        const int col0 = 64 * j + 32 * grp;
+                        uint4 *dst = reinterpret_cast<uint4 *>(g.qh + (size_t)pos * F + col0);
+                        dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                        dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+                        g.dh[(size_t)pos * (F / 32) + col0 / 32] = dq;
+                        uint4 *bdst = reinterpret_cast<uint4 *>(g.qhb + (size_t)pos * F + col0);
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) bdst[c8] = codes_to_bf16_chunk(make_uint2(qw[2 * c8], qw[2 * c8 + 1]));
+                        if (g.h_dbg) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) g.h_dbg[(size_t)pos * F + col0 + c] = h[c];
+                        }
+                    }
+                }
+                named_barrier(BAR_DRAIN, 32 * G_DRAIN_WARPS);   // xch is reused by the next unit
+            } else if (live && valid) {
+                const int col0 = GN * j + 64 * chalf;
+                float4 *yr = reinterpret_cast<float4 *>(g.y + (size_t)pos * H + col0);
+                const float *sd = ers + 2 * F + col0;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    float4 o;
+                    o.x = __fmul_rn(sd[4 * c], acc[2 * c].x);
+                    o.y = __fmul_rn(sd[4 * c + 1], acc[2 * c].y);
+                    o.z = __fmul_rn(sd[4 * c + 2], acc[2 * c + 1].x);
+                    o.w = __fmul_rn(sd[4 * c + 3], acc[2 * c + 1].y);
+                    yr[c] = o;
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G_TMEM_COLS));
+    }
+}
+
+int launch_gather_x(const int8_t *qx, const int32_t *pos_token, const int32_t *offsets, int E, int P, int R,
+                    int T, int H, uint16_t *xg, int *status, cudaStream_t st)
+{
+    const long n = (long)R * (H / 8);
+    if (n == 0) return 0;
+    k_gather_x<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(qx, pos_token, offsets, E, P, R, T, H, xg, status);
+    count_launch();
+    return 0;
+}
+
+int launch_gemm_items(const int32_t *counts, const int32_t *offsets, int E, int T, int P, int32_t *item_expert,
+                      int32_t *item_pos0, int32_t *item_m, int32_t *n_items, cudaStream_t st)
+{
+    k_gemm_items<<<1, 32, 0, st>>>(counts, offsets, E, T, P, item_expert, item_pos0, item_m, n_items);
+    count_launch();
+    return 0;
+}
+
+int launch_combine(const float *y, const int32_t *inv, const float *wts, int T, int k, int P, int H, float *out,
+                   cudaStream_t st)
+{
+    const long n = (long)T * (H / 4);
+    if (n == 0) return 0;
+    k_combine<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, inv, wts, T, k, P, H, out);
+    count_launch();
+    return 0;
+}
+
+int max_gemm_items(int T, int k, int E)
+{
+    const long P = (long)T * k;
+    return (int)(P / GM + (P < E ? P : E) + 1 + (T + GM - 1) / GM);
+}
+
+int gemm_tile_rows() { return GM; }
+
+template <bool GATEUP>
+static int launch_gemm_t(const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st)
+{
+    static int configured_device = -1;
+    const size_t smem = gemm_smem_bytes();
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(k_gemm<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return -1;
+        configured_device = dev;
+    }
+    k_gemm<GATEUP><<<num_sms, G_THREADS, smem, st>>>(maps, g);
+    count_launch();
+    return 0;
+}
+
+int launch_gemm(bool gateup, const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st)
+{
+    return gateup ? launch_gemm_t<true>(maps, g, num_sms, st) : launch_gemm_t<false>(maps, g, num_sms, st);
+}
+
+}  // namespace coli
