@@ -9,7 +9,13 @@ timed region, so the shared expert and router weights are re-read from HBM
 like in a real multi-layer decode.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|verify|prefill]
+                  [--path auto|gemv|gemm]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+The 2048-token prefill workload runs the grouped tensor-core GEMM (auto path);
+its roofline line is the gate/up GEMM's FLOP/s against the measured bf16 dense
+peak (int4 and int8 codes are exact in bf16), and "tops_layer" is the whole
+layer's integer multiply-add rate (2 ops per MAC).
 
 Prints one JSON line (rank 0).
 """
@@ -103,15 +109,19 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- #
-def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000):
+def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: int = 0):
     """Time the CPU oracle on a bounded sample of the workload (forwards of the
-    same shape); returns (tok/s, threads, sample description)."""
+    same shape, or the first `max_tokens` tokens of each when that is set: the
+    oracle's cost is per token and expert, so a token subset keeps its rate);
+    returns (tok/s, threads, sample description)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
     from helpers import OracleLayer
     oracle.build()
     ref = OracleLayer(wl)
     xs = [synth.activations(wl, seed_base + i) for i in range(n_forwards)]
+    if max_tokens > 0:
+        xs = [x[:max_tokens] for x in xs]
     # pack the experts the sample touches before timing (the oracle's converter)
     for x in xs:
         idx, _ = oracle.route(x, ref.W, ref.b, wl.top_k, wl.routed_scale)
@@ -122,7 +132,12 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000):
         ref.forward(x)
     dt = time.perf_counter() - t0
     toks = n_forwards * xs[0].shape[0]
-    return toks / dt, oracle.num_threads(), f"{n_forwards} forwards x {xs[0].shape[0]} tokens of the {wl.name} workload ({dt:.1f} s)"
+    sub = f" (first {xs[0].shape[0]} of {wl.n_tok} tokens)" if xs[0].shape[0] < wl.n_tok else ""
+    return toks / dt, oracle.num_threads(), (f"{n_forwards} forwards x {xs[0].shape[0]} tokens of the {wl.name} "
+                                             f"workload{sub} ({dt:.1f} s)")
+
+
+CPU_SAMPLE_TOKENS = {"prefill": 24}   # bounded oracle sample per forward (tokens)
 
 
 def run_reference(args):
@@ -132,9 +147,12 @@ def run_reference(args):
         return
     wl = synth.WORKLOADS[args.workload]
     n = max(1, args.steps if args.steps <= 50 else 20)
+    if wl.n_tok > 64:
+        n = min(n, 3)
+    mt = CPU_SAMPLE_TOKENS.get(wl.name, 0)
     for _ in range(min(args.warmup, 1)):
-        oracle_baseline(wl, 1, seed_base=800000)
-    tps, cores, sample = oracle_baseline(wl, n)
+        oracle_baseline(wl, 1, seed_base=800000, max_tokens=mt)
+    tps, cores, sample = oracle_baseline(wl, n, max_tokens=mt)
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tok/s", "n_gpus": args.gpus,
         "steps": n, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.n_tok / tps,
@@ -173,14 +191,19 @@ def run(args):
     wl = synth.WORKLOADS[args.workload]
     T = wl.n_tok
     coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
+    path = {"auto": coli.PATH_AUTO, "gemv": coli.PATH_GEMV, "gemm": coli.PATH_GEMM}[args.path]
+    coli.set_path(path)
+    use_gemm = path == coli.PATH_GEMM or (path == coli.PATH_AUTO and T >= coli.GEMM_MIN_TOKENS)
     t_build = time.perf_counter()
     L = build_device_layer(wl)
     W, b = synth.router(wl)
     L["router_b"] = torch.from_numpy(b).cuda()
     t_build = time.perf_counter() - t_build
     n_total = args.warmup + args.steps
+    # distinct inputs per step (cycled for large batches to bound host time and memory)
+    n_in = n_total if T <= 64 else min(n_total, 8)
     xs = torch.from_numpy(np.stack([synth.activations(wl, 10_000 + rank * 100_000 + i)
-                                    for i in range(n_total)])).cuda()
+                                    for i in range(n_in)])).cuda()
     out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     st = torch.cuda.current_stream()
@@ -188,12 +211,12 @@ def run(args):
     # union of routed experts per step (bookkeeping for weight bytes; not timed)
     unions = []
     for i in range(n_total):
-        idx, _ = coli.dbg_route(xs[i], L["router_w"], L["router_b"], wl.top_k)
+        idx, _ = coli.dbg_route(xs[i % n_in], L["router_w"], L["router_b"], wl.top_k)
         unions.append(len(set(idx.cpu().numpy().ravel().tolist())))
     torch.cuda.synchronize()
 
     def fwd(i):
-        coli.layer_forward(xs[i], L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+        coli.layer_forward(xs[i % n_in], L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
                            L["shared_w4"], L["shared_rs"], out=out)
 
     for i in range(args.warmup):
@@ -238,18 +261,19 @@ def run(args):
     status = coli.get_device_status()
 
     # end to end through the host-I/O entry point: pinned host x in, host out
-    xh = torch.from_numpy(np.stack([synth.activations(wl, 20_000 + i) for i in range(args.steps)]))
+    n_h = args.steps if T <= 64 else min(args.steps, 4)
+    xh = torch.from_numpy(np.stack([synth.activations(wl, 20_000 + i) for i in range(n_h)]))
     xh = xh.pin_memory()
     oh = torch.empty((T, wl.hidden), dtype=torch.float32).pin_memory()
     for i in range(min(args.warmup, 5)):
-        coli.layer_forward_hostio(xh[i], L["router_w"], L["router_b"], L["expert_w4"],
+        coli.layer_forward_hostio(xh[i % n_h], L["router_w"], L["router_b"], L["expert_w4"],
                                   L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
     e2e_s = 0.0
     for s in range(args.steps):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        coli.layer_forward_hostio(xh[s], L["router_w"], L["router_b"], L["expert_w4"],
+        coli.layer_forward_hostio(xh[s % n_h], L["router_w"], L["router_b"], L["expert_w4"],
                                   L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
         e2e_s += time.perf_counter() - t0
     if world > 1:
@@ -257,23 +281,38 @@ def run(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
 
-    hbm_peak, _, peak_kind = peaks()
+    hbm_peak, bf16_peak, peak_kind = peaks()
     ub = np.array(unions[args.warmup:], dtype=np.float64)
     bytes_per_fwd = float(np.mean((ub + 1) * expert_bytes(wl)))
     k_avg_ms = k_ms / max(k_n, 1)
-    achieved = bytes_per_fwd / (k_avg_ms * 1e-3) / 1e9
     value = world * args.steps * T / (total_ms * 1e-3)
+    # multiply-adds of one forward: (T*k routed + T shared) rows x (2F*H + H*F)
+    macs_gu = (T * wl.top_k + T) * 2 * wl.ffn * wl.hidden
+    macs_layer = (T * wl.top_k + T) * 3 * wl.ffn * wl.hidden
+    if use_gemm:
+        achieved = 2.0 * macs_gu / (k_avg_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": achieved / bf16_peak, "traffic": None,
+                    "kernel": "k_gemm<gate/up> (tcgen05 bf16 on exact int codes, SiLU*up + Q8_0 of h fused), "
+                              "timed alone",
+                    "algorithmic_flops_per_launch": 2.0 * macs_gu,
+                    "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} bf16_tflops (burst)"}
+    else:
+        achieved = bytes_per_fwd / (k_avg_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": None,
+                    "kernel": "k_experts (gate/up + SiLU*up requant + down + combine), timed alone",
+                    "algorithmic_bytes_per_launch": bytes_per_fwd,
+                    "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} hbm_gbs"}
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32", "data": "synthetic",
         "config": workload_config(wl),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
-                     "kernel": "k_experts (gate/up + SiLU*up requant + down + combine), timed alone",
-                     "algorithmic_bytes_per_launch": bytes_per_fwd,
-                     "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} hbm_gbs"},
+        "roofline": roofline,
+        "expert_path": "gemm" if use_gemm else "gemv",
         "weight_gbs_layer": bytes_per_fwd / (total_ms / args.steps * 1e-3) / 1e9,
+        "tops_layer": 2.0 * macs_layer / (total_ms / args.steps * 1e-3) / 1e12,
         "e2e": {"value": world * args.steps * T / e2e_s, "unit": "tok/s",
                 "h2d_bytes_per_step": T * wl.hidden * 4, "d2h_bytes_per_step": T * wl.hidden * 4},
         "gpu_launches": launches,
@@ -283,7 +322,9 @@ def run(args):
         "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tps, cores, sample = oracle_baseline(wl, args.cpu_forwards)
+        mt = CPU_SAMPLE_TOKENS.get(wl.name, 0)
+        nf = args.cpu_forwards if T <= 64 else 1
+        tps, cores, sample = oracle_baseline(wl, nf, max_tokens=mt)
         line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -295,13 +336,20 @@ def run(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="decode", choices=["decode", "verify", "prefill", "profile", "route_profile"])
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "verify", "prefill", "profile", "route_profile",
+                                                          "prefill_profile"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-forwards", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    big = synth.WORKLOADS[args.workload].n_tok > 64
+    if args.steps is None:
+        args.steps = 30 if big else 1000
+    if args.warmup is None:
+        args.warmup = 5 if big else 20
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libcoli_moe.so")
 
 OK, E_INVAL, E_NOSHAPE, E_NOMEM, E_CUDA, E_TIMEOUT, E_UNIMPL, E_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
 PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
+GEMM_MIN_TOKENS = 64   # COLI_GEMM_MIN_TOKENS: AUTO runs the grouped GEMM from this batch size
 
 EXPORTS = (
     "coli_moe_configure", "coli_moe_layer_forward", "coli_moe_layer_forward_hostio",

@@ -79,6 +79,8 @@ struct GemmArgs {
     float *h_dbg;                    // optional [P+T][F]
     float *y;                        // [P+T][H]
     int *status;
+    unsigned long long *trace;       // optional per-block stage log (null: off)
+    int trace_cap;                   // events per block (four roles, a quarter each)
 };
 
 // Small-batch routing in one launch: Q8_0 of x, router logits, top-k, dispatch,

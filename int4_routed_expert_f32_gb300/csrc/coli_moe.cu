@@ -603,6 +603,8 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
         ga.expert_rs = expert_rowscale; ga.shared_rs = shared_rowscale;
         ga.qh = w.qh; ga.dh = w.dh; ga.qhb = w.qhb; ga.h_dbg = nullptr; ga.y = w.y;
         ga.status = w.status;
+        ga.trace = g.trace;
+        ga.trace_cap = g.trace_cap;
         if (g.timing) {
             int r = timing_events(&e0, &e1);
             if (r != COLI_OK) return r;
@@ -610,6 +612,7 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
         }
         LAUNCH_OK(launch_gemm(true, g.gemm_gu, ga, g.num_sms, st));
         if (g.timing) CUDA_OK(cudaEventRecord(e1, st));
+        ga.trace = nullptr;   // the stage log covers the gate/up kernel
         LAUNCH_OK(launch_gemm(false, g.gemm_dn, ga, g.num_sms, st));
         LAUNCH_OK(launch_combine(w.y, w.inv, w.wts, T, k, P, H, out, st));
         return COLI_OK;

@@ -19,17 +19,20 @@
 // Tile.  M = 128 dispatch positions (rows of operand A: the gathered bf16
 // codes of one expert's tokens), N = 128 weight rows (gate/up: 64 gate rows
 // and the 64 matching up rows; down: 128 output rows), K = 64 per pipeline
-// stage (two blocks).  A drain thread owns one token row and 64 columns, so
-// the per-(token, block) scale is one scalar, and SiLU(gate)*up and the Q8_0
-// requantisation of h stay inside threads.
+// stage (two blocks).  A drain thread owns one token row and 32 columns, so
+// the per-(token, block) scale is one scalar, and a gate warp's 32 columns
+// are exactly one Q8_0 block of h: SiLU(gate)*up and the requantisation stay
+// inside threads (the up values come through shared memory).
 //
-// Warp roles (14 warps, one CTA per SM, persistent over units):
+// Warp roles (24 warps = 6 warpgroups, one CTA per SM, persistent over units):
 //   0      TMA producer (activation tile + packed weight rows)
 //   1      MMA issuer, owner of the TMEM allocation
 //   2..5   weight converters: packed int4 -> bf16 in the 128-byte-swizzled
 //          K-major layout the MMA reads
-//   6..13  drain + epilogue; warp w reads TMEM lanes 32*(w%4).. and the
-//          column half (w-6)/4
+//   6..7   idle (they complete the second warpgroup)
+//   8..23  drain + epilogue; warp w reads TMEM lanes 32*(w%4).. and columns
+//          32*((w-8)/4) ..  Sixteen warps keep four TMEM loads in flight per
+//          scheduler, which hides the load latency behind the FMAs.
 //
 // Element order inside each 8-element K chunk, for both operands:
 // (k0, k2, k4, k6, k1, k3, k5, k7).  It is what splitting the packed bytes
@@ -55,8 +58,14 @@ constexpr int B_BYTES = GN * GK * 2;    // 16 KB bf16, swizzled
 constexpr int RAW_BYTES = GN * GK / 2;  // 4 KB packed int4
 constexpr int XCH_LD = 65;              // padded row of the gate/up exchange tile
 constexpr int G_CONV_WARPS = 4;
-constexpr int G_DRAIN_WARPS = 8;
-constexpr int G_THREADS = 32 * (2 + G_CONV_WARPS + G_DRAIN_WARPS);
+constexpr int G_DRAIN_WARP0 = 8;        // warps 0..7: producer, MMA, converters, 2 idle
+constexpr int G_DRAIN_WARPS = 16;       // 4 TMEM lane quarters x 4 column quarters
+constexpr int G_THREADS = 32 * (G_DRAIN_WARP0 + G_DRAIN_WARPS);
+// Register split (setmaxnreg, per warpgroup): the first two warpgroups give
+// registers to the four drain warpgroups.  The launch allocation must cover
+// the sum; the launcher checks it against the compiled register count.
+constexpr int G_REGS_CTRL = 40;
+constexpr int G_REGS_DRAIN = 96;
 constexpr int G_TMEM_COLS = G_NACC * GN;
 constexpr int BAR_DRAIN = 3;
 constexpr uint64_t G_WAIT_NS = 2000000000ull;
@@ -81,6 +90,32 @@ __device__ __forceinline__ bool g_wait(uint64_t *bar, uint32_t parity, volatile 
         if (*abort) return false;
         if (g_timer() - t0 > G_WAIT_NS) return false;
     }
+}
+
+// Optional stage log.  Each block's region holds four sub-logs (producer,
+// MMA issuer, first converter warp, first drain warp); entry i >= 1 of a
+// sub-log is ((globaltimer << 8) | code, value) and entry 0 receives the
+// event count when the role finishes (the count lives in a register meanwhile,
+// so logging adds no memory round trip).  Only stages [tr0, tr0 + TRACE_NS)
+// of each block (and their blocks) are logged: a steady-state window after
+// the first unit.
+constexpr int TRACE_NS = 40;
+
+__device__ __forceinline__ void gtrace(const GemmArgs &g, int role, int &n, int code, int value)
+{
+    if (n + 1 >= g.trace_cap / 4) return;
+    unsigned long long *sub = g.trace + ((size_t)blockIdx.x * g.trace_cap + (size_t)role * (g.trace_cap / 4)) * 2;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    ++n;
+    sub[2 * n] = (t << 8) | (unsigned)code;
+    sub[2 * n + 1] = (unsigned long long)value;
+}
+
+__device__ __forceinline__ void gtrace_close(const GemmArgs &g, int role, int n)
+{
+    if (!g.trace) return;
+    g.trace[((size_t)blockIdx.x * g.trace_cap + (size_t)role * (g.trace_cap / 4)) * 2] = (unsigned long long)n;
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -284,7 +319,9 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
     const int nst = K / GK;                         // stages per unit
     const int nb = K / 32;                          // blocks per unit
     const int per_item = GATEUP ? F / 64 : H / GN;  // weight tiles per item
-    const long n_units = (long)(*g.n_items) * per_item;
+    const int n_units = *g.n_items * per_item;
+    const int tr0 = nst + 8;                       // first traced stage
+    const bool tr = g.trace != nullptr;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
@@ -294,7 +331,7 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
         }
         for (int b = 0; b < G_NACC; ++b) {
             mbar_init(&S.tfull[b], 1);
-            mbar_init(&S.tempty[b], G_DRAIN_WARPS);
+            mbar_init(&S.tempty[b], G_DRAIN_WARPS);   // one arrival per drain warp
         }
         S.abort = 0;
         fence_barrier_init();
@@ -314,25 +351,32 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
 
+    // Role dispatch.  Each warpgroup changes its register share inside its
+    // own branch, so that the compiler applies the drain's larger budget to
+    // the drain code only.
+    if (warp < G_DRAIN_WARP0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(G_REGS_CTRL));
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            long sc = 0;   // stages issued
-            for (long u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-                const int item = (int)(u / per_item), j = (int)(u - (long)item * per_item);
+            int ntr = 0;
+            int sc = 0;   // stages issued
+            for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+                const int item = u / per_item, j = u - item * per_item;
                 const int e = g.item_expert[item], pos0 = g.item_pos0[item];
                 const bool shared = (e == g.E);
                 const void *wmap = shared ? (const void *)&maps.sw : (const void *)&maps.w;
                 const int z = shared ? 0 : e;
                 for (int s = 0; s < nst; ++s, ++sc) {
-                    const int slot = (int)(sc % G_STAGES);
-                    const long rnd = sc / G_STAGES;
+                    const int slot = sc % G_STAGES;
+                    const int rnd = sc / G_STAGES;
                     if (rnd > 0 && !g_wait(&S.empty[slot], (uint32_t)((rnd - 1) & 1), abort)) {
                         if (!*abort) set_status(g.status, ST_TIMEOUT);
                         *abort = 1;
                         break;
                     }
+                    if (tr && sc >= tr0 && sc < tr0 + TRACE_NS) gtrace(g, 0, ntr, 11, sc);
                     mbar_arrive_expect_tx(&S.full[slot], A_BYTES + RAW_BYTES);
                     tma_load_2d(sA + slot * A_BYTES, &maps.act, s * GK, pos0, &S.full[slot]);
                     unsigned char *raw = sRaw + slot * RAW_BYTES;
@@ -344,45 +388,58 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                     }
                 }
             }
+            gtrace_close(g, 0, ntr);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
+        // One thread issues every MMA of the CTA.  Its loop is kept short (the
+        // issue rate of a single thread bounds the tensor pipe at this tile
+        // size): per stage one wait for the converted operands (which implies
+        // the TMA data), one wait per accumulator of the stage's pair, one
+        // fence, four MMAs and three commits.
         if (lane == 0) {
-            long sc = 0, bc = 0;   // stages consumed, blocks accumulated
-            for (long u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-                for (int s = 0; s < nst && !*abort; ++s, ++sc) {
-                    const int slot = (int)(sc % G_STAGES);
-                    const uint32_t par = (uint32_t)((sc / G_STAGES) & 1);
-                    if (!g_wait(&S.full[slot], par, abort) || !g_wait(&S.conv[slot], par, abort)) {
-                        if (!*abort) set_status(g.status, ST_TIMEOUT);
-                        *abort = 1;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + slot * A_BYTES), b0 = smem_u32(sB + slot * B_BYTES);
-                    for (int blk = 0; blk < 2; ++blk, ++bc) {
-                        const int acc = (int)(bc % G_NACC);
-                        const long use = bc / G_NACC;
-                        if (use > 0 && !g_wait(&S.tempty[acc], (uint32_t)((use - 1) & 1), abort)) {
-                            if (!*abort) set_status(g.status, ST_TIMEOUT);
-                            *abort = 1;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem + (uint32_t)(acc * GN);
-#pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const uint32_t off = (uint32_t)(blk * 64 + ks * 32);
-                            umma_bf16(d, umma_desc(a0 + off), umma_desc(b0 + off), (uint32_t)ks);
-                        }
-                        umma_commit(&S.tfull[acc]);
-                    }
-                    umma_commit(&S.empty[slot]);   // the stage's operands may be overwritten
+            const int my_units =
+                (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+            const int total = my_units * nst;
+            const uint64_t dA = umma_desc(smem_u32(sA)), dB = umma_desc(smem_u32(sB));
+            int slot = 0;
+            uint32_t phase = 0;
+            bool failed = false;
+            for (int sc = 0; sc < total; ++sc) {
+                const int pr = sc & 1;          // accumulator pair {2pr, 2pr+1} (blocks 2sc, 2sc+1)
+                const int puse = sc >> 1;       // earlier uses of the pair
+                bool ok = g_wait(&S.conv[slot], phase, abort);
+                if (ok && puse > 0) {
+                    const uint32_t tp = (uint32_t)((puse - 1) & 1);
+                    ok = g_wait(&S.tempty[2 * pr], tp, abort) && g_wait(&S.tempty[2 * pr + 1], tp, abort);
+                }
+                if (!ok) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                // descriptor start addresses advance in 16-byte units: +2 per 32 bytes of K
+                const uint64_t da = dA + (uint64_t)(slot * (A_BYTES >> 4));
+                const uint64_t db = dB + (uint64_t)(slot * (B_BYTES >> 4));
+                const uint32_t d0 = tmem + (uint32_t)(2 * pr * GN);
+                umma_bf16(d0, da, db, 0u);
+                umma_bf16(d0, da + 2, db + 2, 1u);
+                umma_commit(&S.tfull[2 * pr]);
+                umma_bf16(d0 + GN, da + 4, db + 4, 0u);
+                umma_bf16(d0 + GN, da + 6, db + 6, 1u);
+                umma_commit(&S.tfull[2 * pr + 1]);
+                umma_commit(&S.empty[slot]);    // the stage's operands may be overwritten
+                if (++slot == G_STAGES) {
+                    slot = 0;
+                    phase ^= 1;
                 }
             }
-            // the last commit to `empty` must land before the CTA exits
-            if (sc > 0 && !*abort) {
-                const long last = sc - 1;
+            if (failed) {
+                if (!*abort) set_status(g.status, ST_TIMEOUT);
+                *abort = 1;
+            } else if (total > 0) {
+                // the last commit to `empty` must land before the CTA exits
+                const int last = total - 1;
                 if (!g_wait(&S.empty[last % G_STAGES], (uint32_t)((last / G_STAGES) & 1), abort)) {
                     set_status(g.status, ST_TIMEOUT);
                     *abort = 1;
@@ -393,10 +450,11 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
         // ------------------------------ converters ------------------------------
         // packed weights [GN rows][GK/2 bytes] -> bf16 [GN][GK] in the swizzled layout
         const int ct = threadIdx.x - 64;            // 0 .. 127
-        long sc = 0;
-        for (long u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+        int sc = 0;
+        int ntr = 0;
+        for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
             for (int s = 0; s < nst; ++s, ++sc) {
-                const int slot = (int)(sc % G_STAGES);
+                const int slot = sc % G_STAGES;
                 const uint32_t par = (uint32_t)((sc / G_STAGES) & 1);
                 const bool ok = __all_sync(FULL, g_wait(&S.full[slot], par, abort));
                 if (!ok) {
@@ -406,10 +464,12 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                     }
                     break;
                 }
+                const bool trc = tr && warp == 2 && lane == 0 && sc >= tr0 && sc < tr0 + TRACE_NS;
+                if (trc) gtrace(g, 2, ntr, 14, sc);
                 const unsigned char *raw = sRaw + slot * RAW_BYTES;
                 unsigned char *bt = sB + slot * B_BYTES;
                 // 256 (row, block) pieces of 16 bytes per stage, two per thread
-#pragma unroll
+#pragma unroll 1
                 for (int pi = 0; pi < 2; ++pi) {
                     const int piece = ct + 128 * pi;
                     const int n = piece >> 1, blk = piece & 1;
@@ -425,20 +485,25 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                 fence_proxy_async_shared();   // generic-proxy writes -> visible to the tensor core
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.conv[slot]);
+                if (trc) gtrace(g, 2, ntr, 15, sc);
             }
         }
+        if (warp == 2 && lane == 0) gtrace_close(g, 2, ntr);
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(G_REGS_DRAIN));
         // ------------------------------ drain / epilogue ------------------------------
         // Every drain warp walks the same units and blocks (also after an
         // abort, without touching data) so that the named barriers below
         // always see all of them.
-        const int dw = warp - (2 + G_CONV_WARPS);    // 0 .. 7
+        const int dw = warp - G_DRAIN_WARP0;         // 0 .. 15
         const int quad = warp & 3;                   // TMEM lanes 32*quad ..
-        const int chalf = dw >> 2;                   // columns 64*chalf ..
+        const int cq = dw >> 2;                      // columns 32*cq ..
         const int row = 32 * quad + lane;            // position row of the tile
-        long bc = 0;
-        for (long u = blockIdx.x; u < n_units; u += gridDim.x) {
-            const int item = (int)(u / per_item), j = (int)(u - (long)item * per_item);
+        int bc = 0;
+        int ntr = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            const int item = u / per_item, j = u - item * per_item;
             const int e = g.item_expert[item], pos0 = g.item_pos0[item], m = g.item_m[item];
             const bool active = 32 * quad < m;       // warp-uniform: any valid row in this quad
             const bool valid = row < m;
@@ -451,103 +516,113 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
             } else {
                 dsc = g.dh + (size_t)pos * (F / 32);
             }
-            float2 acc[32];
+            float2 acc[16];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.0f, 0.0f);
-            float dnext = valid ? __ldg(dsc) : 0.0f;
-            for (int b = 0; b < nb; ++b, ++bc) {
-                const float db = dnext;
-                if (b + 1 < nb) dnext = valid ? __ldg(dsc + b + 1) : 0.0f;
-                const int a = (int)(bc % G_NACC);
-                const uint32_t par = (uint32_t)((bc / G_NACC) & 1);
-                const bool ok = !*abort && __all_sync(FULL, g_wait(&S.tfull[a], par, abort));
-                if (ok) {
-                    tc_fence_after();
-                    if (active) {
-                        const uint32_t base =
-                            tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(a * GN + 64 * chalf);
-                        const float2 d2 = make_float2(db, db);
-                        float v[32];
-                        tmem_ld32(base, v);
+            for (int c = 0; c < 16; ++c) acc[c] = make_float2(0.0f, 0.0f);
+            // block scales in groups of 4 (nb % 4 == 0), loaded two groups
+            // ahead so that the L2 round trip hides behind 4-8 blocks of work
+            const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            const float4 *dsc4 = reinterpret_cast<const float4 *>(dsc);
+            float4 d0 = valid ? __ldg(dsc4) : zero4;
+            float4 d1 = (valid && nb > 4) ? __ldg(dsc4 + 1) : zero4;
+            for (int b4 = 0; b4 < nb; b4 += 4) {
+                const float4 dcur = d0;
+                d0 = d1;
+                if (valid && b4 + 8 < nb) d1 = __ldg(dsc4 + (b4 >> 2) + 2);
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) acc[c] = __ffma2_rn(d2, make_float2(v[2 * c], v[2 * c + 1]), acc[c]);
-                        tmem_ld32(base + 32, v);
+                for (int bi = 0; bi < 4; ++bi, ++bc) {
+                    const float db = bi == 0 ? dcur.x : bi == 1 ? dcur.y : bi == 2 ? dcur.z : dcur.w;
+                    const int a = bc % G_NACC;
+                    const uint32_t par = (uint32_t)((bc / G_NACC) & 1);
+                    const bool ok = !*abort && __all_sync(FULL, g_wait(&S.tfull[a], par, abort));
+                    const bool trd = tr && dw == 0 && lane == 0 && bc >= 2 * tr0 && bc < 2 * (tr0 + TRACE_NS);
+                    if (trd) gtrace(g, 3, ntr, 16, bc);
+                    if (ok) {
+                        tc_fence_after();
+                        if (active) {
+                            const uint32_t base =
+                                tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(a * GN + 32 * cq);
+                            const float2 dd = make_float2(db, db);
+                            float v[32];
+                            tmem_ld32(base, v);
 #pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            acc[16 + c] = __ffma2_rn(d2, make_float2(v[2 * c], v[2 * c + 1]), acc[16 + c]);
+                            for (int c = 0; c < 16; ++c)
+                                acc[c] = __ffma2_rn(dd, make_float2(v[2 * c], v[2 * c + 1]), acc[c]);
+                        }
+                        tc_fence_before();
+                    } else if (lane == 0) {
+                        if (!*abort) set_status(g.status, ST_TIMEOUT);
+                        *abort = 1;
                     }
-                    tc_fence_before();
-                } else if (lane == 0) {
-                    if (!*abort) set_status(g.status, ST_TIMEOUT);
-                    *abort = 1;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.tempty[a]);
+                    if (trd) gtrace(g, 3, ntr, 17, bc);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.tempty[a]);
             }
             const bool live = !*abort;
             // ---- epilogue ----
             const float *ers = (e == g.E) ? g.shared_rs : g.expert_rs + (size_t)e * (2 * F + H);
             if (GATEUP) {
                 // columns 0..63: gate rows 64j.., columns 64..127: the matching up rows
-                if (chalf == 1 && live && active) {
-                    const float *su = ers + F + 64 * j;
+                if (cq >= 2 && live && active) {
+                    const int c0 = 32 * (cq - 2);
+                    const float *su = ers + F + 64 * j + c0;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        xch[row * XCH_LD + 2 * c] = __fmul_rn(su[2 * c], acc[c].x);
-                        xch[row * XCH_LD + 2 * c + 1] = __fmul_rn(su[2 * c + 1], acc[c].y);
+                    for (int c = 0; c < 16; ++c) {
+                        xch[row * XCH_LD + c0 + 2 * c] = __fmul_rn(su[2 * c], acc[c].x);
+                        xch[row * XCH_LD + c0 + 2 * c + 1] = __fmul_rn(su[2 * c + 1], acc[c].y);
                     }
                 }
                 named_barrier(BAR_DRAIN, 32 * G_DRAIN_WARPS);
-                if (chalf == 0 && live && valid) {
-                    const float *sg = ers + 64 * j;
+                if (cq < 2 && live && valid) {
+                    // h for rows 64j + 32cq .. +31 of this token: one Q8_0 block
+                    const int c0 = 32 * cq;
+                    const float *sg = ers + 64 * j + c0;
+                    float h[32];
+                    float amax = 0.0f;
 #pragma unroll
-                    for (int grp = 0; grp < 2; ++grp) {
-                        float h[32];
-                        float amax = 0.0f;
+                    for (int c = 0; c < 32; ++c) {
+                        const float gv = (c & 1) ? acc[c >> 1].y : acc[c >> 1].x;
+                        const float gg = __fmul_rn(sg[c], gv);
+                        const float uu = xch[row * XCH_LD + c0 + c];
+                        h[c] = __fmul_rn(__fmul_rn(gg, own_sigmoid(gg)), uu);
+                        amax = fmaxf(amax, fabsf(h[c]));
+                    }
+                    const float dq = __fdiv_rn(amax, 127.0f);
+                    const float id = (dq != 0.0f) ? __fdiv_rn(1.0f, dq) : 0.0f;
+                    uint32_t qw[8];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int col = 32 * grp + c;
-                            const float gv = (c & 1) ? acc[col >> 1].y : acc[col >> 1].x;
-                            const float gg = __fmul_rn(sg[col], gv);
-                            const float uu = xch[row * XCH_LD + col];
-                            h[c] = __fmul_rn(__fmul_rn(gg, own_sigmoid(gg)), uu);
-                            amax = fmaxf(amax, fabsf(h[c]));
+                    for (int w4 = 0; w4 < 8; ++w4) {
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb) {
+                            int q = __float2int_rn(__fmul_rn(h[4 * w4 + bb], id));
+                            q = max(-127, min(127, q));
+                            word |= ((uint32_t)q & 0xFFu) << (8 * bb);
                         }
-                        const float dq = __fdiv_rn(amax, 127.0f);
-                        const float id = (dq != 0.0f) ? __fdiv_rn(1.0f, dq) : 0.0f;
-                        uint32_t qw[8];
+                        qw[w4] = word;
+                    }
+                    const int col0 = 64 * j + c0;
+                    uint4 *dst = reinterpret_cast<uint4 *>(g.qh + (size_t)pos * F + col0);
+                    dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+                    g.dh[(size_t)pos * (F / 32) + col0 / 32] = dq;
+                    uint4 *bdst = reinterpret_cast<uint4 *>(g.qhb + (size_t)pos * F + col0);
 #pragma unroll
-                        for (int w4 = 0; w4 < 8; ++w4) {
-                            uint32_t word = 0;
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        bdst[c8] = codes_to_bf16_chunk(make_uint2(qw[2 * c8], qw[2 * c8 + 1]));
+                    if (g.h_dbg) {
 #pragma unroll
-                            for (int bb = 0; bb < 4; ++bb) {
-                                int q = __float2int_rn(__fmul_rn(h[4 * w4 + bb], id));
-                                q = max(-127, min(127, q));
-                                word |= ((uint32_t)q & 0xFFu) << (8 * bb);
-                            }
-                            qw[w4] = word;
-                        }
-                        const int col0 = 64 * j + 32 * grp;
-                        uint4 *dst = reinterpret_cast<uint4 *>(g.qh + (size_t)pos * F + col0);
-                        dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-                        dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-                        g.dh[(size_t)pos * (F / 32) + col0 / 32] = dq;
-                        uint4 *bdst = reinterpret_cast<uint4 *>(g.qhb + (size_t)pos * F + col0);
-#pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) bdst[c8] = codes_to_bf16_chunk(make_uint2(qw[2 * c8], qw[2 * c8 + 1]));
-                        if (g.h_dbg) {
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) g.h_dbg[(size_t)pos * F + col0 + c] = h[c];
-                        }
+                        for (int c = 0; c < 32; ++c) g.h_dbg[(size_t)pos * F + col0 + c] = h[c];
                     }
                 }
                 named_barrier(BAR_DRAIN, 32 * G_DRAIN_WARPS);   // xch is reused by the next unit
             } else if (live && valid) {
-                const int col0 = GN * j + 64 * chalf;
+                const int col0 = GN * j + 32 * cq;
                 float4 *yr = reinterpret_cast<float4 *>(g.y + (size_t)pos * H + col0);
                 const float *sd = ers + 2 * F + col0;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     float4 o;
                     o.x = __fmul_rn(sd[4 * c], acc[2 * c].x);
                     o.y = __fmul_rn(sd[4 * c + 1], acc[2 * c].y);
@@ -557,6 +632,7 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                 }
             }
         }
+        if (dw == 0 && lane == 0) gtrace_close(g, 3, ntr);
     }
 
     __syncwarp();
@@ -612,6 +688,13 @@ static int launch_gemm_t(const GemmMaps &maps, const GemmArgs &g, int num_sms, c
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (configured_device != dev) {
+        // setmaxnreg.inc waits until enough registers are free: the warpgroups'
+        // shares after the split must fit in what the CTA is launched with
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, k_gemm<GATEUP>) != cudaSuccess) return -1;
+        const long have = (long)fa.numRegs * G_THREADS;
+        const long need = 32L * G_DRAIN_WARP0 * G_REGS_CTRL + 32L * G_DRAIN_WARPS * G_REGS_DRAIN;
+        if (fa.numRegs < G_REGS_CTRL || fa.numRegs > G_REGS_DRAIN || need > have) return -1;
         if (cudaFuncSetAttribute(k_gemm<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return -1;

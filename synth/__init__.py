@@ -101,6 +101,11 @@ WORKLOADS = {
     # with a small expert FFN (~0.6 GB resident): a small case for capturing the
     # routing kernel
     "route_profile": Workload("route_profile", 6144, 256, 256, 8, 1, 1),
+    # the prefill shape on 16 routed experts and 256 tokens (~0.3 GB of
+    # weights, 128 tokens per expert on average): a small case for capturing
+    # the grouped-GEMM kernels
+    "prefill_profile": Workload("prefill_profile", 6144, 2048, 16, 8, 256, 3, norm_jitter=True,
+                                weight_seed=1),
     "sweep": Workload("sweep", 6144, 2048, 256, 8, 128, 100, zipf_beta=ZIPF_BETA, layers=8,
                       layer_corr=SWEEP_LAYER_CORR, batches=(1, 8, 32, 128)),
 }
