@@ -40,6 +40,37 @@ METRIC = "MoE layer tok/s"
 EXPERT_BYTES_PER = None  # filled per workload: int4 bytes + row scales of one expert
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernels, from the ncu captures summarised under profiles/.  A value
+# applies only while the kernel's sources hash to the same SHA-256 as when it
+# was captured, and only to the workloads whose launches move the same bytes
+# as the captured one; otherwise the roofline's traffic is null.
+CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
+TRAFFIC = {
+    "k_experts": {
+        "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
+        "sha256": "00524302bf4d8fac4b59627bc702b81fc48b5d9998f92bbe5a283405d3b7516a",
+        "bytes_per_launch": 173843200,   # 170.32 MB read + 3.52 MB written
+        # a launch of the 16-expert profile workload streams 8 routed + 1 shared
+        # expert, the same units as one decode forward over 256 experts
+        "workloads": ("decode", "profile"),
+        "capture": "profiles/k_experts_decode_profile.md",
+    },
+}
+
+
+def kernel_traffic(kernel: str, workload: str):
+    t = TRAFFIC.get(kernel)
+    if t is None or workload not in t["workloads"]:
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    for f in t["sources"]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return t["bytes_per_launch"] if h.hexdigest() == t["sha256"] else None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -118,10 +149,29 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: in
     import oracle
     from helpers import OracleLayer
     oracle.build()
-    ref = OracleLayer(wl)
     xs = [synth.activations(wl, seed_base + i) for i in range(n_forwards)]
     if max_tokens > 0:
         xs = [x[:max_tokens] for x in xs]
+    if wl.layers > 1:
+        # the stacked layers: x <- x + layer_l(x); experts are packed lazily
+        # inside the timed loop's first pass, so time a second pass
+        refs = [OracleLayer(wl, layer=l) for l in range(wl.layers)]
+
+        def stack(x):
+            for r in refs:
+                x = (x + r.forward(x)).astype(np.float32)
+            return x
+
+        for x in xs:
+            stack(x)
+        t0 = time.perf_counter()
+        for x in xs:
+            stack(x)
+        dt = time.perf_counter() - t0
+        toks = n_forwards * xs[0].shape[0]
+        return toks / dt, oracle.num_threads(), (f"{n_forwards} passes x {xs[0].shape[0]} token(s) through the "
+                                                 f"{wl.layers}-layer {wl.name} stack ({dt:.1f} s)")
+    ref = OracleLayer(wl)
     # pack the experts the sample touches before timing (the oracle's converter)
     for x in xs:
         idx, _ = oracle.route(x, ref.W, ref.b, wl.top_k, wl.routed_scale)
@@ -137,7 +187,7 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: in
                                              f"workload{sub} ({dt:.1f} s)")
 
 
-CPU_SAMPLE_TOKENS = {"prefill": 24}   # bounded oracle sample per forward (tokens)
+CPU_SAMPLE_TOKENS = {"prefill": 24, "sweep": 1}   # bounded oracle sample per forward (tokens)
 
 
 def run_reference(args):
@@ -155,7 +205,8 @@ def run_reference(args):
     tps, cores, sample = oracle_baseline(wl, n, max_tokens=mt)
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tok/s", "n_gpus": args.gpus,
-        "steps": n, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.n_tok / tps,
+        "steps": n, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * (wl.batches[0] if wl.layers > 1 else wl.n_tok) / tps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32",
         "data": "synthetic", "config": workload_config(wl),
         "cpu_baseline": {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
@@ -166,6 +217,15 @@ def run_reference(args):
 
 
 def workload_config(wl):
+    if wl.layers > 1:
+        return {"workload": f"{wl.name}: {wl.layers} stacked GLM-5.2-shaped MoE layers (hidden {wl.hidden}, "
+                            f"expert FFN {wl.ffn}, {wl.n_experts} experts top-{wl.top_k} + 1 shared), residual "
+                            f"add between layers, batches {list(wl.batches)}; value = tokens/s through the "
+                            f"stack at batch {wl.batches[0]}",
+                "layers": wl.layers, "batches": list(wl.batches), "hidden": wl.hidden, "ffn": wl.ffn,
+                "n_experts": wl.n_experts, "top_k": wl.top_k,
+                "weights": f"int4 + F32 row scales, {wl.layers} x {wl.n_experts + 1} experts resident in HBM",
+                "l2": "flushed between timed steps (512 MiB write, outside the timed region)"}
     return {"workload": f"{wl.name}: GLM-5.2-shaped MoE layer, hidden {wl.hidden}, expert FFN {wl.ffn}, "
                         f"{wl.n_experts} routed experts top-{wl.top_k} + 1 shared, {wl.n_tok} token(s) per forward",
             "hidden": wl.hidden, "ffn": wl.ffn, "n_experts": wl.n_experts, "top_k": wl.top_k,
@@ -299,8 +359,9 @@ def run(args):
                     "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} bf16_tflops (burst)"}
     else:
         achieved = bytes_per_fwd / (k_avg_ms * 1e-3) / 1e9
+        traffic = kernel_traffic("k_experts", wl.name)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None,
+                    "frac": achieved / hbm_peak, "traffic": traffic, "traffic_unit": "bytes per launch",
                     "kernel": "k_experts (gate/up + SiLU*up requant + down + combine), timed alone",
                     "algorithmic_bytes_per_launch": bytes_per_fwd,
                     "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} hbm_gbs"}
@@ -333,6 +394,132 @@ def run(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Multi-layer decode sweep: the stacked layers (residual add fused into
+    each layer's combine) at each batch size; one step = one pass through all
+    layers.  `value` is tokens/s through the stack at batch 1; the per-batch
+    figures are in "sweep"."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__._builder().build()
+    import int4_routed_expert_f32_gb300 as coli
+    from synth.device import build_device_layer
+
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    torch.cuda.set_device(local)
+    wl = synth.WORKLOADS["sweep"]
+    t_build = time.perf_counter()
+    layers = [build_device_layer(wl, layer=l) for l in range(wl.layers)]
+    t_build = time.perf_counter() - t_build
+    coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, max(wl.batches))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    hbm_peak, _, peak_kind = peaks()
+    per_b = []
+    launches_total = 0
+    with ClockSampler(local) as clocks:
+        for B in wl.batches:
+            n_in = 4
+            xs = [torch.from_numpy(synth.activations(wl, 30_000 + rank * 100 + i, n_tok=B)).cuda()
+                  for i in range(n_in)]
+            bufs = [torch.empty((B, wl.hidden), dtype=torch.float32, device="cuda") for _ in range(2)]
+
+            def stack(x0, record_unions=None):
+                x = x0
+                for l, L in enumerate(layers):
+                    if record_unions is not None:
+                        idx, _ = coli.dbg_route(x, L["router_w"], L["router_b"], wl.top_k)
+                        record_unions.append(len(set(idx.cpu().numpy().ravel().tolist())))
+                    out = bufs[l & 1]
+                    coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"],
+                                                L["expert_rs"], L["shared_w4"], L["shared_rs"], out=out)
+                    x = out
+                return x
+
+            unions = {}
+            for i in range(n_in):
+                u = []
+                stack(xs[i], u)
+                unions[i] = u
+            for i in range(args.warmup):
+                flush.zero_()
+                stack(xs[i % n_in])
+            torch.cuda.synchronize()
+            coli.launch_count()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for k in range(args.steps):
+                flush.zero_()
+                ev[k][0].record(st)
+                stack(xs[k % n_in])
+                ev[k][1].record(st)
+            torch.cuda.synchronize()
+            launches_total += coli.launch_count()
+            ms = [a.elapsed_time(b) for a, b in ev]
+            t = float(np.mean(ms))
+            ub = [unions[k % n_in] for k in range(args.steps)]
+            bytes_step = float(np.mean([sum(u_ + 1 for u_ in uu) for uu in ub])) * expert_bytes(wl)
+            gbs = bytes_step / (t * 1e-3) / 1e9
+            per_b.append({"batch": B, "ms_per_step": t, "tok_s": B / (t * 1e-3), "weight_gbs": gbs,
+                          "weight_frac_of_hbm": gbs / hbm_peak,
+                          "union_mean": float(np.mean([np.mean(uu) for uu in ub])),
+                          "step_ms_p10_p50_p90": [float(np.percentile(ms, q)) for q in (10, 50, 90)]})
+    status = coli.get_device_status()
+    # end to end at batch 1: pinned host x in, the stack, host out
+    B = wl.batches[0]
+    xh = torch.from_numpy(synth.activations(wl, 40_000, n_tok=B)).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    x_dev = torch.empty((B, wl.hidden), dtype=torch.float32, device="cuda")
+    bufs = [torch.empty((B, wl.hidden), dtype=torch.float32, device="cuda") for _ in range(2)]
+
+    def e2e_once():
+        x_dev.copy_(xh, non_blocking=True)
+        x = x_dev
+        for l, L in enumerate(layers):
+            out = bufs[l & 1]
+            coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                                        L["shared_w4"], L["shared_rs"], out=out)
+            x = out
+        oh.copy_(x, non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(3):
+        e2e_once()
+    e2e_s = 0.0
+    n_e2e = min(args.steps, 50)
+    for _ in range(n_e2e):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_once()
+        e2e_s += time.perf_counter() - t0
+    b1 = per_b[0]
+    line = {
+        "metric": METRIC, "value": world * b1["tok_s"], "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": b1["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32",
+        "data": "synthetic",
+        "config": workload_config(wl),
+        "sweep": per_b,
+        "e2e": {"value": n_e2e * B / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": B * wl.hidden * 4,
+                "d2h_bytes_per_step": B * wl.hidden * 4},
+        "gpu_launches": launches_total,
+        "clocks": clocks.summary(),
+        "device_status": status,
+        "setup_s": round(t_build, 1),
+        "peak_kind": f"{peak_kind} hbm_gbs",
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, cores, sample = oracle_baseline(wl, 2, max_tokens=CPU_SAMPLE_TOKENS["sweep"])
+        line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -340,7 +527,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"])
     ap.add_argument("--workload", default="decode", choices=["decode", "verify", "prefill", "profile", "route_profile",
-                                                          "prefill_profile"])
+                                                          "prefill_profile", "sweep"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-forwards", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -348,12 +535,16 @@ def main():
     big = synth.WORKLOADS[args.workload].n_tok > 64
     if args.steps is None:
         args.steps = 30 if big else 1000
+        if args.workload == "sweep":
+            args.steps = 100
     if args.warmup is None:
         args.warmup = 5 if big else 20
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "sweep":
+        run_sweep(args)
     else:
         run(args)
 

@@ -99,6 +99,22 @@ int coli_moe_layer_forward(const float *x, int n_tok,
                            const uint8_t *shared_w4, const float *shared_rowscale,
                            float *out, void *stream);
 
+/* The forward of one layer of a stacked decoder (the multi-layer sweep of
+ * the benchmark configurations): out = x + MoE(RMSNorm(x)).  RMSNorm has no
+ * learned gain: xn = x / sqrt(mean(x^2) + 1e-6) per token, the sum of squares
+ * in the router's fixed F32 order (coli_moe_dbg_rmsnorm runs it alone); the
+ * residual add is fused into the combine (one F32 add after the weighted
+ * sum).  The pre-norm is this library's reading: the pages chain the sweep's
+ * layers with a residual add only, and without a norm the SwiGLU output grows
+ * as the square of its input, so the stream overflows within a few layers.
+ * Same arguments, rules and errors as coli_moe_layer_forward; `out` may not
+ * alias `x`. */
+int coli_moe_layer_forward_residual(const float *x, int n_tok,
+                                    const float *router_w, const float *router_bias,
+                                    const uint8_t *expert_w4, const float *expert_rowscale,
+                                    const uint8_t *shared_w4, const float *shared_rowscale,
+                                    float *out, void *stream);
+
 /* The same forward with x and out in HOST memory (pinned memory gives
  * asynchronous copies).  Copies x into a library-owned device buffer, runs the
  * forward, copies the result back, and synchronises `stream` before
@@ -197,6 +213,10 @@ int coli_moe_dbg_quantize(const float *x, int n, int8_t *q, float *d, void *stre
 int coli_moe_dbg_route(const float *x, int n_tok, const float *router_w,
                        const float *router_bias, int32_t *idx, float *w, float *logits,
                        void *stream);
+
+/* Stage entry point: the stacked layer's pre-norm alone.  x and xn [n_tok][hidden]
+ * F32 device pointers (16-byte aligned, hidden % 4 == 0); needs no configure. */
+int coli_moe_dbg_rmsnorm(const float *x, int n_tok, int hidden, float *xn, void *stream);
 
 /* Dispatch only: from idx [n_tok][k] (values < E) produce counts [E],
  * offsets [E+1], perm [n_tok*k] (perm[pos] = pair t*k+r), inv [n_tok*k]. */

@@ -24,12 +24,14 @@ PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
 GEMM_MIN_TOKENS = 64   # COLI_GEMM_MIN_TOKENS: AUTO runs the grouped GEMM from this batch size
 
 EXPORTS = (
-    "coli_moe_configure", "coli_moe_layer_forward", "coli_moe_layer_forward_hostio",
+    "coli_moe_configure", "coli_moe_layer_forward", "coli_moe_layer_forward_residual",
+    "coli_moe_layer_forward_hostio",
     "coli_moe_set_path", "coli_moe_get_device_status", "coli_moe_strerror", "coli_moe_release",
     "coli_moe_pack_int4", "coli_moe_timing_enable", "coli_moe_timing_read",
     "coli_moe_launch_count", "coli_moe_trace_enable", "coli_moe_trace_read",
     "coli_moe_dbg_quantize", "coli_moe_dbg_route",
-    "coli_moe_dbg_dispatch", "coli_moe_dbg_block_dots", "coli_moe_dbg_forward_intermediates",
+    "coli_moe_dbg_dispatch", "coli_moe_dbg_rmsnorm", "coli_moe_dbg_block_dots",
+    "coli_moe_dbg_forward_intermediates",
     "coli_moe_dbg_expert_hidden", "coli_moe_route_noalloc",
 )
 
@@ -56,6 +58,7 @@ def _load():
     sig = {
         "coli_moe_configure": ([ctypes.POINTER(_Shape)], i),
         "coli_moe_layer_forward": ([P, i, P, P, P, P, P, P, P, P], i),
+        "coli_moe_layer_forward_residual": ([P, i, P, P, P, P, P, P, P, P], i),
         "coli_moe_layer_forward_hostio": ([P, i, P, P, P, P, P, P, P, P], i),
         "coli_moe_set_path": ([i, i], i),
         "coli_moe_get_device_status": ([P], i),
@@ -71,6 +74,7 @@ def _load():
         "coli_moe_dbg_quantize": ([P, i, P, P, P], i),
         "coli_moe_dbg_route": ([P, i, P, P, P, P, P, P], i),
         "coli_moe_dbg_dispatch": ([P, i, P, P, P, P, P], i),
+        "coli_moe_dbg_rmsnorm": ([P, i, i, P, P], i),
         "coli_moe_dbg_block_dots": ([P, i, i, P, P, P], i),
         "coli_moe_dbg_forward_intermediates": ([P, i, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P], i),
         "coli_moe_dbg_expert_hidden": ([P, P, P, P, i, P, P, P, P], i),
@@ -139,6 +143,20 @@ def layer_forward(x, router_w, router_bias, expert_w4, expert_rowscale, shared_w
                                        _ptr(expert_w4), _ptr(expert_rowscale), _ptr(shared_w4),
                                        _ptr(shared_rowscale), _ptr(out), _stream(stream)),
            "layer_forward")
+    return out
+
+
+def layer_forward_residual(x, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                           shared_rowscale, out=None, stream=None):
+    """out = x + MoE(x) (one layer of a stacked decoder, residual fused)."""
+    if out is None:
+        out = torch.empty_like(x)
+    n_tok = x.shape[0] if x.dim() == 2 else 0
+    _check(_lib.coli_moe_layer_forward_residual(_ptr(x), n_tok, _ptr(router_w), _ptr(router_bias),
+                                                _ptr(expert_w4), _ptr(expert_rowscale),
+                                                _ptr(shared_w4), _ptr(shared_rowscale), _ptr(out),
+                                                _stream(stream)),
+           "layer_forward_residual")
     return out
 
 
@@ -280,6 +298,14 @@ def dbg_forward_intermediates(x, router_w, router_bias, expert_w4, expert_rowsca
         _ptr(r["idx"]), _ptr(r["w"]), _ptr(r["qh"]), _ptr(r["dh"]), _ptr(r["y"]),
         _stream(stream)), "dbg_forward_intermediates")
     return r
+
+
+def dbg_rmsnorm(x, stream=None):
+    """The stacked layer's pre-norm alone: x / sqrt(mean(x^2) + 1e-6) per token."""
+    xn = torch.empty_like(x)
+    _check(_lib.coli_moe_dbg_rmsnorm(_ptr(x), x.shape[0], x.shape[1], _ptr(xn), _stream(stream)),
+           "dbg_rmsnorm")
+    return xn
 
 
 def dbg_expert_hidden(ew4, ers, qx, dx, ffn, stream=None):

@@ -41,6 +41,7 @@ struct ExpertArgs {
     float *h_dbg;                   // optional [P+T][F] hidden before requantisation
     float *y;                       // [P+T][H] expert outputs, by position
     float *out;                     // [T][H]
+    const float *res;               // optional [T][H] residual: out = res + layer output
     int *g_done;                    // [n_tiles] finished gate/up units per tile
     int *w_done;                    // [H/64] finished down units per row chunk
     int *work_counter;              // next unit to claim
@@ -109,6 +110,9 @@ constexpr int ROUTE_SMALL_MAX_T = 8;
 void count_launch();
 
 int launch_q8_0(const float *x, long n, int8_t *q, float *d, cudaStream_t st);
+// Pre-norm of a stacked layer (xn = x / sqrt(mean(x^2) + eps) per token).
+constexpr float RMSNORM_EPS = 1e-6f;
+int launch_rmsnorm(const float *x, int T, int H, float eps, float *xn, cudaStream_t st);
 int launch_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *scale, cudaStream_t st);
 int launch_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q, int32_t *I, cudaStream_t st);
 
@@ -144,7 +148,7 @@ int launch_gather_x(const int8_t *qx, const int32_t *pos_token, const int32_t *o
 int launch_gemm_items(const int32_t *counts, const int32_t *offsets, int E, int T, int P, int32_t *item_expert,
                       int32_t *item_pos0, int32_t *item_m, int32_t *n_items, cudaStream_t st);
 int launch_gemm(bool gateup, const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st);
-int launch_combine(const float *y, const int32_t *inv, const float *wts, int T, int k, int P, int H, float *out,
-                   cudaStream_t st);
+int launch_combine(const float *y, const int32_t *inv, const float *wts, int T, int k, int P, int H,
+                   const float *res, float *out, cudaStream_t st);
 
 }  // namespace coli

@@ -43,6 +43,7 @@ struct Workspace {
     float *dh = nullptr;
     float *y = nullptr;
     float *x_io = nullptr, *out_io = nullptr;
+    float *xn = nullptr;             // [T][H] normalised input of a stacked layer
     int *status = nullptr;
     // grouped tensor-core path
     uint16_t *xg = nullptr;          // [R'][H] bf16 codes of x by dispatch position
@@ -297,6 +298,7 @@ int coli_moe_configure(const coli_moe_shape *s)
         {(void **)&w.y, R * H * 4},
         {(void **)&w.x_io, T * H * 4},
         {(void **)&w.out_io, T * H * 4},
+        {(void **)&w.xn, T * H * 4},
         {(void **)&w.status, 4},
         {(void **)&w.xg, Ra * H * 2},
         {(void **)&w.qhb, Ra * F * 2},
@@ -536,7 +538,7 @@ static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *
     a.tile_expert = w.tile_expert; a.tile_pos0 = w.tile_pos0; a.tile_m = w.tile_m;
     a.n_tiles = w.n_tiles;
     a.inv = w.inv; a.wts = w.wts;
-    a.qh = w.qh; a.dh = w.dh; a.h_dbg = nullptr; a.y = w.y; a.out = nullptr;
+    a.qh = w.qh; a.dh = w.dh; a.h_dbg = nullptr; a.y = w.y; a.out = nullptr; a.res = nullptr;
     a.g_done = w.sync;
     a.w_done = w.sync + g.max_tiles;
     a.work_counter = w.sync + g.max_tiles + s.hidden / 64;
@@ -553,7 +555,7 @@ static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *
 static int forward_impl(const float *x, int n_tok, const float *router_w, const float *router_bias,
                         const uint8_t *expert_w4, const float *expert_rowscale,
                         const uint8_t *shared_w4, const float *shared_rowscale, float *out,
-                        cudaStream_t st)
+                        cudaStream_t st, const float *res = nullptr)
 {
     const coli_moe_shape &s = g.s;
     Workspace &w = g.ws;
@@ -614,12 +616,13 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
         if (g.timing) CUDA_OK(cudaEventRecord(e1, st));
         ga.trace = nullptr;   // the stage log covers the gate/up kernel
         LAUNCH_OK(launch_gemm(false, g.gemm_dn, ga, g.num_sms, st));
-        LAUNCH_OK(launch_combine(w.y, w.inv, w.wts, T, k, P, H, out, st));
+        LAUNCH_OK(launch_combine(w.y, w.inv, w.wts, T, k, P, H, res, out, st));
         return COLI_OK;
     }
 
     ExpertArgs a = expert_args(T, expert_rowscale, shared_rowscale);
     a.out = out;
+    a.res = res;
     if (g.timing) {
         int r = timing_events(&e0, &e1);
         if (r != COLI_OK) return r;
@@ -640,6 +643,29 @@ int coli_moe_layer_forward(const float *x, int n_tok, const float *router_w,
     if (st != COLI_OK || n_tok == 0) return st;
     return forward_impl(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
                         shared_rowscale, out, (cudaStream_t)stream);
+}
+
+int coli_moe_layer_forward_residual(const float *x, int n_tok, const float *router_w,
+                                    const float *router_bias, const uint8_t *expert_w4,
+                                    const float *expert_rowscale, const uint8_t *shared_w4,
+                                    const float *shared_rowscale, float *out, void *stream)
+{
+    int st = check_forward_args(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale,
+                                shared_w4, shared_rowscale, out);
+    if (st != COLI_OK || n_tok == 0) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    LAUNCH_OK(launch_rmsnorm(x, n_tok, g.s.hidden, RMSNORM_EPS, g.ws.xn, cs));
+    return forward_impl(g.ws.xn, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                        shared_rowscale, out, cs, x);
+}
+
+int coli_moe_dbg_rmsnorm(const float *x, int n_tok, int hidden, float *xn, void *stream)
+{
+    if (n_tok < 0 || hidden <= 0 || hidden % 4 != 0) return COLI_E_INVAL;
+    if (n_tok == 0) return COLI_OK;
+    if (!x || !xn || !aligned16(x) || !aligned16(xn)) return COLI_E_INVAL;
+    LAUNCH_OK(launch_rmsnorm(x, n_tok, hidden, RMSNORM_EPS, xn, (cudaStream_t)stream));
+    return COLI_OK;
 }
 
 int coli_moe_layer_forward_hostio(const float *x_host, int n_tok, const float *router_w,

@@ -530,6 +530,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                         o = __fmaf_rn(__ldcg(a.wts + (size_t)t * k + rr),
                                       __ldcg(a.y + (size_t)pos * H + col), o);
                     }
+                    if (a.res) o = __fadd_rn(__ldg(a.res + (size_t)t * H + col), o);
                     a.out[(size_t)t * H + col] = o;
                 }
                 named_barrier(BAR_CONSUMERS, CONSUMERS);

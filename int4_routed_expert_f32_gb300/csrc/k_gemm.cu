@@ -259,10 +259,11 @@ __global__ void k_gemm_items(const int32_t *__restrict__ counts, const int32_t *
 
 // Combine: out[t] = y[shared row of t], then + w_r * y[pair (t, r)] for the
 // ranks r in order, one fused multiply-add each (the method's weighted sum of
-// the shared expert and the k routed experts).
+// the shared expert and the k routed experts); with `res`, the residual of a
+// stacked decoder is added last: out = res + that sum.
 __global__ void __launch_bounds__(256) k_combine(const float *__restrict__ y, const int32_t *__restrict__ inv,
                                                  const float *__restrict__ wts, int T, int k, int P, int H,
-                                                 float *__restrict__ out)
+                                                 const float *__restrict__ res, float *__restrict__ out)
 {
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;   // 4 columns
     const int per = H / 4;
@@ -278,6 +279,13 @@ __global__ void __launch_bounds__(256) k_combine(const float *__restrict__ y, co
         o.y = __fmaf_rn(w, v.y, o.y);
         o.z = __fmaf_rn(w, v.z, o.z);
         o.w = __fmaf_rn(w, v.w, o.w);
+    }
+    if (res) {
+        const float4 r = reinterpret_cast<const float4 *>(res + (size_t)t * H)[c];
+        o.x = __fadd_rn(r.x, o.x);
+        o.y = __fadd_rn(r.y, o.y);
+        o.z = __fadd_rn(r.z, o.z);
+        o.w = __fadd_rn(r.w, o.w);
     }
     reinterpret_cast<float4 *>(out + (size_t)t * H)[c] = o;
 }
@@ -662,12 +670,12 @@ int launch_gemm_items(const int32_t *counts, const int32_t *offsets, int E, int 
     return 0;
 }
 
-int launch_combine(const float *y, const int32_t *inv, const float *wts, int T, int k, int P, int H, float *out,
-                   cudaStream_t st)
+int launch_combine(const float *y, const int32_t *inv, const float *wts, int T, int k, int P, int H,
+                   const float *res, float *out, cudaStream_t st)
 {
     const long n = (long)T * (H / 4);
     if (n == 0) return 0;
-    k_combine<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, inv, wts, T, k, P, H, out);
+    k_combine<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, inv, wts, T, k, P, H, res, out);
     count_launch();
     return 0;
 }

@@ -101,3 +101,65 @@ int launch_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q, int32
 }
 
 }  // namespace coli
+
+namespace coli {
+
+// ---------------------------------------------------------------------------
+// Pre-norm of a stacked decoder layer: xn = x / sqrt(mean(x^2) + eps) per
+// token, no learned gain.  The sum of squares follows the router logits' fixed
+// order (chunks of 4 into 256 partials, chunks ascending, one fma per element;
+// xor-butterfly folds over 32 and then 8), and the scalar steps are single
+// IEEE operations, so the result is reproducible bit for bit.  One block of
+// 256 threads per token.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_rmsnorm(const float *__restrict__ x, int H, float eps,
+                                                 float *__restrict__ xn)
+{
+    const int t = blockIdx.x, j = threadIdx.x, lane = j & 31, warp = j >> 5;
+    const float4 *xt = reinterpret_cast<const float4 *>(x + (size_t)t * H);
+    float p = 0.0f;
+    for (int c = j; c < (H >> 2); c += 256) {
+        const float4 v = __ldg(xt + c);
+        p = __fmaf_rn(v.x, v.x, p);
+        p = __fmaf_rn(v.y, v.y, p);
+        p = __fmaf_rn(v.z, v.z, p);
+        p = __fmaf_rn(v.w, v.w, p);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(FULL, p, o));
+    __shared__ float red[8];
+    __shared__ float r_sh;
+    if (lane == 0) red[warp] = p;
+    __syncthreads();
+    if (j == 0) {
+        float s[8], tmp[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s[w] = red[w];
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) tmp[w] = __fadd_rn(s[w], s[w ^ o]);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s[w] = tmp[w];
+        }
+        const float ms = __fdiv_rn(s[0], (float)H);
+        r_sh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    }
+    __syncthreads();
+    const float r = r_sh;
+    float4 *ot = reinterpret_cast<float4 *>(xn + (size_t)t * H);
+    for (int c = j; c < (H >> 2); c += 256) {
+        const float4 v = __ldg(xt + c);
+        ot[c] = make_float4(__fmul_rn(v.x, r), __fmul_rn(v.y, r), __fmul_rn(v.z, r), __fmul_rn(v.w, r));
+    }
+}
+
+int launch_rmsnorm(const float *x, int T, int H, float eps, float *xn, cudaStream_t st)
+{
+    if (T <= 0) return 0;
+    k_rmsnorm<<<T, 256, 0, st>>>(x, H, eps, xn);
+    count_launch();
+    return 0;
+}
+
+}  // namespace coli

@@ -58,6 +58,7 @@ def lib():
             L.orc_router_logit.restype = f
             L.orc_route.argtypes = [P, i, i, P, P, i, i, f, P, P, P, P]
             L.orc_dispatch.argtypes = [P, i, i, i, P, P, P, P]
+            L.orc_rmsnorm.argtypes = [P, i, i, f, P]
             L.orc_block_dots.argtypes = [P, i, i, P, P]
             L.orc_rows_dot.argtypes = [P, P, i, i, P, P, P]
             L.orc_expert_ffn.argtypes = [P, P, i, i, P, P, P, P, P, P, P, P]
@@ -145,6 +146,19 @@ def route(x, W, bias, k, routed_scale, want_logits=False):
     if want_logits:
         return idx, w, logits, sigma
     return idx, w
+
+
+RMSNORM_EPS = 1e-6
+
+
+def rmsnorm(x, eps=RMSNORM_EPS):
+    """Pre-norm of a stacked layer: x_k / sqrt(mean(x^2) + eps) per token, the
+    sum of squares in the router's canonical order (see orc_rmsnorm)."""
+    x = _c(x, np.float32)
+    T, H = x.shape
+    out = np.empty_like(x)
+    lib().orc_rmsnorm(_p(x), T, H, float(eps), _p(out))
+    return out
 
 
 def dispatch(idx, E):

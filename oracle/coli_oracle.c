@@ -246,6 +246,25 @@ ORC_API void orc_route(const float *x, int T, int H, const float *W, const float
     }
 }
 
+/* Pre-norm of one layer of a stacked decoder (a reading: the multi-layer
+ * sweep of the benchmark configurations chains layers with a residual add;
+ * without a norm the SwiGLU output grows as the square of its input and the
+ * stream overflows within a few layers, so each layer reads RMSNorm(x) as in
+ * GLM-class decoders, with no learned gain).  Per token: ss = sum of x_k^2 in
+ * the router's canonical order (the router dot of x with itself), ms = ss / H,
+ * r = 1 / sqrtf(ms + eps), xn_k = x_k * r; every step one IEEE operation. */
+ORC_API void orc_rmsnorm(const float *x, int T, int H, float eps, float *xn)
+{
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const float *xt = x + (size_t)t * H;
+        const float ss = orc_router_logit(xt, xt, H);
+        const float ms = ss / (float)H;
+        const float r = 1.0f / sqrtf(ms + eps);
+        for (int k = 0; k < H; ++k) xn[(size_t)t * H + k] = xt[k] * r;
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* O4  Batch-union dispatch: histogram and stable permutation  [P3 Technical  */
 /*     excellence: batch-union MoE in prefill]                               */

@@ -155,3 +155,23 @@ def test_prefill_2048_sampled(coli, glm, orc):
     want = ref_p.forward(x[sample])
     assert_float_close(got[sample], want)
     np.testing.assert_array_equal(got[sample], want)
+
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_tiny_residual_forward(coli, tiny, path):
+    """layer_forward_residual = x + the layer's output on RMSNorm(x), the add
+    fused into the combine (one F32 add, as the stacked-layer sweep chains its
+    layers)."""
+    wl, L, ref = tiny
+    _configure(coli, wl, 64)
+    T = 37
+    x = synth.activations(wl, 21, n_tok=T)
+    coli.set_path(coli.PATH_GEMM if path == "gemm" else coli.PATH_GEMV)
+    try:
+        got = coli.layer_forward_residual(_cuda(x), L["router_w"], L["router_b"], L["expert_w4"],
+                                          L["expert_rs"], L["shared_w4"], L["shared_rs"]).cpu().numpy()
+    finally:
+        coli.set_path(coli.PATH_AUTO)
+    import oracle
+    want = (x + ref.forward(oracle.rmsnorm(x))).astype(np.float32)
+    np.testing.assert_array_equal(got, want)

@@ -138,3 +138,14 @@ def test_expert_hidden_requant_bitexact(coli, orc, wl_name, n):
     q2, d2 = orc.q8_0(h)
     np.testing.assert_array_equal(qh, q2)
     np.testing.assert_array_equal(dh.view(np.uint32), d2.view(np.uint32))
+
+
+def test_rmsnorm_bit_exact():
+    """The stacked layer's pre-norm: same F32 operation sequence as the oracle."""
+    import oracle
+    import int4_routed_expert_f32_gb300 as coli
+    rng = np.random.default_rng(11)
+    for T, H in ((5, 6144), (3, 256), (1, 128)):
+        x = (rng.standard_normal((T, H)) * rng.uniform(0.01, 100.0, size=(T, 1))).astype(np.float32)
+        got = coli.dbg_rmsnorm(torch.from_numpy(x).cuda()).cpu().numpy()
+        np.testing.assert_array_equal(got, oracle.rmsnorm(x))

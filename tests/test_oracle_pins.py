@@ -418,3 +418,40 @@ def test_forward_rejects_missing_expert(orc):
     ew4[int(idx[0, 0])] = None
     with pytest.raises(ValueError):
         orc.moe_forward(x, W, b, ew4, ers, sw4, srs, wl.hidden, wl.ffn, wl.top_k, wl.routed_scale)
+
+
+# --------------------------------------------------------------------------- #
+# Pre-norm of the stacked-layer sweep: x / sqrt(mean(x^2) + eps)               #
+# --------------------------------------------------------------------------- #
+def test_rmsnorm_constant_vector_gives_unit_sign(orc):
+    """A constant row c (|c| = 2^10, so eps is below half an ulp of mean(x^2)):
+    mean(x^2) = c^2 exactly and every output is sign(c) exactly.  A sum in
+    place of the mean, or a missing square root, fails this."""
+    x = np.full((3, 256), 1024.0, np.float32)
+    x[1] = -1024.0
+    x[2, :128] = 1024.0
+    x[2, 128:] = -1024.0
+    xn = orc.rmsnorm(x)
+    np.testing.assert_array_equal(xn, np.sign(x))
+
+
+def test_rmsnorm_power_of_two_scaling_is_exact(orc):
+    """Scaling a row by 2 scales every partial sum by 4 exactly and the root
+    by 2 exactly, so the output does not change in any bit (eps absorbed)."""
+    x = (np.random.default_rng(5).standard_normal((4, 6144)) * 1024.0).astype(np.float32)
+    np.testing.assert_array_equal(orc.rmsnorm(x), orc.rmsnorm((2.0 * x).astype(np.float32)))
+
+
+def test_rmsnorm_matches_double_precision(orc):
+    rng = np.random.default_rng(6)
+    for H in (256, 6144):
+        x = rng.standard_normal((7, H)).astype(np.float32) * np.float32(3.0)
+        xd = x.astype(np.float64)
+        want = xd / np.sqrt(np.mean(xd * xd, axis=1, keepdims=True) + 1e-6)
+        got = orc.rmsnorm(x)
+        assert np.max(np.abs(got - want) / np.abs(want).max()) < 2e-6
+
+
+def test_rmsnorm_zero_row_is_zero(orc):
+    x = np.zeros((2, 256), np.float32)
+    np.testing.assert_array_equal(orc.rmsnorm(x), x)
