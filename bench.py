@@ -140,11 +140,13 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- #
-def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: int = 0):
+def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: int = 0,
+                    min_seconds: float = 0.0):
     """Time the CPU oracle on a bounded sample of the workload (forwards of the
     same shape, or the first `max_tokens` tokens of each when that is set: the
     oracle's cost is per token and expert, so a token subset keeps its rate);
-    returns (tok/s, threads, sample description)."""
+    the timed loop cycles over the sample's inputs until at least `min_seconds`
+    have passed; returns (tok/s, threads, sample description)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
     from helpers import OracleLayer
@@ -178,9 +180,14 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: in
         for e in set(int(v) for v in idx.ravel()):
             ref.expert(e)
     t0 = time.perf_counter()
-    for x in xs:
-        ref.forward(x)
-    dt = time.perf_counter() - t0
+    done = 0
+    while True:
+        ref.forward(xs[done % len(xs)])
+        done += 1
+        dt = time.perf_counter() - t0
+        if done >= n_forwards and dt >= min_seconds:
+            break
+    n_forwards = done
     toks = n_forwards * xs[0].shape[0]
     sub = f" (first {xs[0].shape[0]} of {wl.n_tok} tokens)" if xs[0].shape[0] < wl.n_tok else ""
     return toks / dt, oracle.num_threads(), (f"{n_forwards} forwards x {xs[0].shape[0]} tokens of the {wl.name} "
@@ -253,7 +260,8 @@ def run(args):
     coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
     path = {"auto": coli.PATH_AUTO, "gemv": coli.PATH_GEMV, "gemm": coli.PATH_GEMM}[args.path]
     coli.set_path(path)
-    use_gemm = path == coli.PATH_GEMM or (path == coli.PATH_AUTO and T >= coli.GEMM_MIN_TOKENS)
+    use_gemm = path == coli.PATH_GEMM or (path == coli.PATH_AUTO and
+                                          coli.auto_uses_gemm(T, wl.top_k, wl.n_experts))
     t_build = time.perf_counter()
     L = build_device_layer(wl)
     W, b = synth.router(wl)
@@ -385,7 +393,7 @@ def run(args):
     if rank == 0 and not args.no_cpu_baseline:
         mt = CPU_SAMPLE_TOKENS.get(wl.name, 0)
         nf = args.cpu_forwards if T <= 64 else 1
-        tps, cores, sample = oracle_baseline(wl, nf, max_tokens=mt)
+        tps, cores, sample = oracle_baseline(wl, nf, max_tokens=mt, min_seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -530,6 +538,8 @@ def main():
                                                           "prefill_profile", "sweep"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-forwards", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum oracle time of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     big = synth.WORKLOADS[args.workload].n_tok > 64

@@ -130,9 +130,12 @@ int coli_moe_layer_forward_hostio(const float *x_host, int n_tok,
  * tokens runs the grouped tensor-core GEMM (the batch union of all experts:
  * gather of the activation codes by dispatch position, gate/up GEMM with
  * SiLU*up and Q8_0 of h, down GEMM, combine), a smaller one the streaming GEMV
- * kernel; <= 0 keeps the built-in threshold (COLI_GEMM_MIN_TOKENS).  Returns
- * COLI_E_INVAL for an unknown path.  Takes effect at the next forward. */
-#define COLI_GEMM_MIN_TOKENS 64
+ * kernel.  <= 0 keeps the built-in threshold: n_tok * top_k >=
+ * COLI_GEMM_MIN_PAIRS_PER_EXPERT * n_experts, i.e. an average of 7 routed
+ * tokens per expert (224 tokens for 256 experts top-8; measured crossover on
+ * that shape between 192 and 256).  Returns COLI_E_INVAL for an unknown path.
+ * Takes effect at the next forward. */
+#define COLI_GEMM_MIN_PAIRS_PER_EXPERT 7
 int coli_moe_set_path(int path, int gemm_min_tokens);
 
 /* Synchronise `stream`, then read and clear the device status word.

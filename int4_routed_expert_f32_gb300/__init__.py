@@ -21,7 +21,14 @@ LIB_PATH = os.path.join(_HERE, "libcoli_moe.so")
 
 OK, E_INVAL, E_NOSHAPE, E_NOMEM, E_CUDA, E_TIMEOUT, E_UNIMPL, E_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
 PATH_AUTO, PATH_GEMV, PATH_GEMM = 0, 1, 2
-GEMM_MIN_TOKENS = 64   # COLI_GEMM_MIN_TOKENS: AUTO runs the grouped GEMM from this batch size
+GEMM_MIN_PAIRS_PER_EXPERT = 7   # AUTO runs the grouped GEMM when n_tok * top_k >= 7 * n_experts
+
+
+def auto_uses_gemm(n_tok: int, top_k: int, n_experts: int, gemm_min_tokens: int = 0) -> bool:
+    """The AUTO path's choice (mirrors the library's rule)."""
+    if gemm_min_tokens > 0:
+        return n_tok >= gemm_min_tokens
+    return n_tok * top_k >= GEMM_MIN_PAIRS_PER_EXPERT * n_experts
 
 EXPORTS = (
     "coli_moe_configure", "coli_moe_layer_forward", "coli_moe_layer_forward_residual",

@@ -561,8 +561,9 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
     Workspace &w = g.ws;
     const int T = n_tok, H = s.hidden, E = s.n_experts, k = s.top_k;
 
-    const int thr = g.gemm_min_tokens > 0 ? g.gemm_min_tokens : COLI_GEMM_MIN_TOKENS;
-    const bool use_gemm = g.path == COLI_PATH_GEMM || (g.path == COLI_PATH_AUTO && T >= thr);
+    const bool big = g.gemm_min_tokens > 0 ? T >= g.gemm_min_tokens
+                                           : (long)T * k >= (long)COLI_GEMM_MIN_PAIRS_PER_EXPERT * E;
+    const bool use_gemm = g.path == COLI_PATH_GEMM || (g.path == COLI_PATH_AUTO && big);
     ExpertMaps maps;
     if (use_gemm) {
         if (!gemm_weight_maps(expert_w4, E, shared_w4)) return COLI_E_CUDA;
