@@ -49,8 +49,8 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "00524302bf4d8fac4b59627bc702b81fc48b5d9998f92bbe5a283405d3b7516a",
-        "bytes_per_launch": 173843200,   # 170.32 MB read + 3.52 MB written
+        "sha256": "e894f682ed2171bd2b69bdc228e7bb67b34233547caf0f4ad22adc12b2dc3bf9",
+        "bytes_per_launch": 173524224,   # 170.32 MB read + 3.21 MB written
         # a launch of the 16-expert profile workload streams 8 routed + 1 shared
         # expert, the same units as one decode forward over 256 experts
         "workloads": ("decode", "profile"),

@@ -454,7 +454,7 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                 }
             }
         }
-    } else if (warp < 2 + G_CONV_WARPS) {
+    } else if (warp >= 2 && warp < 2 + G_CONV_WARPS) {
         // ------------------------------ converters ------------------------------
         // packed weights [GN rows][GK/2 bytes] -> bf16 [GN][GK] in the swizzled layout
         const int ct = threadIdx.x - 64;            // 0 .. 127
