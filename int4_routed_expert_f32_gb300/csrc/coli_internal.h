@@ -27,6 +27,7 @@ struct ExpertArgs {
     int gate_up_only;               // 1: stop after h (stage tests)
     const float *expert_rs;         // [E][2F+H]
     const float *shared_rs;         // [2F+H]
+    const uint8_t *shared_w4;       // [3FH/2] packed shared expert (prefetched into L2 during routing)
     const int8_t *qx;               // [T][H]
     const float *dx;                // [T][H/32]
     const int32_t *pos_token;       // [P+T] token of each dispatch position
@@ -95,6 +96,7 @@ struct RouteArgs {
     int8_t *qx;
     float *dx;
     float *logits;
+    float *sig, *key;               // [T][E] sigma and selection key (sigma + bias)
     int32_t *idx;
     float *wts;
     int32_t *counts, *offsets, *perm, *inv, *pos_token;

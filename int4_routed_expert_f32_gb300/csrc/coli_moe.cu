@@ -31,6 +31,7 @@ struct Workspace {
     int8_t *qx = nullptr;
     float *dx = nullptr;
     float *logits = nullptr;
+    float *sig = nullptr, *key = nullptr;
     int32_t *idx = nullptr;
     float *wts = nullptr;
     int32_t *counts = nullptr, *offsets = nullptr, *perm = nullptr, *inv = nullptr;
@@ -280,6 +281,8 @@ int coli_moe_configure(const coli_moe_shape *s)
         {(void **)&w.qx, T * H},
         {(void **)&w.dx, T * (H / 32) * 4},
         {(void **)&w.logits, T * E * 4},
+        {(void **)&w.sig, T * E * 4},
+        {(void **)&w.key, T * E * 4},
         {(void **)&w.idx, P * 4},
         {(void **)&w.wts, P * 4},
         {(void **)&w.counts, E * 4},
@@ -534,6 +537,7 @@ static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *
     a.KC = stage_kc(s.hidden, s.ffn);
     a.gate_up_only = 0;
     a.expert_rs = expert_rowscale; a.shared_rs = shared_rowscale;
+    a.shared_w4 = nullptr;
     a.qx = w.qx; a.dx = w.dx; a.pos_token = w.pos_token;
     a.tile_expert = w.tile_expert; a.tile_pos0 = w.tile_pos0; a.tile_m = w.tile_m;
     a.n_tiles = w.n_tiles;
@@ -576,6 +580,7 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
         r.x = x; r.T = T; r.H = H; r.E = E; r.k = k; r.routed_scale = s.routed_scale;
         r.W = router_w; r.bias = router_bias;
         r.qx = w.qx; r.dx = w.dx; r.logits = w.logits; r.idx = w.idx; r.wts = w.wts;
+        r.sig = w.sig; r.key = w.key;
         r.counts = w.counts; r.offsets = w.offsets; r.perm = w.perm; r.inv = w.inv;
         r.pos_token = w.pos_token;
         r.tile_expert = w.tile_expert; r.tile_pos0 = w.tile_pos0; r.tile_m = w.tile_m;
@@ -624,6 +629,7 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
     ExpertArgs a = expert_args(T, expert_rowscale, shared_rowscale);
     a.out = out;
     a.res = res;
+    a.shared_w4 = shared_w4;
     if (g.timing) {
         int r = timing_events(&e0, &e1);
         if (r != COLI_OK) return r;

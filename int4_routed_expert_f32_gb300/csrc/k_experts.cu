@@ -299,6 +299,20 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
         prefetch_tmap(&maps.sgu);
         prefetch_tmap(&maps.sdn);
     }
+    // The shared expert runs on every token whatever the routing: while the
+    // routing grid is still running, the blocks spread an L2 prefetch of its
+    // packed weights over themselves, so that its units read from L2 and HBM
+    // does not sit idle during routing.
+    if (a.shared_w4 && threadIdx.x == 32 * CONSUMER_WARPS) {
+        const size_t total_b = (size_t)3 * F * H / 2;            // multiple of 16 (H, F % 128 == 0)
+        const size_t per = ((total_b / gridDim.x) + 4095) & ~(size_t)4095;
+        const size_t b0 = (size_t)blockIdx.x * per;
+        const size_t b1 = b0 + per < total_b ? b0 + per : total_b;
+        for (size_t o = b0; o < b1; o += 16384) {
+            const size_t n = b1 - o < 16384 ? b1 - o : 16384;
+            prefetch_l2_bulk(a.shared_w4 + o, (uint32_t)n);
+        }
+    }
     __syncthreads();
     // routing results (tile list, activations) are complete past this point
     asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -502,6 +502,11 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
             for (int w = 0; w < 8; ++w) s8[w] = tmp[w];
         }
         ra.logits[(size_t)tid * E + e] = s8[0];
+        // sigma and the selection key here, in every block, rather than in
+        // the last block's serial tail
+        const float sg = own_sigmoid(s8[0]);
+        ra.sig[(size_t)tid * E + e] = sg;
+        ra.key[(size_t)tid * E + e] = __fadd_rn(sg, __ldg(ra.bias + e));
     }
 
     // 3. the last block routes
@@ -529,15 +534,16 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     __shared__ int s_cnt[MAX_E], s_base[MAX_E], s_tile0[MAX_E], s_off[MAX_E];
     __shared__ int s_ntiles;
     __shared__ float s_key[ROUTE_SMALL_MAX_T][MAX_E], s_sg[ROUTE_SMALL_MAX_T][MAX_E];
-    // sigma and selection key of every (token, expert), all threads at once
+    // sigma and selection key of every (token, expert), computed by the
+    // expert's block
 #pragma unroll 1
     for (int i = tid; i < T * E; i += 256) {
         const int t = i / E, ee = i - t * E;
-        const float sg = own_sigmoid(__ldcg(ra.logits + (size_t)t * E + ee));
-        s_sg[t][ee] = sg;
-        s_key[t][ee] = __fadd_rn(sg, ra.bias[ee]);
+        s_sg[t][ee] = __ldcg(ra.sig + (size_t)t * E + ee);
+        s_key[t][ee] = __ldcg(ra.key + (size_t)t * E + ee);
     }
     __syncthreads();
+    stamp(7);
     // Top-k by rank: expert e of token t ranks below every expert with a
     // larger key, and below equal keys of lower index (lowest-index ties);
     // it is selected, at position rank, iff rank < k.
@@ -557,16 +563,20 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
         }
     }
     __syncthreads();
+    stamp(8);
+    // S = sum of the chosen sigma in rank order (one thread per token), then
+    // the weights, one pair per thread
+    __shared__ float s_S[ROUTE_SMALL_MAX_T];
     if (tid < T) {
-        // S = sum of the chosen sigma in rank order, then the weights
         float S = 0.0f;
 #pragma unroll 1
         for (int r = 0; r < k; ++r) S = __fadd_rn(S, s_sig[tid * k + r]);
-#pragma unroll 1
-        for (int r = 0; r < k; ++r) {
-            ra.idx[(size_t)tid * k + r] = s_idx[tid * k + r];
-            ra.wts[(size_t)tid * k + r] = __fmul_rn(__fdiv_rn(s_sig[tid * k + r], S), ra.routed_scale);
-        }
+        s_S[tid] = S;
+    }
+    __syncthreads();
+    if (tid < T * k) {
+        ra.idx[tid] = s_idx[tid];
+        ra.wts[tid] = __fmul_rn(__fdiv_rn(s_sig[tid], s_S[tid / k]), ra.routed_scale);
     }
     __syncthreads();
     stamp(2);
