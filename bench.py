@@ -49,8 +49,8 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "e894f682ed2171bd2b69bdc228e7bb67b34233547caf0f4ad22adc12b2dc3bf9",
-        "bytes_per_launch": 173524224,   # 170.32 MB read + 3.21 MB written
+        "sha256": "8e41f205dd5b18a02dc44626503b61077574faf0a6cac9a37f910f533f227c8a",
+        "bytes_per_launch": 173469440,   # 170.74 MB read + 2.73 MB written
         # a launch of the 16-expert profile workload streams 8 routed + 1 shared
         # expert, the same units as one decode forward over 256 experts
         "workloads": ("decode", "profile"),
