@@ -71,6 +71,18 @@ def kernel_traffic(kernel: str, workload: str):
     return t["bytes_per_launch"] if h.hexdigest() == t["sha256"] else None
 
 
+def max_over_ranks(value: float, world: int, device: str = "cuda") -> float:
+    """The slowest rank's figure: whole-job timings take the max over ranks
+    (each rank times its own replica of the workload)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -309,11 +321,7 @@ def run(args):
         dist.barrier()
     launches = coli.launch_count()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), world)
 
     # dominant-kernel timing: the library records events around the expert
     # kernel; they serialise it behind routing, so this is a separate pass over
@@ -344,10 +352,7 @@ def run(args):
         coli.layer_forward_hostio(xh[s % n_h], L["router_w"], L["router_b"], L["expert_w4"],
                                   L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
         e2e_s += time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world)
 
     hbm_peak, bf16_peak, peak_kind = peaks()
     ub = np.array(unions[args.warmup:], dtype=np.float64)
@@ -414,10 +419,13 @@ def run_sweep(args):
     import int4_routed_expert_f32_gb300 as coli
     from synth.device import build_device_layer
 
+    import torch.distributed as dist
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
     wl = synth.WORKLOADS["sweep"]
     t_build = time.perf_counter()
     layers = [build_device_layer(wl, layer=l) for l in range(wl.layers)]
@@ -457,6 +465,8 @@ def run_sweep(args):
                 stack(xs[i % n_in])
             torch.cuda.synchronize()
             coli.launch_count()
+            if world > 1:
+                dist.barrier()
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
             for k in range(args.steps):
@@ -467,12 +477,12 @@ def run_sweep(args):
             torch.cuda.synchronize()
             launches_total += coli.launch_count()
             ms = [a.elapsed_time(b) for a, b in ev]
-            t = float(np.mean(ms))
+            t = max_over_ranks(float(np.mean(ms)), world)
             ub = [unions[k % n_in] for k in range(args.steps)]
             bytes_step = float(np.mean([sum(u_ + 1 for u_ in uu) for uu in ub])) * expert_bytes(wl)
             gbs = bytes_step / (t * 1e-3) / 1e9
-            per_b.append({"batch": B, "ms_per_step": t, "tok_s": B / (t * 1e-3), "weight_gbs": gbs,
-                          "weight_frac_of_hbm": gbs / hbm_peak,
+            per_b.append({"batch": B, "ms_per_step": t, "tok_s": world * B / (t * 1e-3),
+                          "weight_gbs_per_gpu": gbs, "weight_frac_of_hbm": gbs / hbm_peak,
                           "union_mean": float(np.mean([np.mean(uu) for uu in ub])),
                           "step_ms_p10_p50_p90": [float(np.percentile(ms, q)) for q in (10, 50, 90)]})
     status = coli.get_device_status()
@@ -504,15 +514,16 @@ def run_sweep(args):
         t0 = time.perf_counter()
         e2e_once()
         e2e_s += time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world)
     b1 = per_b[0]
     line = {
-        "metric": METRIC, "value": world * b1["tok_s"], "unit": "tok/s", "n_gpus": world,
+        "metric": METRIC, "value": b1["tok_s"], "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": b1["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32",
         "data": "synthetic",
         "config": workload_config(wl),
         "sweep": per_b,
-        "e2e": {"value": n_e2e * B / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": B * wl.hidden * 4,
+        "e2e": {"value": world * n_e2e * B / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": B * wl.hidden * 4,
                 "d2h_bytes_per_step": B * wl.hidden * 4},
         "gpu_launches": launches_total,
         "clocks": clocks.summary(),
@@ -521,11 +532,14 @@ def run_sweep(args):
         "peak_kind": f"{peak_kind} hbm_gbs",
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tps, cores, sample = oracle_baseline(wl, 2, max_tokens=CPU_SAMPLE_TOKENS["sweep"])
+        tps, cores, sample = oracle_baseline(wl, 2, max_tokens=CPU_SAMPLE_TOKENS["sweep"],
+                                             min_seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
 
 
 def main():
@@ -534,8 +548,8 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "verify", "prefill", "profile", "route_profile",
-                                                          "prefill_profile", "sweep"])
+    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "verify", "prefill", "profile",
+                                                          "route_profile", "prefill_profile", "sweep"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-forwards", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
