@@ -544,22 +544,60 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     }
     __syncthreads();
     stamp(7);
-    // Top-k by rank: expert e of token t ranks below every expert with a
-    // larger key, and below equal keys of lower index (lowest-index ties);
-    // it is selected, at position rank, iff rank < k.
+    if (T == 1) {
+        // Top-k by rank: expert e ranks below every expert with a larger key,
+        // and below equal keys of lower index (lowest-index ties); it is
+        // selected, at position rank, iff rank < k.  One expert per thread.
 #pragma unroll 1
-    for (int i = tid; i < T * E; i += 256) {
-        const int t = i / E, ee = i - t * E;
-        const float ke = s_key[t][ee];
-        int rank = 0;
+        for (int ee = tid; ee < E; ee += 256) {
+            const float ke = s_key[0][ee];
+            int rank = 0;
 #pragma unroll 4
-        for (int e2 = 0; e2 < E; ++e2) {
-            const float k2 = s_key[t][e2];
-            rank += (k2 > ke) | ((k2 == ke) & (e2 < ee));
+            for (int e2 = 0; e2 < E; ++e2) {
+                const float k2 = s_key[0][e2];
+                rank += (k2 > ke) | ((k2 == ke) & (e2 < ee));
+            }
+            if (rank < k) {
+                s_idx[rank] = ee;
+                s_sig[rank] = s_sg[0][ee];
+            }
         }
-        if (rank < k) {
-            s_idx[t * k + rank] = ee;
-            s_sig[t * k + rank] = s_sg[t][ee];
+    } else if (warp < T) {
+        // Several tokens: one warp per token (the rank method's cost grows
+        // with T), k rounds of a warp-wide argmax over the experts not yet
+        // taken under the same order: larger key first, then lower index.
+        // Lane l holds experts l, l+32, ...
+        const int t = warp;
+        unsigned taken = 0;                       // bit i: expert lane + 32 i taken
+#pragma unroll 1
+        for (int r = 0; r < k; ++r) {
+            float bk = 0.0f;
+            int be = -1;
+#pragma unroll 1
+            for (int i = 0; i < MAX_E / 32; ++i) {
+                const int ee = lane + 32 * i;
+                if (ee < E && !((taken >> i) & 1u)) {
+                    const float kv = s_key[t][ee];
+                    if (be < 0 || kv > bk) {      // ascending ee: the first of equal keys stays
+                        bk = kv;
+                        be = ee;
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const float ok = __shfl_xor_sync(FULL, bk, o);
+                const int oe = __shfl_xor_sync(FULL, be, o);
+                if (oe >= 0 && (be < 0 || ok > bk || (ok == bk && oe < be))) {
+                    bk = ok;
+                    be = oe;
+                }
+            }
+            if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
+            if (lane == 0) {
+                s_idx[t * k + r] = be;
+                s_sig[t * k + r] = be >= 0 ? s_sg[t][be] : 0.0f;
+            }
         }
     }
     __syncthreads();

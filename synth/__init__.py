@@ -104,6 +104,10 @@ WORKLOADS = {
     # with a small expert FFN (~0.6 GB resident): a small case for capturing the
     # routing kernel
     "route_profile": Workload("route_profile", 6144, 256, 256, 8, 1, 1),
+    # the verify batch (4 correlated tokens) on the decode shape with 16
+    # routed experts: a small case for capturing the 4-token expert kernel
+    "verify_profile": Workload("verify_profile", 6144, 2048, 16, 8, 4, 2, correlated_tokens=True,
+                               weight_seed=1),
     # the prefill shape on 16 routed experts and 256 tokens (~0.3 GB of
     # weights, 128 tokens per expert on average): a small case for capturing
     # the grouped-GEMM kernels
