@@ -92,13 +92,16 @@ __device__ __forceinline__ bool g_wait(uint64_t *bar, uint32_t parity, volatile 
     }
 }
 
-// Optional stage log.  Each block's region holds four sub-logs (producer,
-// MMA issuer, first converter warp, first drain warp); entry i >= 1 of a
-// sub-log is ((globaltimer << 8) | code, value) and entry 0 receives the
-// event count when the role finishes (the count lives in a register meanwhile,
-// so logging adds no memory round trip).  Only stages [tr0, tr0 + TRACE_NS)
-// of each block (and their blocks) are logged: a steady-state window after
-// the first unit.
+// Optional stage log.  Each block's region holds four sub-logs: 0 producer
+// (code 11: stage issued), 1 reserved for the MMA issuer (which stays
+// untraced: its loop bounds the tensor pipe), 2 first converter warp (14:
+// stage landed, 15: stage converted), 3 first drain warp (16: block's
+// accumulator ready, 17: block folded).  Entry i >= 1 of a sub-log is
+// ((globaltimer << 8) | code, value), the timer's top bits dropped; entry 0
+// receives the event count when the role finishes (the count lives in a
+// register meanwhile, so logging adds no memory round trip).  Only stages
+// [tr0, tr0 + TRACE_NS) of each block (and their blocks) are logged: a
+// steady-state window after the first unit.
 constexpr int TRACE_NS = 40;
 
 __device__ __forceinline__ void gtrace(const GemmArgs &g, int role, int &n, int code, int value)
