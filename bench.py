@@ -153,7 +153,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- #
 def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: int = 0,
-                    min_seconds: float = 0.0):
+                    min_seconds: float = 0.0, threads: int = 0):
     """Time the CPU oracle on a bounded sample of the workload (forwards of the
     same shape, or the first `max_tokens` tokens of each when that is set: the
     oracle's cost is per token and expert, so a token subset keeps its rate);
@@ -163,6 +163,14 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: in
     import oracle
     from helpers import OracleLayer
     oracle.build()
+    oracle.set_threads(threads)
+    try:
+        return _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens, min_seconds)
+    finally:
+        oracle.set_threads(0)
+
+
+def _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens, min_seconds):
     xs = [synth.activations(wl, seed_base + i) for i in range(n_forwards)]
     if max_tokens > 0:
         xs = [x[:max_tokens] for x in xs]
@@ -173,7 +181,7 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: in
 
         def stack(x):
             for r in refs:
-                x = (x + r.forward(x)).astype(np.float32)
+                x = (x + r.forward(oracle.rmsnorm(x))).astype(np.float32)
             return x
 
         for x in xs:
@@ -207,6 +215,19 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: in
 
 
 CPU_SAMPLE_TOKENS = {"prefill": 24, "sweep": 1}   # bounded oracle sample per forward (tokens)
+
+
+def cpu_baseline_line(wl, n_forwards: int, min_seconds: float):
+    """The oracle on all of the host's cores, plus a shorter single-thread
+    sample, with the host's machine type."""
+    import platform
+    mt = CPU_SAMPLE_TOKENS.get(wl.name, 0)
+    tps, cores, sample = oracle_baseline(wl, n_forwards, max_tokens=mt, min_seconds=min_seconds)
+    st_tps, _, st_sample = oracle_baseline(wl, max(1, n_forwards // 4), max_tokens=mt,
+                                           min_seconds=min_seconds / 3.0, threads=1)
+    return {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "machine": platform.machine(),
+            "single_thread": {"value": st_tps, "unit": "tok/s", "sample": st_sample}}
 
 
 def run_reference(args):
@@ -387,6 +408,9 @@ def run(args):
         "expert_path": "gemm" if use_gemm else "gemv",
         "weight_gbs_layer": bytes_per_fwd / (total_ms / args.steps * 1e-3) / 1e9,
         "tops_layer": 2.0 * macs_layer / (total_ms / args.steps * 1e-3) / 1e12,
+        # whole-layer bound: max(weight bytes / HBM peak, ops / bf16 peak) over the step time
+        "layer_roofline_frac": max(bytes_per_fwd / (hbm_peak * 1e9), 2.0 * macs_layer / (bf16_peak * 1e12))
+                               / (total_ms / args.steps * 1e-3),
         "e2e": {"value": world * args.steps * T / e2e_s, "unit": "tok/s",
                 "h2d_bytes_per_step": T * wl.hidden * 4, "d2h_bytes_per_step": T * wl.hidden * 4},
         "gpu_launches": launches,
@@ -396,11 +420,8 @@ def run(args):
         "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
     }
     if rank == 0 and not args.no_cpu_baseline:
-        mt = CPU_SAMPLE_TOKENS.get(wl.name, 0)
         nf = args.cpu_forwards if T <= 64 else 1
-        tps, cores, sample = oracle_baseline(wl, nf, max_tokens=mt, min_seconds=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
-                                "sample": sample}
+        line["cpu_baseline"] = cpu_baseline_line(wl, nf, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -443,12 +464,16 @@ def run_sweep(args):
                   for i in range(n_in)]
             bufs = [torch.empty((B, wl.hidden), dtype=torch.float32, device="cuda") for _ in range(2)]
 
-            def stack(x0, record_unions=None):
+            def stack(x0, record_unions=None, record_idx=None):
                 x = x0
                 for l, L in enumerate(layers):
                     if record_unions is not None:
-                        idx, _ = coli.dbg_route(x, L["router_w"], L["router_b"], wl.top_k)
-                        record_unions.append(len(set(idx.cpu().numpy().ravel().tolist())))
+                        xn = coli.dbg_rmsnorm(x)    # the layer routes its normalised input
+                        idx, _ = coli.dbg_route(xn, L["router_w"], L["router_b"], wl.top_k)
+                        idx = idx.cpu().numpy()
+                        record_unions.append(len(set(idx.ravel().tolist())))
+                        if record_idx is not None:
+                            record_idx.append(idx)
                     out = bufs[l & 1]
                     coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"],
                                                 L["expert_rs"], L["shared_w4"], L["shared_rs"], out=out)
@@ -456,10 +481,14 @@ def run_sweep(args):
                 return x
 
             unions = {}
+            overlaps = []
             for i in range(n_in):
-                u = []
-                stack(xs[i], u)
+                u, ids = [], []
+                stack(xs[i], u, ids)
                 unions[i] = u
+                for l in range(1, len(ids)):
+                    overlaps.append(np.mean([len(set(ids[l][t]) & set(ids[l - 1][t])) / wl.top_k
+                                             for t in range(B)]))
             for i in range(args.warmup):
                 flush.zero_()
                 stack(xs[i % n_in])
@@ -484,6 +513,7 @@ def run_sweep(args):
             per_b.append({"batch": B, "ms_per_step": t, "tok_s": world * B / (t * 1e-3),
                           "weight_gbs_per_gpu": gbs, "weight_frac_of_hbm": gbs / hbm_peak,
                           "union_mean": float(np.mean([np.mean(uu) for uu in ub])),
+                          "routing_overlap_prev_layer": float(np.mean(overlaps)),
                           "step_ms_p10_p50_p90": [float(np.percentile(ms, q)) for q in (10, 50, 90)]})
     status = coli.get_device_status()
     # end to end at batch 1: pinned host x in, the stack, host out
@@ -532,10 +562,7 @@ def run_sweep(args):
         "peak_kind": f"{peak_kind} hbm_gbs",
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tps, cores, sample = oracle_baseline(wl, 2, max_tokens=CPU_SAMPLE_TOKENS["sweep"],
-                                             min_seconds=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
-                                "sample": sample}
+        line["cpu_baseline"] = cpu_baseline_line(wl, 2, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

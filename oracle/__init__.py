@@ -66,6 +66,8 @@ def lib():
                                           P, P, P, P, P, P]
             L.orc_moe_forward.restype = i
             L.orc_num_threads.restype = i
+            L.orc_set_threads.argtypes = [i]
+            L.orc_set_threads.restype = None
             _lib = L
     return _lib
 
@@ -81,6 +83,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return lib().orc_num_threads()
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's OpenMP loops (n <= 0: the default)."""
+    lib().orc_set_threads(int(n))
 
 
 def pack_int4_rows(w):

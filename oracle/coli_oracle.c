@@ -435,10 +435,18 @@ done:
     return status;
 }
 
-/* Number of OpenMP threads the oracle will use (1 without OpenMP). */
+/* Number of OpenMP threads the oracle will use (1 without OpenMP), and a
+ * setter (n <= 0 restores the default); results do not depend on it. */
 #ifdef _OPENMP
 #include <omp.h>
+static int orc_default_threads = 0;
 ORC_API int orc_num_threads(void) { return omp_get_max_threads(); }
+ORC_API void orc_set_threads(int n)
+{
+    if (orc_default_threads == 0) orc_default_threads = omp_get_max_threads();
+    omp_set_num_threads(n > 0 ? n : orc_default_threads);
+}
 #else
 ORC_API int orc_num_threads(void) { return 1; }
+ORC_API void orc_set_threads(int n) { (void)n; }
 #endif
