@@ -57,7 +57,7 @@ struct ExpertArgs {
 // Tensor maps of one grouped-GEMM launch: the bf16 activation codes by
 // dispatch position (2-D, box 64 x 128, 128-byte swizzle) and the packed
 // weight rows of the routed experts and of the shared expert (3-D, box
-// 32 bytes x 64 or 128 rows x 1, no swizzle).
+// 32 bytes x 128 or 256 rows x 1, no swizzle).
 struct GemmMaps {
     CUtensorMap act;
     CUtensorMap w;

@@ -196,17 +196,17 @@ static bool encode_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t ro
 }
 
 // Weight maps of the grouped GEMM: 32 bytes (64 weights) of a row per stage,
-// 64 rows per box for gate/up (two boxes: gate rows, then the matching up
-// rows), 128 rows for down.
+// 128 rows per box for gate/up (two boxes: gate rows, then the matching up
+// rows), 256 rows for down (rows past the matrix read as zeros).
 static bool gemm_weight_maps(const uint8_t *ew4, int E, const uint8_t *sw4)
 {
     if (g.gemm_valid && g.gemm_key[0] == ew4 && g.gemm_key[1] == sw4) return true;
     const uint64_t H = g.s.hidden, F = g.s.ffn, stride = 3 * F * H / 2;
     GemmMaps gu{}, dn{};
-    bool ok = encode_rows(&gu.w, ew4, H / 2, 2 * F, (uint64_t)E, stride, 64, 32) &&
-              encode_rows(&gu.sw, sw4, H / 2, 2 * F, 1, stride, 64, 32) &&
-              encode_rows(&dn.w, ew4 + F * H, F / 2, H, (uint64_t)E, stride, 128, 32) &&
-              encode_rows(&dn.sw, sw4 + F * H, F / 2, H, 1, stride, 128, 32);
+    bool ok = encode_rows(&gu.w, ew4, H / 2, 2 * F, (uint64_t)E, stride, 128, 32) &&
+              encode_rows(&gu.sw, sw4, H / 2, 2 * F, 1, stride, 128, 32) &&
+              encode_rows(&dn.w, ew4 + F * H, F / 2, H, (uint64_t)E, stride, 256, 32) &&
+              encode_rows(&dn.sw, sw4 + F * H, F / 2, H, 1, stride, 256, 32);
     if (!ok) return false;
     gu.act = g.act_x;
     dn.act = g.act_h;

@@ -17,22 +17,26 @@
 // is bit-identical to both.
 //
 // Tile.  M = 128 dispatch positions (rows of operand A: the gathered bf16
-// codes of one expert's tokens), N = 128 weight rows (gate/up: 64 gate rows
-// and the 64 matching up rows; down: 128 output rows), K = 64 per pipeline
-// stage (two blocks).  A drain thread owns one token row and 32 columns, so
-// the per-(token, block) scale is one scalar, and a gate warp's 32 columns
-// are exactly one Q8_0 block of h: SiLU(gate)*up and the requantisation stay
-// inside threads (the up values come through shared memory).
+// codes of one expert's tokens), N = 256 weight rows (gate/up: 128 gate rows
+// and the 128 matching up rows; down: 256 output rows), K = 64 per pipeline
+// stage (two blocks).  The per-block exact fold makes every block a round
+// trip between the MMA thread and the drain warps, and each round trip costs
+// a roughly fixed number of cycles (MMA issue from one thread, commit, two
+// mbarrier hand-offs) whatever N is; N = 256, the widest single-CTA MMA,
+// gives each round trip the most work.  TMEM holds two such accumulators
+// (2 x 256 columns): the MMAs of one block run while the other is drained.
+// A drain thread owns one token row and 64 columns: 32 gate columns and the
+// 32 up columns of the same hidden units (down: two groups of 32 output
+// rows), so the per-(token, block) scale is one scalar, and SiLU(gate)*up and
+// the requantisation of that Q8_0 block of h stay inside the thread.
 //
-// Warp roles (24 warps = 6 warpgroups, one CTA per SM, persistent over units):
+// Warp roles (20 warps = 5 warpgroups, one CTA per SM, persistent over units):
 //   0      TMA producer (activation tile + packed weight rows)
 //   1      MMA issuer, owner of the TMEM allocation
-//   2..5   weight converters: packed int4 -> bf16 in the 128-byte-swizzled
+//   2..3   weight converters: packed int4 -> bf16 in the 128-byte-swizzled
 //          K-major layout the MMA reads
-//   6..7   idle (they complete the second warpgroup)
-//   8..23  drain + epilogue; warp w reads TMEM lanes 32*(w%4).. and columns
-//          32*((w-8)/4) ..  Sixteen warps keep four TMEM loads in flight per
-//          scheduler, which hides the load latency behind the FMAs.
+//   4..19  drain + epilogue; warp w reads TMEM lanes 32*(w%4).. and columns
+//          32*((w-4)/4) .. and 128 + 32*((w-4)/4) .. of an accumulator.
 //
 // Element order inside each 8-element K chunk, for both operands:
 // (k0, k2, k4, k6, k1, k3, k5, k7).  It is what splitting the packed bytes
@@ -49,28 +53,28 @@
 namespace coli {
 
 constexpr int GM = 128;                 // positions per tile (MMA M)
-constexpr int GN = 128;                 // weight rows per tile (MMA N)
+constexpr int GN = 256;                 // weight rows per tile (MMA N)
 constexpr int GK = 64;                  // K per stage (two Q8_0 blocks)
 constexpr int G_STAGES = 4;
-constexpr int G_NACC = 4;               // TMEM accumulators (one per block in flight)
+constexpr int G_NACC = 2;               // TMEM accumulators (one per block in flight)
 constexpr int A_BYTES = GM * GK * 2;    // 16 KB bf16, swizzled
-constexpr int B_BYTES = GN * GK * 2;    // 16 KB bf16, swizzled
-constexpr int RAW_BYTES = GN * GK / 2;  // 4 KB packed int4
-constexpr int XCH_LD = 65;              // padded row of the gate/up exchange tile
-constexpr int G_CONV_WARPS = 4;
-constexpr int G_DRAIN_WARP0 = 8;        // warps 0..7: producer, MMA, converters, 2 idle
-constexpr int G_DRAIN_WARPS = 16;       // 4 TMEM lane quarters x 4 column quarters
+constexpr int B_BYTES = GN * GK * 2;    // 32 KB bf16, swizzled
+constexpr int RAW_BYTES = GN * GK / 2;  // 8 KB packed int4
+constexpr int G_CONV_WARPS = 2;
+constexpr int G_DRAIN_WARP0 = 4;        // warps 0..3: producer, MMA, two converters
+constexpr int G_DRAIN_WARPS = 16;       // 4 TMEM lane quarters x 4 column groups
 constexpr int G_THREADS = 32 * (G_DRAIN_WARP0 + G_DRAIN_WARPS);
-// Register split (setmaxnreg, per warpgroup): the first two warpgroups give
-// registers to the four drain warpgroups.  The launch allocation must cover
-// the sum; the launcher checks it against the compiled register count.
-constexpr int G_REGS_CTRL = 40;
-constexpr int G_REGS_DRAIN = 96;
+// Register split (setmaxnreg, per warpgroup): the control warpgroup gives
+// registers to the four drain warpgroups (64 F32 accumulators per thread).
+// The launch allocation must cover the sum; the launcher checks it against
+// the compiled register count.
+constexpr int G_REGS_CTRL = 64;
+constexpr int G_REGS_DRAIN = 104;
 constexpr int G_TMEM_COLS = G_NACC * GN;
-constexpr int BAR_DRAIN = 3;
 constexpr uint64_t G_WAIT_NS = 2000000000ull;
 
 static_assert(G_TMEM_COLS <= 512, "TMEM has 512 columns");
+static_assert(32L * 4 * G_REGS_CTRL + 32L * G_DRAIN_WARPS * G_REGS_DRAIN <= 65536, "register split");
 
 __device__ __forceinline__ uint64_t g_timer()
 {
@@ -168,6 +172,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(addr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -305,8 +324,7 @@ struct GemmSmem {
 
 size_t gemm_smem_bytes()
 {
-    return 1024 + (size_t)G_STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + (size_t)GM * XCH_LD * 4 +
-           sizeof(GemmSmem);
+    return 1024 + (size_t)G_STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + sizeof(GemmSmem);
 }
 
 // GATEUP: A = gathered x codes (K = H), B = gate/up rows; epilogue SiLU*up and
@@ -320,8 +338,7 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
     unsigned char *sA = smem;                                   // [G_STAGES][A_BYTES]
     unsigned char *sB = sA + G_STAGES * A_BYTES;                // [G_STAGES][B_BYTES]
     unsigned char *sRaw = sB + G_STAGES * B_BYTES;              // [G_STAGES][RAW_BYTES]
-    float *xch = reinterpret_cast<float *>(sRaw + G_STAGES * RAW_BYTES);   // [GM][XCH_LD]
-    GemmSmem &S = *reinterpret_cast<GemmSmem *>(xch + GM * XCH_LD);
+    GemmSmem &S = *reinterpret_cast<GemmSmem *>(sRaw + G_STAGES * RAW_BYTES);
     volatile int *abort = &S.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -329,7 +346,10 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
     const int K = GATEUP ? H : F;
     const int nst = K / GK;                         // stages per unit
     const int nb = K / 32;                          // blocks per unit
-    const int per_item = GATEUP ? F / 64 : H / GN;  // weight tiles per item
+    // weight tiles per item: F/128 gate/up tiles; ceil(H/256) down tiles (the
+    // last one half past the matrix when H is an odd multiple of 128: the TMA
+    // box reads zeros there and the drain stores nothing for those rows)
+    const int per_item = GATEUP ? F / (GN / 2) : (H + GN - 1) / GN;
     const int n_units = *g.n_items * per_item;
     const int tr0 = nst + 8;                       // first traced stage
     const bool tr = g.trace != nullptr;
@@ -392,8 +412,10 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                     tma_load_2d(sA + slot * A_BYTES, &maps.act, s * GK, pos0, &S.full[slot]);
                     unsigned char *raw = sRaw + slot * RAW_BYTES;
                     if (GATEUP) {
-                        tma_load_3d(raw, wmap, s * (GK / 2), 64 * j, z, &S.full[slot], pol);
-                        tma_load_3d(raw + 64 * (GK / 2), wmap, s * (GK / 2), F + 64 * j, z, &S.full[slot], pol);
+                        // 128 gate rows, then the 128 matching up rows (32 bytes each)
+                        tma_load_3d(raw, wmap, s * (GK / 2), (GN / 2) * j, z, &S.full[slot], pol);
+                        tma_load_3d(raw + (GN / 2) * (GK / 2), wmap, s * (GK / 2), F + (GN / 2) * j, z,
+                                    &S.full[slot], pol);
                     } else {
                         tma_load_3d(raw, wmap, s * (GK / 2), GN * j, z, &S.full[slot], pol);
                     }
@@ -403,11 +425,10 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
-        // One thread issues every MMA of the CTA.  Its loop is kept short (the
-        // issue rate of a single thread bounds the tensor pipe at this tile
-        // size): per stage one wait for the converted operands (which implies
-        // the TMA data), one wait per accumulator of the stage's pair, one
-        // fence, four MMAs and three commits.
+        // One thread issues every MMA of the CTA.  Per stage: one wait for the
+        // converted operands (which implies the TMA data), then per block one
+        // wait for its accumulator to be drained, a fence, two K = 16 MMAs and
+        // a commit; a last commit frees the stage.
         if (lane == 0) {
             const int my_units =
                 (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -416,29 +437,28 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
             int slot = 0;
             uint32_t phase = 0;
             bool failed = false;
-            for (int sc = 0; sc < total; ++sc) {
-                const int pr = sc & 1;          // accumulator pair {2pr, 2pr+1} (blocks 2sc, 2sc+1)
-                const int puse = sc >> 1;       // earlier uses of the pair
-                bool ok = g_wait(&S.conv[slot], phase, abort);
-                if (ok && puse > 0) {
-                    const uint32_t tp = (uint32_t)((puse - 1) & 1);
-                    ok = g_wait(&S.tempty[2 * pr], tp, abort) && g_wait(&S.tempty[2 * pr + 1], tp, abort);
-                }
-                if (!ok) {
+            for (int sc = 0; sc < total && !failed; ++sc) {
+                if (!g_wait(&S.conv[slot], phase, abort)) {
                     failed = true;
                     break;
                 }
-                tc_fence_after();
                 // descriptor start addresses advance in 16-byte units: +2 per 32 bytes of K
                 const uint64_t da = dA + (uint64_t)(slot * (A_BYTES >> 4));
                 const uint64_t db = dB + (uint64_t)(slot * (B_BYTES >> 4));
-                const uint32_t d0 = tmem + (uint32_t)(2 * pr * GN);
-                umma_bf16(d0, da, db, 0u);
-                umma_bf16(d0, da + 2, db + 2, 1u);
-                umma_commit(&S.tfull[2 * pr]);
-                umma_bf16(d0 + GN, da + 4, db + 4, 0u);
-                umma_bf16(d0 + GN, da + 6, db + 6, 1u);
-                umma_commit(&S.tfull[2 * pr + 1]);
+#pragma unroll
+                for (int h = 0; h < G_NACC; ++h) {
+                    // block 2 sc + h goes to accumulator h, whose previous block was drained
+                    if (sc > 0 && !g_wait(&S.tempty[h], (uint32_t)((sc - 1) & 1), abort)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(h * GN);
+                    umma_bf16(d, da + 4 * h, db + 4 * h, 0u);
+                    umma_bf16(d, da + 4 * h + 2, db + 4 * h + 2, 1u);
+                    umma_commit(&S.tfull[h]);
+                }
+                if (failed) break;
                 umma_commit(&S.empty[slot]);    // the stage's operands may be overwritten
                 if (++slot == G_STAGES) {
                     slot = 0;
@@ -457,10 +477,14 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                 }
             }
         }
-    } else if (warp >= 2 && warp < 2 + G_CONV_WARPS) {
+    } else {
         // ------------------------------ converters ------------------------------
         // packed weights [GN rows][GK/2 bytes] -> bf16 [GN][GK] in the swizzled layout
-        const int ct = threadIdx.x - 64;            // 0 .. 127
+        const int ct = threadIdx.x - 32 * 2;        // 0 .. 63
+        constexpr int PIECES = GN * 2;              // (row, block) pieces of 16 packed bytes per stage
+        constexpr int PER = PIECES / (32 * G_CONV_WARPS);
+        constexpr int BATCH = 4;                    // packed loads in flight per thread
+        static_assert(PER % BATCH == 0, "converter batches");
         int sc = 0;
         int ntr = 0;
         for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
@@ -479,18 +503,23 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                 if (trc) gtrace(g, 2, ntr, 14, sc);
                 const unsigned char *raw = sRaw + slot * RAW_BYTES;
                 unsigned char *bt = sB + slot * B_BYTES;
-                // 256 (row, block) pieces of 16 bytes per stage, two per thread
 #pragma unroll 1
-                for (int pi = 0; pi < 2; ++pi) {
-                    const int piece = ct + 128 * pi;
-                    const int n = piece >> 1, blk = piece & 1;
-                    const uint4 w = *reinterpret_cast<const uint4 *>(raw + n * (GK / 2) + blk * 16);
-                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                for (int p0 = 0; p0 < PER; p0 += BATCH) {
+                    uint4 w[BATCH];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int c = blk * 4 + q;   // 8-element chunk along K
-                        *reinterpret_cast<uint4 *>(bt + n * 128 + ((c ^ (n & 7)) << 4)) =
-                            nibbles_to_bf16_chunk(wv[q]);
+                    for (int i = 0; i < BATCH; ++i)
+                        w[i] = *reinterpret_cast<const uint4 *>(raw + (size_t)(ct + 64 * (p0 + i)) * 16);
+#pragma unroll
+                    for (int i = 0; i < BATCH; ++i) {
+                        const int piece = ct + 64 * (p0 + i);
+                        const int n = piece >> 1, blk = piece & 1;
+                        const uint32_t wv[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int c = blk * 4 + q;   // 8-element chunk along K
+                            *reinterpret_cast<uint4 *>(bt + n * 128 + ((c ^ (n & 7)) << 4)) =
+                                nibbles_to_bf16_chunk(wv[q]);
+                        }
                     }
                 }
                 fence_proxy_async_shared();   // generic-proxy writes -> visible to the tensor core
@@ -505,11 +534,11 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(G_REGS_DRAIN));
         // ------------------------------ drain / epilogue ------------------------------
         // Every drain warp walks the same units and blocks (also after an
-        // abort, without touching data) so that the named barriers below
-        // always see all of them.
+        // abort, without touching data) so that every accumulator hand-off
+        // sees all sixteen arrivals.
         const int dw = warp - G_DRAIN_WARP0;         // 0 .. 15
         const int quad = warp & 3;                   // TMEM lanes 32*quad ..
-        const int cq = dw >> 2;                      // columns 32*cq ..
+        const int cq = dw >> 2;                      // columns 32*cq .. and 128 + 32*cq ..
         const int row = 32 * quad + lane;            // position row of the tile
         int bc = 0;
         int ntr = 0;
@@ -527,24 +556,23 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
             } else {
                 dsc = g.dh + (size_t)pos * (F / 32);
             }
-            float2 acc[16];
+            // acc[0..15]: columns 32cq .. +31, acc[16..31]: columns 128 + 32cq .. +31
+            float2 acc[32];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) acc[c] = make_float2(0.0f, 0.0f);
-            // block scales in groups of 4 (nb % 4 == 0), loaded two groups
-            // ahead so that the L2 round trip hides behind 4-8 blocks of work
+            for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.0f, 0.0f);
+            // block scales in groups of 4 (nb % 4 == 0), the next group loaded
+            // while this one is folded
             const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             const float4 *dsc4 = reinterpret_cast<const float4 *>(dsc);
-            float4 d0 = valid ? __ldg(dsc4) : zero4;
-            float4 d1 = (valid && nb > 4) ? __ldg(dsc4 + 1) : zero4;
+            float4 dnext = valid ? __ldg(dsc4) : zero4;
             for (int b4 = 0; b4 < nb; b4 += 4) {
-                const float4 dcur = d0;
-                d0 = d1;
-                if (valid && b4 + 8 < nb) d1 = __ldg(dsc4 + (b4 >> 2) + 2);
+                const float4 dcur = dnext;
+                if (valid && b4 + 4 < nb) dnext = __ldg(dsc4 + (b4 >> 2) + 1);
 #pragma unroll
                 for (int bi = 0; bi < 4; ++bi, ++bc) {
                     const float db = bi == 0 ? dcur.x : bi == 1 ? dcur.y : bi == 2 ? dcur.z : dcur.w;
-                    const int a = bc % G_NACC;
-                    const uint32_t par = (uint32_t)((bc / G_NACC) & 1);
+                    const int a = bc & 1;
+                    const uint32_t par = (uint32_t)((bc >> 1) & 1);
                     const bool ok = !*abort && __all_sync(FULL, g_wait(&S.tfull[a], par, abort));
                     const bool trd = tr && dw == 0 && lane == 0 && bc >= 2 * tr0 && bc < 2 * (tr0 + TRACE_NS);
                     if (trd) gtrace(g, 3, ntr, 16, bc);
@@ -554,11 +582,16 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                             const uint32_t base =
                                 tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(a * GN + 32 * cq);
                             const float2 dd = make_float2(db, db);
-                            float v[32];
-                            tmem_ld32(base, v);
 #pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                acc[c] = __ffma2_rn(dd, make_float2(v[2 * c], v[2 * c + 1]), acc[c]);
+                            for (int hq = 0; hq < 4; ++hq) {
+                                // 16 columns: half hq/2 (+128 columns), quarter hq%2
+                                float v[16];
+                                tmem_ld16(base + (uint32_t)(128 * (hq >> 1) + 16 * (hq & 1)), v);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    acc[8 * hq + c] =
+                                        __ffma2_rn(dd, make_float2(v[2 * c], v[2 * c + 1]), acc[8 * hq + c]);
+                            }
                         }
                         tc_fence_before();
                     } else if (lane == 0) {
@@ -574,28 +607,18 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
             // ---- epilogue ----
             const float *ers = (e == g.E) ? g.shared_rs : g.expert_rs + (size_t)e * (2 * F + H);
             if (GATEUP) {
-                // columns 0..63: gate rows 64j.., columns 64..127: the matching up rows
-                if (cq >= 2 && live && active) {
-                    const int c0 = 32 * (cq - 2);
-                    const float *su = ers + F + 64 * j + c0;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        xch[row * XCH_LD + c0 + 2 * c] = __fmul_rn(su[2 * c], acc[c].x);
-                        xch[row * XCH_LD + c0 + 2 * c + 1] = __fmul_rn(su[2 * c + 1], acc[c].y);
-                    }
-                }
-                named_barrier(BAR_DRAIN, 32 * G_DRAIN_WARPS);
-                if (cq < 2 && live && valid) {
-                    // h for rows 64j + 32cq .. +31 of this token: one Q8_0 block
-                    const int c0 = 32 * cq;
-                    const float *sg = ers + 64 * j + c0;
+                if (live && valid) {
+                    // hidden units 128j + 32cq .. +31 of this token: one Q8_0 block of h
+                    const int col0 = (GN / 2) * j + 32 * cq;
+                    const float *sg = ers + col0, *su = ers + F + col0;
                     float h[32];
                     float amax = 0.0f;
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const float gv = (c & 1) ? acc[c >> 1].y : acc[c >> 1].x;
+                        const float uv = (c & 1) ? acc[16 + (c >> 1)].y : acc[16 + (c >> 1)].x;
                         const float gg = __fmul_rn(sg[c], gv);
-                        const float uu = xch[row * XCH_LD + c0 + c];
+                        const float uu = __fmul_rn(su[c], uv);
                         h[c] = __fmul_rn(__fmul_rn(gg, own_sigmoid(gg)), uu);
                         amax = fmaxf(amax, fabsf(h[c]));
                     }
@@ -613,7 +636,6 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                         }
                         qw[w4] = word;
                     }
-                    const int col0 = 64 * j + c0;
                     uint4 *dst = reinterpret_cast<uint4 *>(g.qh + (size_t)pos * F + col0);
                     dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
                     dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
@@ -627,19 +649,23 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                         for (int c = 0; c < 32; ++c) g.h_dbg[(size_t)pos * F + col0 + c] = h[c];
                     }
                 }
-                named_barrier(BAR_DRAIN, 32 * G_DRAIN_WARPS);   // xch is reused by the next unit
             } else if (live && valid) {
-                const int col0 = GN * j + 32 * cq;
-                float4 *yr = reinterpret_cast<float4 *>(g.y + (size_t)pos * H + col0);
-                const float *sd = ers + 2 * F + col0;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float4 o;
-                    o.x = __fmul_rn(sd[4 * c], acc[2 * c].x);
-                    o.y = __fmul_rn(sd[4 * c + 1], acc[2 * c].y);
-                    o.z = __fmul_rn(sd[4 * c + 2], acc[2 * c + 1].x);
-                    o.w = __fmul_rn(sd[4 * c + 3], acc[2 * c + 1].y);
-                    yr[c] = o;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int col0 = GN * j + 128 * hh + 32 * cq;
+                    if (GN * j + 128 * hh < H) {          // H % 128 == 0: the half is whole or absent
+                        float4 *yr = reinterpret_cast<float4 *>(g.y + (size_t)pos * H + col0);
+                        const float *sd = ers + 2 * F + col0;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            float4 o;
+                            o.x = __fmul_rn(sd[4 * c], acc[16 * hh + 2 * c].x);
+                            o.y = __fmul_rn(sd[4 * c + 1], acc[16 * hh + 2 * c].y);
+                            o.z = __fmul_rn(sd[4 * c + 2], acc[16 * hh + 2 * c + 1].x);
+                            o.w = __fmul_rn(sd[4 * c + 3], acc[16 * hh + 2 * c + 1].y);
+                            yr[c] = o;
+                        }
+                    }
                 }
             }
         }
