@@ -114,6 +114,14 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
+            # nvidia-smi's start-up (driver/NVML initialisation) can hold up
+            # CUDA calls of this process for seconds: let it finish, i.e. wait
+            # for its first sample, before the timed region begins
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < 15.0 and self.proc.poll() is None:
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.05)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
