@@ -416,6 +416,35 @@ int launch_dispatch(const int32_t *idx, int T, int k, int E, int32_t *counts, in
     return 0;
 }
 
+// Order-preserving 64-bit image of a (selection key, expert) pair: a larger
+// key first, then the lower expert index (the selection order of the
+// sigmoid router); 0 lies below the image of every finite key.  Keys are
+// sigma + bias, finite; adding +0 maps -0 to +0 so that equal keys have
+// equal images.
+__device__ __forceinline__ unsigned long long route_image(float key, int e)
+{
+    const uint32_t u = __float_as_uint(__fadd_rn(key, 0.0f));
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+}
+
+// Bitonic sort of one value per lane across the warp, largest in lane 0.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long c, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(FULL, c, stride);
+            // the lower lane of a pair keeps the larger value in blocks that
+            // end up descending (all of them at the last size)
+            const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+            c = keep_max ? (c > o ? c : o) : (c < o ? c : o);
+        }
+    }
+    return c;
+}
+
 // ---------------------------------------------------------------------------
 // Small batches (T <= ROUTE_SMALL_MAX_T) route in a single launch of E blocks:
 // every block quantises a share of x and computes the logits of its expert
@@ -423,7 +452,7 @@ int launch_dispatch(const int32_t *idx, int T, int k, int E, int32_t *counts, in
 // finish (a completion counter) runs top-k, the stable dispatch of the
 // T*k <= 128 pairs, the tile list, and zeroes the expert kernel's counters.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
+__global__ void __launch_bounds__(256, 3) k_route_small(const RouteArgs ra)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = ra.T, H = ra.H, E = ra.E, k = ra.k;
@@ -534,6 +563,94 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     __shared__ int s_cnt[MAX_E], s_base[MAX_E], s_tile0[MAX_E], s_off[MAX_E];
     __shared__ int s_ntiles;
     __shared__ float s_key[ROUTE_SMALL_MAX_T][MAX_E], s_sg[ROUTE_SMALL_MAX_T][MAX_E];
+    if (T == 1) {
+        // ---- one token: the k best of E <= 256 keys, then dispatch of k
+        //      distinct experts, in three barrier-separated phases ----
+        __shared__ unsigned long long s_cand[8 * MAX_K];
+        // (a) each warp sorts the images of its 32 experts and offers its k best
+        unsigned long long c = 0;
+        if (tid < E) {
+            s_sg[0][tid] = __ldcg(ra.sig + tid);
+            c = route_image(__ldcg(ra.key + tid), tid);
+        }
+        c = warp_sort_desc(c, lane);
+        if (lane < k) s_cand[warp * k + lane] = c;
+        __syncthreads();
+        stamp(7);
+        // (b) the rank of each candidate among the 8k (images are distinct
+        //     for valid experts; the k best are valid since E >= k)
+        const int nc = 8 * k;
+        if (tid < nc) {
+            const unsigned long long ci = s_cand[tid];
+            int rank = 0;
+#pragma unroll 8
+            for (int j = 0; j < nc; ++j) rank += (s_cand[j] > ci);
+            if (rank < k) {
+                const int sel = ci ? (int)(0xFFFFFFFFu - (uint32_t)ci) : -1;
+                s_idx[rank] = sel;
+                s_sig[rank] = sel >= 0 ? s_sg[0][sel] : 0.0f;
+            }
+        }
+        __syncthreads();
+        stamp(8);
+        // (c) weights, positions and tiles of the k pairs (warp 0), counts and
+        //     offsets of every expert (all threads).  Position of a pair = the
+        //     number of chosen experts with a lower index; tile 0 is the
+        //     shared expert's, tile 1 + pos the pair's.
+        if (warp == 0) {
+            const bool act = lane < k;
+            const int e_r = act ? s_idx[lane] : 0;
+            const float sg_r = act ? s_sig[lane] : 0.0f;
+            float S = 0.0f;
+            int pos = 0;
+#pragma unroll 1
+            for (int r = 0; r < k; ++r) {
+                S = __fadd_rn(S, __shfl_sync(FULL, sg_r, r));
+                pos += (__shfl_sync(FULL, e_r, r) < e_r);
+            }
+            if (act) {
+                ra.idx[lane] = e_r;
+                ra.wts[lane] = __fmul_rn(__fdiv_rn(sg_r, S), ra.routed_scale);
+                if (e_r >= 0 && e_r < E) {
+                    ra.perm[pos] = lane;
+                    ra.inv[lane] = pos;
+                    ra.pos_token[pos] = 0;
+                    ra.tile_expert[1 + pos] = e_r;
+                    ra.tile_pos0[1 + pos] = pos;
+                    ra.tile_m[1 + pos] = 1;
+                } else {
+                    ra.inv[lane] = -1;
+                    set_status(ra.status, ST_BAD_INDEX);
+                }
+            }
+            if (lane == 0) {
+                ra.pos_token[k] = 0;
+                ra.tile_expert[0] = E;
+                ra.tile_pos0[0] = k;
+                ra.tile_m[0] = 1;
+                *ra.n_tiles = 1 + k;
+                ra.offsets[E] = k;
+            }
+        }
+        for (int e2 = tid; e2 < E; e2 += 256) {
+            int below = 0, hit = 0;
+#pragma unroll 1
+            for (int r = 0; r < k; ++r) {
+                const int er = s_idx[r];
+                below += (er < e2);
+                hit += (er == e2);
+            }
+            ra.counts[e2] = hit;
+            ra.offsets[e2] = below;
+        }
+        __syncthreads();
+        stamp(2);
+        stamp(3);
+        stamp(4);
+        stamp(5);
+        stamp(6);
+        return;
+    }
     // sigma and selection key of every (token, expert), computed by the
     // expert's block
 #pragma unroll 1
@@ -544,28 +661,10 @@ __global__ void __launch_bounds__(256) k_route_small(const RouteArgs ra)
     }
     __syncthreads();
     stamp(7);
-    if (T == 1) {
-        // Top-k by rank: expert e ranks below every expert with a larger key,
-        // and below equal keys of lower index (lowest-index ties); it is
-        // selected, at position rank, iff rank < k.  One expert per thread.
-#pragma unroll 1
-        for (int ee = tid; ee < E; ee += 256) {
-            const float ke = s_key[0][ee];
-            int rank = 0;
-#pragma unroll 4
-            for (int e2 = 0; e2 < E; ++e2) {
-                const float k2 = s_key[0][e2];
-                rank += (k2 > ke) | ((k2 == ke) & (e2 < ee));
-            }
-            if (rank < k) {
-                s_idx[rank] = ee;
-                s_sig[rank] = s_sg[0][ee];
-            }
-        }
-    } else if (warp < T) {
-        // Several tokens: one warp per token (the rank method's cost grows
-        // with T), k rounds of a warp-wide argmax over the experts not yet
-        // taken under the same order: larger key first, then lower index.
+    if (warp < T) {
+        // Several tokens: one warp per token, k rounds of a warp-wide argmax
+        // over the experts not yet taken under the selection order: larger
+        // key first, then lower index.
         // Lane l holds experts l, l+32, ...
         const int t = warp;
         unsigned taken = 0;                       // bit i: expert lane + 32 i taken

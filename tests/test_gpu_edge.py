@@ -52,6 +52,11 @@ SHAPES = [
     ("max_hidden", 16384, 128, 4, 2, 3),
     ("max_ffn", 128, 16384, 4, 2, 3),
     ("many_tokens", 256, 128, 8, 2, 1000),
+    # one token: the single-token routing tail (warp sorts of 64-bit key
+    # images, a rank among the warps' candidates, one dispatch phase)
+    ("t1_odd_E", 256, 128, 5, 3, 1),
+    ("t1_k16", 256, 128, 40, 16, 1),
+    ("t1_E256", 256, 128, 256, 8, 1),
 ]
 
 
@@ -170,4 +175,32 @@ def test_zero_and_one_hot_weight_rows(coli, path):
     got = _run(coli, path, wl, L, x)
     want = oracle.moe_forward(x, np.zeros_like(W), b, w4s[:E], rss[:E], w4s[E], rss[E], H, F, wl.top_k,
                               wl.routed_scale)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+@pytest.mark.parametrize("E,k", [(8, 2), (256, 8), (37, 16)])
+def test_one_token_tied_keys(coli, path, E, k):
+    """One token, a zero router (every sigma = 0.5) and biases drawn from
+    four values: most selection keys tie, and the lowest expert index must
+    win among equal keys, exactly as in the oracle."""
+    import oracle
+    from synth.device import build_device_layer
+    wl = synth.Workload("t1_ties", 256, 128, E, k, 1, 900 + E + k)
+    L = build_device_layer(wl)
+    rng = np.random.default_rng(E * 31 + k)
+    b = rng.choice(np.array([-0.25, 0.0, 0.125, 0.5], np.float32), size=E).astype(np.float32)
+    L["router_w"] = torch.zeros_like(L["router_w"])
+    L["router_b"] = torch.from_numpy(b).cuda()
+    x = synth.activations(wl, 11)
+    got = _run(coli, path, wl, L, x)
+    ref = OracleLayer(wl)
+    ridx, _ = oracle.route(x, np.zeros_like(ref.W), b, k, wl.routed_scale)
+    order = sorted(range(E), key=lambda e: (-b[e], e))[:k]
+    assert list(ridx[0]) == order                       # the oracle follows the rule
+    w4, rs = [None] * E, [None] * E
+    for e in order:
+        w4[e], rs[e] = ref.expert(e)
+    want = oracle.moe_forward(x, np.zeros_like(ref.W), b, w4, rs, ref.shared[0], ref.shared[1],
+                              wl.hidden, wl.ffn, k, wl.routed_scale)
     np.testing.assert_array_equal(got, want)
