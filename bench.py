@@ -49,12 +49,19 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "8e41f205dd5b18a02dc44626503b61077574faf0a6cac9a37f910f533f227c8a",
+        "sha256": "d48a0945b2818300ef476bad9aebe1c450f17a66c19e52982f6700d2d5811637",
         "bytes_per_launch": 173469440,   # 170.74 MB read + 2.73 MB written
         # a launch of the 16-expert profile workload streams 8 routed + 1 shared
         # expert, the same units as one decode forward over 256 experts
         "workloads": ("decode", "profile"),
         "capture": "profiles/k_experts_decode_profile.md",
+    },
+    "k_gemm_gateup": {
+        "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
+        "sha256": "fd9829b56982fd2ae287ce13ead69322196f39d3bc78e6ffee1ea84d5ff648bb",
+        "bytes_per_launch": 5391012352,  # 5295.90 MB read + 95.12 MB written
+        "workloads": ("prefill",),
+        "capture": "profiles/prefill_layer_launches.md",
     },
 }
 
@@ -394,7 +401,8 @@ def run(args):
     if use_gemm:
         achieved = 2.0 * macs_gu / (k_avg_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": achieved / bf16_peak, "traffic": None,
+                    "frac": achieved / bf16_peak, "traffic": kernel_traffic("k_gemm_gateup", wl.name),
+                    "traffic_unit": "DRAM bytes per launch",
                     "kernel": "k_gemm<gate/up> (tcgen05 bf16 on exact int codes, SiLU*up + Q8_0 of h fused), "
                               "timed alone",
                     "algorithmic_flops_per_launch": 2.0 * macs_gu,
