@@ -117,8 +117,11 @@ int coli_moe_layer_forward_residual(const float *x, int n_tok,
 
 /* The same forward with x and out in HOST memory (pinned memory gives
  * asynchronous copies).  Copies x into a library-owned device buffer, runs the
- * forward, copies the result back, and synchronises `stream` before
- * returning, so out_host is valid on return.  Weights are device pointers. */
+ * forward and synchronises `stream` before returning, so out_host is valid on
+ * return.  When out_host is page-locked and mapped into the device's address
+ * space (cudaHostAlloc / cudaMallocHost memory, 16-byte aligned) the final
+ * combine writes the result directly into it; any other host buffer receives
+ * a copy of a library-owned device result.  Weights are device pointers. */
 int coli_moe_layer_forward_hostio(const float *x_host, int n_tok,
                                   const float *router_w, const float *router_bias,
                                   const uint8_t *expert_w4, const float *expert_rowscale,

@@ -101,6 +101,13 @@ def lib():
     return _lib
 
 
+# Pointers travel as plain integers (the argtypes convert them); the current
+# stream is read as a raw handle where this PyTorch exposes it, which keeps
+# the per-call marshalling to a few microseconds.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _ptr(t):
     if t is None:
         return None
@@ -108,18 +115,21 @@ def _ptr(t):
         raise TypeError("expected a torch.Tensor")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _host_ptr(t):
     if t.is_cuda or not t.is_contiguous():
         raise ValueError("expected a contiguous host tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is None:
+        if _raw_stream is not None and _cur_device is not None:
+            return _raw_stream(_cur_device())
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
 
 
 def _check(code: int, what: str):

@@ -687,11 +687,22 @@ int coli_moe_layer_forward_hostio(const float *x_host, int n_tok, const float *r
     if (st != COLI_OK || n_tok == 0) return st;
     cudaStream_t s = (cudaStream_t)stream;
     const size_t bytes = (size_t)n_tok * g.s.hidden * sizeof(float);
+    // Page-locked, device-mapped output (pinned memory on this platform):
+    // the combine writes the result straight into it over the host link,
+    // which saves a copy-out launch.  Any other host memory gets the
+    // device-side result copied out.
+    float *out_mapped = nullptr;
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer && aligned16(pa.devicePointer))
+        out_mapped = static_cast<float *>(pa.devicePointer);
+    else
+        (void)cudaGetLastError();   // an unregistered pointer leaves an error to clear
     CUDA_OK(cudaMemcpyAsync(g.ws.x_io, x_host, bytes, cudaMemcpyHostToDevice, s));
     st = forward_impl(g.ws.x_io, n_tok, router_w, router_bias, expert_w4, expert_rowscale,
-                      shared_w4, shared_rowscale, g.ws.out_io, s);
+                      shared_w4, shared_rowscale, out_mapped ? out_mapped : g.ws.out_io, s);
     if (st != COLI_OK) return st;
-    CUDA_OK(cudaMemcpyAsync(out_host, g.ws.out_io, bytes, cudaMemcpyDeviceToHost, s));
+    if (!out_mapped) CUDA_OK(cudaMemcpyAsync(out_host, g.ws.out_io, bytes, cudaMemcpyDeviceToHost, s));
     CUDA_OK(cudaStreamSynchronize(s));
     return COLI_OK;
 }

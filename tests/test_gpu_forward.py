@@ -99,6 +99,33 @@ def test_tiny_hostio_matches_device_call(coli, tiny):
     np.testing.assert_array_equal(oh.numpy(), ref.forward(x))
 
 
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_hostio_pinned_and_pageable_outputs(coli, tiny, path):
+    """Pinned (device-mapped) output buffers receive the combine's stores
+    directly; pageable ones a copy of the device result.  Both must match the
+    oracle bit for bit, over repeated calls with fresh inputs."""
+    wl, L, ref = tiny
+    _configure(coli, wl, 8)
+    coli.set_path({"gemv": coli.PATH_GEMV, "gemm": coli.PATH_GEMM}[path])
+    try:
+        for step in range(3):
+            x = synth.activations(wl, 40 + step, n_tok=5)
+            want = ref.forward(x)
+            xh = torch.from_numpy(x).pin_memory()
+            for oh in (torch.full_like(xh, float("nan")).pin_memory(), torch.full((5, wl.hidden), float("nan"))):
+                coli.layer_forward_hostio(xh, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                                          L["shared_w4"], L["shared_rs"], oh)
+                np.testing.assert_array_equal(oh.numpy(), want)
+            # a pageable input as well
+            oh = torch.empty((5, wl.hidden)).pin_memory()
+            coli.layer_forward_hostio(torch.from_numpy(x.copy()), L["router_w"], L["router_b"], L["expert_w4"],
+                                      L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
+            np.testing.assert_array_equal(oh.numpy(), want)
+    finally:
+        coli.set_path(coli.PATH_AUTO)
+    assert coli.get_device_status() == coli.OK
+
+
 # --------------------------------------------------------------------------- #
 # GLM-5.2-shaped layer (256 experts + shared, all resident)                    #
 # --------------------------------------------------------------------------- #
