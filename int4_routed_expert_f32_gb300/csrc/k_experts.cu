@@ -10,7 +10,8 @@
 //
 // Structure: several small blocks per SM, each 2 consumer warps + 1 producer
 // warp, all blocks resident (the grid is sized by the occupancy calculator).
-//   * Work units, claimed in increasing order from a global counter: first
+//   * Work units, claimed in increasing order from a global counter (the
+//     next one with the current unit's last copy): first
 //     every gate/up unit (a tile of <= GEMV_MT tokens of one expert x 32
 //     hidden units = 32 gate rows + 32 up rows), then every down unit (a tile x
 //     64 output rows).
@@ -337,8 +338,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                     decode_unit(u, n_gu, G, CH, &gu, &tile, &j);
                     e = __ldg(a.tile_expert + tile);
                 }
-                // claim the next unit early: its round trip overlaps this one's copies
-                const long u_next = done ? total : atomicAdd(a.work_counter, 1);
+                long u_next = total;
                 const int nst = done ? 1 : (gu ? nst_gu : nst_dn);
                 const int nsub = gu ? nsub_gu : nsub_dn;
                 const bool shared = (e == a.E);
@@ -380,6 +380,12 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                         phase ^= 1;
                         first_round = false;
                     }
+                    // claim the next unit with this unit's last copy: the
+                    // atomic's round trip overlaps the stages still in the
+                    // ring, and units are handed out in the order in which
+                    // blocks run out of work (claimed at the start of a unit,
+                    // a block's second unit was fixed before its first ran)
+                    if (s == nst - 1) u_next = atomicAdd(a.work_counter, 1);
                 }
                 if (stop) break;
                 u = u_next;

@@ -57,6 +57,11 @@ SHAPES = [
     ("t1_odd_E", 256, 128, 5, 3, 1),
     ("t1_k16", 256, 128, 40, 16, 1),
     ("t1_E256", 256, 128, 256, 8, 1),
+    # one token with more gate/up units (17 tiles x 32) than expert-kernel
+    # blocks, so that units are claimed in a second wave (even and odd stage
+    # counts per row)
+    ("t1_split_even", 1024, 1024, 32, 16, 1),
+    ("t1_split_odd", 768, 1024, 32, 16, 1),
 ]
 
 
