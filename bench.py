@@ -49,7 +49,7 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "d3c6392e6510e0287925ed18b9a97ef2a2909a587a24ffffc859cd55cd10e044",
+        "sha256": "34e58d7acfcc90cc8fea7460554eaafe86a2f24fe5430415e758500a3fefcfc0",
         "bytes_per_launch": 173673216,   # 170.81 MB read + 2.86 MB written
         # a launch of the 16-expert profile workload streams 8 routed + 1 shared
         # expert, the same units as one decode forward over 256 experts

@@ -128,17 +128,31 @@ size_t experts_smem_bytes_mt(int H, int F, int mt, int nstage)
 }
 
 // Ring depth.  More blocks per SM help more than deeper rings: each block's
-// consumers drain a bounded rate.  COLI_MOE_RING_STAGES (2..16) overrides the
-// default for tuning.
-static int ring_stages(int, int, int)
+// consumers drain a bounded rate.  Three stages, unless three blocks of that
+// size do not fit in one SM's shared memory (several tokens' activations
+// make the block larger); then two, which keeps three blocks per SM (a
+// 4-token forward ran 26% faster that way).  COLI_MOE_RING_STAGES (2..16)
+// overrides the choice for tuning.
+static int ring_stages(int H, int F, int mt)
 {
-    static int n = 0;
-    if (n == 0) {
+    static int env_n = -1;
+    if (env_n < 0) {
         const char *env = getenv("COLI_MOE_RING_STAGES");
         const int v = env ? atoi(env) : 0;
-        n = (v >= 2 && v <= NSTAGE_MAX) ? v : 3;
+        env_n = (v >= 2 && v <= NSTAGE_MAX) ? v : 0;
     }
-    return n;
+    if (env_n > 0) return env_n;
+    static int smem_per_sm = 0;
+    if (smem_per_sm == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess && v > 0)
+            smem_per_sm = v;
+        else
+            smem_per_sm = 228 * 1024;
+    }
+    // 1 KB of each block's shared memory is reserved by the system
+    return 3 * (experts_smem_bytes_mt(H, F, mt, 3) + 1024) <= (size_t)smem_per_sm ? 3 : 2;
 }
 
 size_t experts_smem_bytes(int H, int F) { return experts_smem_bytes_mt(H, F, GEMV_MT, ring_stages(H, F, GEMV_MT)); }
