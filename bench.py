@@ -58,7 +58,7 @@ TRAFFIC = {
     },
     "k_gemm_gateup": {
         "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "fd9829b56982fd2ae287ce13ead69322196f39d3bc78e6ffee1ea84d5ff648bb",
+        "sha256": "739296d8a09c24eb73abe39744c2d2ba6e7f17ab7e487657b3fa15875fc6fb13",
         "bytes_per_launch": 5391012352,  # 5295.90 MB read + 95.12 MB written
         "workloads": ("prefill",),
         "capture": "profiles/prefill_layer_launches.md",

@@ -256,27 +256,50 @@ __global__ void __launch_bounds__(256) k_gather_x(const int8_t *__restrict__ qx,
 }
 
 // GEMM work items: each expert's dispatch positions in tiles of GM, the shared
-// expert (rows P .. P+T-1) first, then routed experts in ascending id.
-__global__ void k_gemm_items(const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int E,
-                             int T, int P, int32_t *item_expert, int32_t *item_pos0, int32_t *item_m,
-                             int32_t *n_items)
+// expert (rows P .. P+T-1) first, then routed experts in ascending id.  One
+// block of 256 threads (E <= 256): thread e counts expert e's tiles, a block
+// scan gives its first item, and every thread writes its own items.
+__global__ void __launch_bounds__(256) k_gemm_items(const int32_t *__restrict__ counts,
+                                                    const int32_t *__restrict__ offsets, int E, int T, int P,
+                                                    int32_t *item_expert, int32_t *item_pos0, int32_t *item_m,
+                                                    int32_t *n_items)
 {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    int n = 0;
-    for (int p = 0; p < T; p += GM) {
-        item_expert[n] = E;
-        item_pos0[n] = P + p;
-        item_m[n] = min(GM, T - p);
-        ++n;
+    __shared__ int s_warp[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int shared_items = (T + GM - 1) / GM;
+    for (int q = tid; q < shared_items; q += blockDim.x) {
+        item_expert[q] = E;
+        item_pos0[q] = P + q * GM;
+        item_m[q] = min(GM, T - q * GM);
     }
-    for (int e = 0; e < E; ++e)
-        for (int p = 0; p < counts[e]; p += GM) {
-            item_expert[n] = e;
-            item_pos0[n] = offsets[e] + p;
-            item_m[n] = min(GM, counts[e] - p);
-            ++n;
+    const int cnt = tid < E ? counts[tid] : 0;
+    const int ni = (cnt + GM - 1) / GM;
+    // inclusive scan of the tile counts: within the warp, then over the warps
+    int inc = ni;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULL, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int v = s_warp[w];
+        before += (w < warp) ? v : 0;
+        total += v;
+    }
+    const int first = shared_items + before + inc - ni;
+    if (tid < E) {
+        const int off = offsets[tid];
+        for (int q = 0; q < ni; ++q) {
+            item_expert[first + q] = tid;
+            item_pos0[first + q] = off + q * GM;
+            item_m[first + q] = min(GM, cnt - q * GM);
         }
-    *n_items = n;
+    }
+    if (tid == 0) *n_items = shared_items + total;
 }
 
 // Combine: out[t] = y[shared row of t], then + w_r * y[pair (t, r)] for the
@@ -694,7 +717,7 @@ int launch_gather_x(const int8_t *qx, const int32_t *pos_token, const int32_t *o
 int launch_gemm_items(const int32_t *counts, const int32_t *offsets, int E, int T, int P, int32_t *item_expert,
                       int32_t *item_pos0, int32_t *item_m, int32_t *n_items, cudaStream_t st)
 {
-    k_gemm_items<<<1, 32, 0, st>>>(counts, offsets, E, T, P, item_expert, item_pos0, item_m, n_items);
+    k_gemm_items<<<1, 256, 0, st>>>(counts, offsets, E, T, P, item_expert, item_pos0, item_m, n_items);
     count_launch();
     return 0;
 }
