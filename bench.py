@@ -49,7 +49,7 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "34e58d7acfcc90cc8fea7460554eaafe86a2f24fe5430415e758500a3fefcfc0",
+        "sha256": "3714d7666e6b66a88fa19d75bce10a9a1db24152765af8f15ef9da896aee0ac5",
         "bytes_per_launch": 173673216,   # 170.81 MB read + 2.86 MB written
         # a launch of the 16-expert profile workload streams 8 routed + 1 shared
         # expert, the same units as one decode forward over 256 experts
@@ -58,7 +58,7 @@ TRAFFIC = {
     },
     "k_gemm_gateup": {
         "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "739296d8a09c24eb73abe39744c2d2ba6e7f17ab7e487657b3fa15875fc6fb13",
+        "sha256": "ce67970fb2ce0f75bd1e8697edca09c50564dc99bdc47febf96ccb0b81fe1ec3",
         "bytes_per_launch": 5391012352,  # 5295.90 MB read + 95.12 MB written
         "workloads": ("prefill",),
         "capture": "profiles/prefill_layer_launches.md",

@@ -136,16 +136,6 @@ __device__ __forceinline__ void split_block(uint4 a, uint4 b, uint4 *lo, uint4 *
 constexpr int MAGIC_I = 0x4B400000;
 constexpr float MAGIC_F = 12582912.0f;
 
-// Streaming 16-byte load that bypasses L1 (weights are read once).
-__device__ __forceinline__ uint4 ld_stream(const void *p)
-{
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
-
 __device__ __forceinline__ void set_status(int *status, int bit)
 {
     if (status) atomicOr(status, bit);

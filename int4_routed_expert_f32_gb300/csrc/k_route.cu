@@ -171,51 +171,6 @@ __device__ __noinline__ float warp_topk(const float *logits_row, int E, int k,
     return S;
 }
 
-// Top-k selection for one token by one warp over keys already in shared
-// memory (key = sigma + bias; taken experts are overwritten with -inf).
-// Lane 0 writes the experts in rank order to idx_out and their sigma to
-// sig_out; returns S = sum of the chosen sigma in rank order.  Every loop is
-// rolled: this runs once per token, on code no other block has fetched, so a
-// small body beats unrolling.
-__device__ __noinline__ float warp_select(float *key, const float *sig, int E, int k, int *idx_out,
-                                          float *sig_out)
-{
-    const int lane = threadIdx.x & 31;
-    float S = 0.0f;
-#pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-        float bv = -__int_as_float(0x7f800000);
-        int be = INT_MAX;
-#pragma unroll 1
-        for (int e = lane; e < E; e += 32) {
-            const float v = key[e];
-            if (v != -__int_as_float(0x7f800000) && (be == INT_MAX || v > bv)) {
-                bv = v;
-                be = e;
-            }
-        }
-#pragma unroll 1
-        for (int o = 16; o >= 1; o >>= 1) {
-            const float ov = __shfl_xor_sync(FULL, bv, o);
-            const int oe = __shfl_xor_sync(FULL, be, o);
-            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        const float bs = (be == INT_MAX) ? 0.0f : sig[be];
-        __syncwarp();
-        if (lane == 0) {
-            idx_out[r] = (be == INT_MAX) ? -1 : be;
-            sig_out[r] = bs;
-            if (be != INT_MAX) key[be] = -__int_as_float(0x7f800000);
-        }
-        __syncwarp();
-        S = __fadd_rn(S, bs);
-    }
-    return S;
-}
-
 __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int T, int E, int k,
                                               const float *__restrict__ bias, float scale,
                                               int32_t *__restrict__ idx, float *__restrict__ w)

@@ -52,16 +52,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase: returns false if it gave up.
-constexpr uint32_t WAIT_LIMIT = 1u << 24;   // each try_wait suspends for a while
-
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
-{
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
 // L2 policy for data read once (streamed weights).
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
@@ -109,13 +99,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p)
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ int atomic_add_release_gpu(int *p, int v)
-{
-    int old;
-    asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
 }
 
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v)
