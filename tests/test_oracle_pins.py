@@ -455,3 +455,44 @@ def test_rmsnorm_matches_double_precision(orc):
 def test_rmsnorm_zero_row_is_zero(orc):
     x = np.zeros((2, 256), np.float32)
     np.testing.assert_array_equal(orc.rmsnorm(x), x)
+
+
+# --------------------------------------------------------------------------- #
+# Thread count: OpenMP runs over independent outputs only                     #
+# --------------------------------------------------------------------------- #
+def test_results_do_not_depend_on_thread_count(orc):
+    """Every parallel loop of the oracle writes disjoint outputs, each with its
+    own sequential arithmetic, so one thread and several give identical bits:
+    routing, the intermediates and the layer output of a multi-token batch
+    (including tokens that share experts), and the router logits."""
+    from helpers import OracleLayer
+    wl = synth.Workload("threads", 512, 256, 16, 4, 9, 41)
+    ref = OracleLayer(wl)
+    x = synth.activations(wl, 3)
+    idx, _ = orc.route(x, ref.W, ref.b, wl.top_k, wl.routed_scale)
+    w4, rs = [None] * wl.n_experts, [None] * wl.n_experts
+    for e in set(int(v) for v in idx.ravel()):
+        w4[e], rs[e] = ref.expert(e)
+    runs = []
+    try:
+        for n in (1, 4):
+            orc.set_threads(n)
+            r = orc.route(x, ref.W, ref.b, wl.top_k, wl.routed_scale, want_logits=True)
+            f = orc.moe_forward(x, ref.W, ref.b, w4, rs, ref.shared[0], ref.shared[1], wl.hidden, wl.ffn,
+                                wl.top_k, wl.routed_scale, intermediates=True)
+            runs.append((r, f))
+    finally:
+        orc.set_threads(0)
+
+    def flat(v):
+        if isinstance(v, dict):
+            return [a for key in sorted(v) for a in flat(v[key])]
+        if isinstance(v, (tuple, list)):
+            return [a for item in v for a in flat(item)]
+        return [np.asarray(v)]
+
+    a, b = flat(runs[0]), flat(runs[1])
+    assert len(a) == len(b) and len(a) > 4
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u.view(np.uint8) if u.dtype.kind == "f" else u,
+                                      v.view(np.uint8) if v.dtype.kind == "f" else v)
