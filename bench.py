@@ -121,7 +121,7 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
-            # nvidia-smi's start-up (driver/NVML initialisation) can hold up
+            # nvidia-smi's start-up (NVML initialisation) can hold up
             # CUDA calls of this process for seconds: let it finish, i.e. wait
             # for its first sample, before the timed region begins
             t0 = time.perf_counter()
