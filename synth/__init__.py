@@ -86,8 +86,10 @@ class Workload:
 # the quietest a handful ("from ~0 to several hundred").
 ZIPF_BETA = 0.16
 # Correlation of a sweep layer's router rows with the previous layer's.
-# Calibrated with the oracle's router: on the same tokens, 69.6% of a layer's
-# top-8 choices are also in the previous layer's ("70% correlated").
+# Calibrated with the oracle's router: on the same tokens, about 67-70% of a
+# layer's top-8 choices are also in the previous layer's ("70% correlated";
+# 69.6% in the calibration run, 0.67 on the 128 normalised tokens of the
+# input-recipe test).
 SWEEP_LAYER_CORR = 0.97
 
 WORKLOADS = {

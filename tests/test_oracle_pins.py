@@ -496,3 +496,4 @@ def test_results_do_not_depend_on_thread_count(orc):
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u.view(np.uint8) if u.dtype.kind == "f" else u,
                                       v.view(np.uint8) if v.dtype.kind == "f" else v)
+
