@@ -1,0 +1,42 @@
+"""bench.py's command line and JSON line, checked on CPU through the
+reference arm (the oracle timed on the host cores), which needs no GPU."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args, timeout=600):
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          capture_output=True, text=True, timeout=timeout, env=env)
+
+
+def test_reference_line_carries_every_contract_key():
+    r = _run("--impl", "reference", "--steps", "2", "--warmup", "3", "--workload", "tiny")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == "MoE layer tok/s" and d["unit"] == "tok/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["vs_baseline"] is None
+    assert isinstance(d["dtype"], str) and d["data"] == "synthetic"
+    assert isinstance(d["config"], dict) and "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert isinstance(cb["sample"], str) and cb["unit"] == "tok/s"
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == "tok/s"
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_fewer_than_three_warmup_steps_are_rejected():
+    r = _run("--impl", "reference", "--steps", "1", "--warmup", "2", "--workload", "tiny", timeout=120)
+    assert r.returncode != 0
+    assert "warmup" in r.stderr
