@@ -2,6 +2,7 @@
 library's event log (``coli_moe_trace_enable`` / ``coli_moe_trace_read``).
 
     python -m int4_routed_expert_f32_gb300.trace_report [workload] [reps]
+    python -m int4_routed_expert_f32_gb300.trace_report --gemm [workload]
 
 Builds the workload's layer on the current CUDA device, runs a few untraced
 forwards (L2 flushed before each, as in the benchmark), then traces ``reps``
@@ -14,6 +15,15 @@ forwards and prints, relative to the first expert-kernel consumer start:
 * the consumers' time waiting for weight stages and the producers' time
   waiting for free ring slots;
 * when the 64-row output chunks were combined.
+
+With ``--gemm`` (the grouped tensor-core path, default workload
+prefill_profile) it prints, for a few blocks of the gate/up GEMM, the median
+stage interval, the TMA latency (stage issued to stage landed), the weight
+conversion time per stage, the drain time per accumulator block and the
+interval between drained blocks, from the GEMM's stage log (per block four
+sub-logs: producer code 11 stage issued; first converter warp 14 landed,
+15 converted; first drain warp 16 accumulator ready, 17 folded; entry 0 of a
+sub-log counts its events; a steady-state window of stages is logged).
 
 Event codes written by the expert kernel (per block, slot 0 counts events):
 1 consumer start, 2 unit start (first stage arrived), 3 activations staged,
@@ -133,5 +143,89 @@ def _print_rep(rep, fwd_ms, ev, nb, ne, G, CH):
     print(f"  tiles {n_tiles}")
 
 
+def gemm_sublog(ev_block: np.ndarray, role: int, quarter: int):
+    """Events (time_ns, code, value) of one role's sub-log of a GEMM block."""
+    n = int(ev_block[role * quarter, 0])
+    out = []
+    for i in range(1, min(n, quarter - 1) + 1):
+        w, v = int(ev_block[role * quarter + i, 0]), int(np.int64(ev_block[role * quarter + i, 1]))
+        out.append((w >> 8, w & 255, v))
+    return out
+
+
+def gemm_stage_stats(ev_block: np.ndarray) -> dict:
+    """Medians (us) of one gate/up GEMM block's stage log; NaN where a role
+    logged nothing."""
+    q = ev_block.shape[0] // 4
+    prod, conv, drain = gemm_sublog(ev_block, 0, q), gemm_sublog(ev_block, 2, q), gemm_sublog(ev_block, 3, q)
+    issue = {v: t / 1000.0 for t, c, v in prod if c == 11}
+    landed = {v: t / 1000.0 for t, c, v in conv if c == 14}
+    converted = {v: t / 1000.0 for t, c, v in conv if c == 15}
+    ready = {v: t / 1000.0 for t, c, v in drain if c == 16}
+    folded = {v: t / 1000.0 for t, c, v in drain if c == 17}
+    nan = float("nan")
+    st = sorted(issue)
+    iss = np.array([issue[k] for k in st])
+    land = np.array([landed.get(k, np.nan) for k in st])
+    cv = np.array([converted.get(k, np.nan) for k in st])
+    bl = sorted(folded)
+    dd = np.array([folded[b] - ready[b] for b in bl if b in ready])
+    fo = np.array([folded[b] for b in bl])
+    return {
+        "stages": len(st),
+        "stage_interval_us": float(np.median(np.diff(iss))) if len(iss) > 1 else nan,
+        "issue_to_landed_us": float(np.nanmedian(land - iss)) if len(st) else nan,
+        "convert_us": float(np.nanmedian(cv - land)) if len(st) else nan,
+        "drain_per_block_us": float(np.median(dd)) if len(dd) else nan,
+        "drained_interval_us": float(np.median(np.diff(fo))) if len(fo) > 1 else nan,
+    }
+
+
+def report_gemm(name: str = "prefill_profile", blocks=(0, 1, 77), events_per_block: int = 2048) -> None:
+    import synth
+    from synth.device import build_device_layer
+
+    wl = synth.WORKLOADS[name]
+    T = wl.n_tok
+    coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
+    coli.set_path(coli.PATH_GEMM)
+    try:
+        L = build_device_layer(wl)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        x = torch.from_numpy(synth.activations(wl, 5000)).cuda()
+        out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
+
+        def fwd():
+            coli.layer_forward(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                               L["shared_w4"], L["shared_rs"], out=out)
+
+        for _ in range(3):
+            flush.zero_()
+            fwd()
+        torch.cuda.synchronize()
+        coli.trace_enable(events_per_block)
+        try:
+            flush.zero_()
+            torch.cuda.synchronize()
+            fwd()
+            torch.cuda.synchronize()
+            ev, nb, ne = coli.trace_read()
+        finally:
+            coli.trace_enable(0)
+    finally:
+        coli.set_path(coli.PATH_AUTO)
+    for blk in blocks:
+        if blk >= nb:
+            continue
+        st = gemm_stage_stats(ev[blk])
+        print(f"block {blk}: {st['stages']} stages logged; stage interval {st['stage_interval_us']:.3f} us, "
+              f"issue->landed {st['issue_to_landed_us']:.3f}, convert {st['convert_us']:.3f}, "
+              f"drain per block {st['drain_per_block_us']:.3f}, drained-block interval "
+              f"{st['drained_interval_us']:.3f}")
+
+
 if __name__ == "__main__":
-    report(sys.argv[1] if len(sys.argv) > 1 else "decode", int(sys.argv[2]) if len(sys.argv) > 2 else 3)
+    if len(sys.argv) > 1 and sys.argv[1] == "--gemm":
+        report_gemm(sys.argv[2] if len(sys.argv) > 2 else "prefill_profile")
+    else:
+        report(sys.argv[1] if len(sys.argv) > 1 else "decode", int(sys.argv[2]) if len(sys.argv) > 2 else 3)
