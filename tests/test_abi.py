@@ -50,6 +50,15 @@ def test_shape_validation_without_gpu(lib):
         (256, 128, 8, 9, 2.5, 4),     # top_k > n_experts
         (256, 128, 8, 2, 0.0, 4),     # routed_scale must be > 0
         (256, 128, 8, 2, 2.5, 0),     # max_tok >= 1
+        (16512, 128, 8, 2, 2.5, 4),   # hidden above 16384
+        (256, 16512, 8, 2, 2.5, 4),   # ffn above 16384
+        (256, 128, 0, 1, 2.5, 4),     # no experts
+        (256, 128, 32, 17, 2.5, 4),   # top_k above 16
+        (256, 128, 8, 0, 2.5, 4),     # top_k >= 1
+        (256, 128, 8, 2, 2.5, 65537), # max_tok above 65536
+        (256, 128, 8, 2, float("nan"), 4),
+        (256, 128, 8, 2, float("inf"), 4),
+        (256, 128, 8, 2, -2.5, 4),
     ]
     for s in bad:
         with pytest.raises(coli.ColiError) as ei:
