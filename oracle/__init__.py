@@ -47,6 +47,12 @@ def lib():
             f = ctypes.c_float
             L.orc_pack_int4_rows.argtypes = [P, i, i, P, P]
             L.orc_unpack_int4_rows.argtypes = [P, i, i, P]
+            L.orc_pack_int8_rows.argtypes = [P, i, i, P, P]
+            L.orc_block_dots_w8.argtypes = [P, i, i, P, P]
+            L.orc_expert_ffn_w.argtypes = [P, i, P, i, i, P, P, P, P, P, P, P, P]
+            L.orc_moe_forward_w.argtypes = [P, i, i, i, i, i, f, P, P, i, P, P, P, P, P,
+                                            P, P, P, P, P, P]
+            L.orc_moe_forward_w.restype = i
             L.orc_q8_0.argtypes = [P, i, P, P]
             L.orc_lrintf.argtypes = [f]
             L.orc_lrintf.restype = ctypes.c_long
@@ -106,6 +112,16 @@ def unpack_int4_rows(packed):
     q = np.empty((R, 2 * K2), np.int8)
     lib().orc_unpack_int4_rows(_p(packed), R, 2 * K2, _p(q))
     return q
+
+
+def pack_int8_rows(w):
+    """The int8 container: F32 rows [R][K] -> (int8 codes [R][K], scale float32 [R])."""
+    w = _c(w, np.float32)
+    R, K = w.shape
+    q = np.empty((R, K), np.int8)
+    scale = np.empty(R, np.float32)
+    lib().orc_pack_int8_rows(_p(w), R, K, _p(q), _p(scale))
+    return q, scale
 
 
 def q8_0(x):
@@ -190,6 +206,16 @@ def block_dots(w4, q):
     return I
 
 
+def block_dots_w8(w8, q):
+    """Per-block int32 dot products I [rows][K/32] of int8 rows with int8 q [K]."""
+    w8 = _c(w8, np.int8)
+    q = _c(q, np.int8)
+    R, K = w8.shape
+    I = np.empty((R, K // 32), np.int32)
+    lib().orc_block_dots_w8(_p(w8), R, K, _p(q), _p(I))
+    return I
+
+
 def rows_dot(w4, s, q, d):
     w4 = _c(w4, np.uint8)
     s = _c(s, np.float32)
@@ -201,9 +227,11 @@ def rows_dot(w4, s, q, d):
     return out
 
 
-def expert_ffn(ew4, ers, H, F, qx, dx):
-    """O5 for one expert and one token: returns dict(qh, dh, y, g, u, h)."""
-    ew4 = _c(ew4, np.uint8).reshape(-1)
+def expert_ffn(ew4, ers, H, F, qx, dx, wbits=4):
+    """O5 for one expert and one token: returns dict(qh, dh, y, g, u, h).
+    ``wbits`` is the weight container: 4 (packed int4 bytes, 3*F*H/2) or 8
+    (int8 codes as bytes, 3*F*H)."""
+    ew4 = np.ascontiguousarray(ew4).view(np.uint8).reshape(-1)
     ers = _c(ers, np.float32).reshape(-1)
     qx = _c(qx, np.int8)
     dx = _c(dx, np.float32)
@@ -213,18 +241,19 @@ def expert_ffn(ew4, ers, H, F, qx, dx):
     g = np.empty(F, np.float32)
     u = np.empty(F, np.float32)
     h = np.empty(F, np.float32)
-    lib().orc_expert_ffn(_p(ew4), _p(ers), H, F, _p(qx), _p(dx), _p(qh), _p(dh), _p(y),
-                         _p(g), _p(u), _p(h))
+    lib().orc_expert_ffn_w(_p(ew4), int(wbits), _p(ers), H, F, _p(qx), _p(dx), _p(qh), _p(dh), _p(y),
+                           _p(g), _p(u), _p(h))
     return dict(qh=qh, dh=dh, y=y, g=g, u=u, h=h)
 
 
 def moe_forward(x, router_w, router_b, experts_w4, experts_rs, shared_w4, shared_rs, H, F, k,
-                routed_scale, intermediates=False):
+                routed_scale, intermediates=False, wbits=4):
     """O6: the whole layer on T tokens.
 
     ``experts_w4``/``experts_rs`` are sequences of length E holding, per expert,
-    its packed bytes (uint8, 3*F*H/2) and row scales (F32, 2F+H), or None for an
-    expert no token selects.
+    its weight bytes and row scales (F32, 2F+H), or None for an expert no token
+    selects.  ``wbits`` is the weight container: 4 (packed int4, 3*F*H/2
+    bytes per expert) or 8 (int8 codes, 3*F*H bytes).
     """
     x = _c(x, np.float32)
     T = x.shape[0]
@@ -237,14 +266,14 @@ def moe_forward(x, router_w, router_b, experts_w4, experts_rs, shared_w4, shared
             W4[e] = None
             RS[e] = None
         else:
-            a = _c(experts_w4[e], np.uint8)
+            a = np.ascontiguousarray(experts_w4[e]).view(np.uint8)
             b = _c(experts_rs[e], np.float32)
             keep += [a, b]
             W4[e] = a.ctypes.data
             RS[e] = b.ctypes.data
     rw = _c(router_w, np.float32)
     rb = _c(router_b, np.float32)
-    sw = _c(shared_w4, np.uint8)
+    sw = np.ascontiguousarray(shared_w4).view(np.uint8)
     srs = _c(shared_rs, np.float32)
     out = np.empty((T, H), np.float32)
     qx = np.empty((T, H), np.int8) if intermediates else None
@@ -253,10 +282,10 @@ def moe_forward(x, router_w, router_b, experts_w4, experts_rs, shared_w4, shared
     w = np.empty((T, k), np.float32) if intermediates else None
     yr = np.empty((T, k, H), np.float32) if intermediates else None
     ys = np.empty((T, H), np.float32) if intermediates else None
-    st = lib().orc_moe_forward(_p(x), T, H, F, E, k, float(routed_scale), _p(rw), _p(rb),
-                               ctypes.cast(W4, ctypes.c_void_p), ctypes.cast(RS, ctypes.c_void_p),
-                               _p(sw), _p(srs), _p(out), _p(qx), _p(dx), _p(idx), _p(w),
-                               _p(yr), _p(ys))
+    st = lib().orc_moe_forward_w(_p(x), T, H, F, E, k, float(routed_scale), _p(rw), _p(rb), int(wbits),
+                                 ctypes.cast(W4, ctypes.c_void_p), ctypes.cast(RS, ctypes.c_void_p),
+                                 _p(sw), _p(srs), _p(out), _p(qx), _p(dx), _p(idx), _p(w),
+                                 _p(yr), _p(ys))
     if st != 0:
         raise ValueError(f"oracle: routed expert {-st - 1} was selected but not supplied")
     if intermediates:

@@ -98,6 +98,35 @@ ORC_API void orc_unpack_int4_rows(const uint8_t *packed, int rows, int K, int8_t
     }
 }
 
+/* int8 weight container (the pages' int8 head and their int8 container, to
+ * which the int4 packing decodes bit-identically) [P1 Key features]: one
+ * two's-complement byte per weight, s = max_k |w_k| / 127 (an IEEE F32
+ * divide), q_k = clamp(lrintf(w_k / s), -127, 127); an all-zero row has s = 0
+ * and every q = 0 (the same reading as the int4 container). */
+ORC_API void orc_pack_int8_rows(const float *w, int rows, int K, int8_t *q, float *scale)
+{
+    for (int r = 0; r < rows; ++r) {
+        const float *wr = w + (size_t)r * K;
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            float a = fabsf(wr[k]);
+            if (a > amax) amax = a;
+        }
+        float sr = amax / 127.0f;
+        scale[r] = sr;
+        int8_t *qr = q + (size_t)r * K;
+        for (int k = 0; k < K; ++k) {
+            long v = 0;
+            if (sr > 0.0f) {
+                v = lrintf(wr[k] / sr);
+                if (v < -127) v = -127;
+                if (v > 127) v = 127;
+            }
+            qr[k] = (int8_t)v;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* O2  Q8_0-style activation quantiser  [P1 Key features; P2 Attention and    */
 /*     kernels; P3 Optimised integer kernels; rounding per P5 TL;DR]         */
@@ -315,23 +344,49 @@ ORC_API void orc_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q,
     }
 }
 
+/* Weight code k of a row in a container of `wbits` bits per weight: 4 is the
+ * packed int4 container (nibble - 8), 8 the int8 container (the byte). */
+static int orc_wcode(const uint8_t *row, int wbits, int k)
+{
+    if (wbits == 8) return (int)(int8_t)row[k];
+    uint8_t byte = row[k / 2];
+    int nib = (k & 1) ? (byte >> 4) : (byte & 0x0F);
+    return nib - 8;
+}
+
 /* One output row: y = s_row * acc, where acc = 0 and, for blocks b ascending,
- * acc = fmaf(d_b, (float)I_b, acc) (reading: the per-row scale is applied once,
- * after the block sum). */
-static float orc_row_dot(const uint8_t *row4, float s_row, int K, const int8_t *q, const float *d)
+ * acc = fmaf(d_b, (float)I_b, acc) with I_b the int32 sum over block b of
+ * code * q (reading: the per-row scale is applied once, after the block sum). */
+static float orc_row_dot_w(const uint8_t *row, int wbits, float s_row, int K, const int8_t *q, const float *d)
 {
     float acc = 0.0f;
     for (int b = 0; b < K / 32; ++b) {
         int32_t I = 0;
         for (int i = 0; i < 32; ++i) {
             int k = 32 * b + i;
-            uint8_t byte = row4[k / 2];
-            int nib = (k & 1) ? (byte >> 4) : (byte & 0x0F);
-            I += (nib - 8) * (int32_t)q[k];
+            I += orc_wcode(row, wbits, k) * (int32_t)q[k];
         }
         acc = fmaf(d[b], (float)I, acc);
     }
     return s_row * acc;
+}
+
+static float orc_row_dot(const uint8_t *row4, float s_row, int K, const int8_t *q, const float *d)
+{
+    return orc_row_dot_w(row4, 4, s_row, K, q, d);
+}
+
+/* Block dots of the int8 container: I[r][b] = sum over block b of w8 * q. */
+ORC_API void orc_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *q, int32_t *I)
+{
+    int nb = K / 32;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < nb; ++b) {
+            int32_t acc = 0;
+            for (int i = 0; i < 32; ++i)
+                acc += (int32_t)w8[(size_t)r * K + 32 * b + i] * (int32_t)q[32 * b + i];
+            I[(size_t)r * nb + b] = acc;
+        }
 }
 
 ORC_API void orc_rows_dot(const uint8_t *w4, const float *s, int rows, int K, const int8_t *q,
@@ -346,17 +401,19 @@ ORC_API void orc_rows_dot(const uint8_t *w4, const float *s, int rows, int K, co
  * [gate F | up F | down H].  g_i, u_i by orc_row_dot over qx; h_i = (g_i *
  * sigma(g_i)) * u_i; h is Q8_0-quantised (F/32 blocks) into qh, dh; then
  * y_j = orc_row_dot(down_j) over qh.  Optional outputs g, u, h may be NULL. */
-ORC_API void orc_expert_ffn(const uint8_t *ew4, const float *ers, int H, int F,
-                            const int8_t *qx, const float *dx, int8_t *qh, float *dh, float *y,
-                            float *g_out, float *u_out, float *h_out)
+ORC_API void orc_expert_ffn_w(const uint8_t *ew, int wbits, const float *ers, int H, int F,
+                              const int8_t *qx, const float *dx, int8_t *qh, float *dh, float *y,
+                              float *g_out, float *u_out, float *h_out)
 {
-    const uint8_t *gate = ew4;
-    const uint8_t *up = ew4 + (size_t)F * (H / 2);
-    const uint8_t *down = ew4 + (size_t)2 * F * (H / 2);
+    /* a row of K weights takes K * wbits / 8 bytes */
+    const size_t rh = (size_t)H * wbits / 8, rf = (size_t)F * wbits / 8;
+    const uint8_t *gate = ew;
+    const uint8_t *up = ew + (size_t)F * rh;
+    const uint8_t *down = ew + (size_t)2 * F * rh;
     float *h = (float *)malloc(sizeof(float) * F);
     for (int i = 0; i < F; ++i) {
-        float g = orc_row_dot(gate + (size_t)i * (H / 2), ers[i], H, qx, dx);
-        float u = orc_row_dot(up + (size_t)i * (H / 2), ers[F + i], H, qx, dx);
+        float g = orc_row_dot_w(gate + (size_t)i * rh, wbits, ers[i], H, qx, dx);
+        float u = orc_row_dot_w(up + (size_t)i * rh, wbits, ers[F + i], H, qx, dx);
         h[i] = (g * orc_sigmoid(g)) * u;
         if (g_out) g_out[i] = g;
         if (u_out) u_out[i] = u;
@@ -364,8 +421,15 @@ ORC_API void orc_expert_ffn(const uint8_t *ew4, const float *ers, int H, int F,
     }
     orc_q8_0(h, F, qh, dh);
     for (int j = 0; j < H; ++j)
-        y[j] = orc_row_dot(down + (size_t)j * (F / 2), ers[2 * F + j], F, qh, dh);
+        y[j] = orc_row_dot_w(down + (size_t)j * rf, wbits, ers[2 * F + j], F, qh, dh);
     free(h);
+}
+
+ORC_API void orc_expert_ffn(const uint8_t *ew4, const float *ers, int H, int F,
+                            const int8_t *qx, const float *dx, int8_t *qh, float *dh, float *y,
+                            float *g_out, float *u_out, float *h_out)
+{
+    orc_expert_ffn_w(ew4, 4, ers, H, F, qx, dx, qh, dh, y, g_out, u_out, h_out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -379,12 +443,12 @@ ORC_API void orc_expert_ffn(const uint8_t *ew4, const float *ers, int H, int F,
  * Returns 0, or -(1 + e) if a selected expert e was not supplied.
  * Optional intermediates (NULL to skip): qx [T][H], dx [T][H/32], idx [T][k],
  * w [T][k], y_routed [T][k][H] (pair order), y_shared [T][H]. */
-ORC_API int orc_moe_forward(const float *x, int T, int H, int F, int E, int k, float routed_scale,
-                            const float *router_w, const float *router_b,
-                            const uint8_t *const *ew4, const float *const *ers,
-                            const uint8_t *sw4, const float *srs, float *out,
-                            int8_t *qx_out, float *dx_out, int32_t *idx_out, float *w_out,
-                            float *yr_out, float *ys_out)
+ORC_API int orc_moe_forward_w(const float *x, int T, int H, int F, int E, int k, float routed_scale,
+                              const float *router_w, const float *router_b, int wbits,
+                              const uint8_t *const *ew4, const float *const *ers,
+                              const uint8_t *sw4, const float *srs, float *out,
+                              int8_t *qx_out, float *dx_out, int32_t *idx_out, float *w_out,
+                              float *yr_out, float *ys_out)
 {
     int8_t *qx = (int8_t *)malloc((size_t)T * H);
     float *dx = (float *)malloc(sizeof(float) * (size_t)T * (H / 32));
@@ -406,12 +470,12 @@ ORC_API int orc_moe_forward(const float *x, int T, int H, int F, int E, int k, f
         float *dh = (float *)malloc(sizeof(float) * (F / 32));
         if (p < T * k) {
             int t = p / k, e = idx[p];
-            orc_expert_ffn(ew4[e], ers[e], H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
-                           qh, dh, yr + (size_t)p * H, NULL, NULL, NULL);
+            orc_expert_ffn_w(ew4[e], wbits, ers[e], H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
+                             qh, dh, yr + (size_t)p * H, NULL, NULL, NULL);
         } else {
             int t = p - T * k;
-            orc_expert_ffn(sw4, srs, H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
-                           qh, dh, ys + (size_t)t * H, NULL, NULL, NULL);
+            orc_expert_ffn_w(sw4, wbits, srs, H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
+                             qh, dh, ys + (size_t)t * H, NULL, NULL, NULL);
         }
         free(qh); free(dh);
     }
@@ -433,6 +497,17 @@ ORC_API int orc_moe_forward(const float *x, int T, int H, int F, int E, int k, f
 done:
     free(qx); free(dx); free(idx); free(w); free(yr); free(ys);
     return status;
+}
+
+ORC_API int orc_moe_forward(const float *x, int T, int H, int F, int E, int k, float routed_scale,
+                            const float *router_w, const float *router_b,
+                            const uint8_t *const *ew4, const float *const *ers,
+                            const uint8_t *sw4, const float *srs, float *out,
+                            int8_t *qx_out, float *dx_out, int32_t *idx_out, float *w_out,
+                            float *yr_out, float *ys_out)
+{
+    return orc_moe_forward_w(x, T, H, F, E, k, routed_scale, router_w, router_b, 4, ew4, ers, sw4, srs, out,
+                             qx_out, dx_out, idx_out, w_out, yr_out, ys_out);
 }
 
 /* Number of OpenMP threads the oracle will use (1 without OpenMP), and a

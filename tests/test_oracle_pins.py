@@ -497,3 +497,109 @@ def test_results_do_not_depend_on_thread_count(orc):
         np.testing.assert_array_equal(u.view(np.uint8) if u.dtype.kind == "f" else u,
                                       v.view(np.uint8) if v.dtype.kind == "f" else v)
 
+
+
+# --------------------------------------------------------------------------- #
+# The int8 weight container (the pages' int8 head / int8 container)          #
+# --------------------------------------------------------------------------- #
+def test_int8_container_rule(orc):
+    """s = max|row| / 127, q = clamp(lrintf(w / s), -127, 127): the largest
+    element maps to +-127, every element is within s/2 of q*s, a zero row has
+    s = 0 and zero codes, and a row of one repeated value is exact."""
+    g = np.random.default_rng(21)
+    w = (g.standard_normal((32, 256)) * 0.02).astype(np.float32)
+    w[3] = 0.0
+    w[4] = np.float32(0.5)
+    q, s = orc.pack_int8_rows(w)
+    assert q.dtype == np.int8 and np.all(np.abs(q.astype(np.int32)) <= 127)
+    for r in range(32):
+        if r == 3:
+            assert s[r] == 0.0 and not np.any(q[r])
+            continue
+        assert s[r] == np.float32(np.float32(np.abs(w[r]).max()) / np.float32(127.0))
+        k = int(np.argmax(np.abs(w[r])))
+        assert abs(int(q[r, k])) == 127
+        err = np.abs(w[r].astype(np.float64) - q[r].astype(np.float64) * float(s[r]))
+        assert np.all(err <= float(s[r]) / 2 * (1 + 2 ** -20) + 1e-12)
+    assert np.all(q[4] == 127)
+
+
+def test_int8_block_dots_bruteforce(orc):
+    g = np.random.default_rng(22)
+    K = 512
+    w8 = g.integers(-127, 128, (16, K)).astype(np.int8)
+    w8[0] = -127
+    q = g.integers(-127, 128, K).astype(np.int8)
+    q[:32] = 127
+    I = orc.block_dots_w8(w8, q)
+    ref = (w8.astype(np.int64) * q.astype(np.int64)).reshape(16, K // 32, 32).sum(-1)
+    np.testing.assert_array_equal(I, ref)
+    assert I[0, 0] == -127 * 127 * 32
+
+
+def test_int4_codes_in_the_int8_container_give_identical_bits(orc):
+    """The pages report the int4 packing verified bit-identical to the int8
+    container.  Here: an expert's int4 codes, widened into the int8 container
+    with the same row scales, give the same block dots, the same expert
+    outputs (g, u, h, the requantised h and y) and the same layer output, bit
+    for bit, through the int8 path."""
+    H, F = TINY.hidden, TINY.ffn
+    g = np.random.default_rng(23)
+    mats = [(g.standard_normal((F, H)) * 0.02).astype(np.float32),
+            (g.standard_normal((F, H)) * 0.02).astype(np.float32),
+            (g.standard_normal((H, F)) * 0.02).astype(np.float32)]
+    packs = [orc.pack_int4_rows(m) for m in mats]
+    ew4 = np.concatenate([p.ravel() for p, _ in packs])
+    ew8 = np.concatenate([orc.unpack_int4_rows(p).ravel() for p, _ in packs])
+    ers = np.concatenate([s for _, s in packs])
+    x = g.standard_normal((3, H)).astype(np.float32)
+    qx, dx = orc.q8_0(x)
+    np.testing.assert_array_equal(orc.block_dots(packs[0][0], qx[0]),
+                                  orc.block_dots_w8(orc.unpack_int4_rows(packs[0][0]), qx[0]))
+    for t in range(3):
+        r4 = orc.expert_ffn(ew4, ers, H, F, qx[t], dx[t], wbits=4)
+        r8 = orc.expert_ffn(ew8, ers, H, F, qx[t], dx[t], wbits=8)
+        for key in ("g", "u", "h", "qh", "dh", "y"):
+            np.testing.assert_array_equal(r4[key].view(np.uint8), r8[key].view(np.uint8), err_msg=key)
+    # the whole layer: E = 4 experts sharing this draw's pattern, plus a shared one
+    E, k = 4, 2
+    W = (g.standard_normal((E, H)) * 0.02).astype(np.float32)
+    b = (g.standard_normal(E) * 0.01).astype(np.float32)
+    out4 = orc.moe_forward(x, W, b, [ew4] * E, [ers] * E, ew4, ers, H, F, k, 2.5, wbits=4)
+    out8 = orc.moe_forward(x, W, b, [ew8] * E, [ers] * E, ew8, ers, H, F, k, 2.5, wbits=8)
+    np.testing.assert_array_equal(out4.view(np.uint32), out8.view(np.uint32))
+
+
+def test_int8_expert_ffn_against_float_swiglu(orc):
+    """Int8 weights: against double SwiGLU on the dequantised weights the error
+    is the activation quantisers' alone, and against the unquantised weights
+    the weight noise (~s/sqrt(12), 18x smaller than int4's) is added; both
+    within twice the prediction, and well below the int4 container's error."""
+    H, F = TINY.hidden, TINY.ffn
+    g = np.random.default_rng(24)
+    Ws = [(g.standard_normal((F, H)) * 0.02).astype(np.float32),
+          (g.standard_normal((F, H)) * 0.02).astype(np.float32),
+          (g.standard_normal((H, F)) * 0.02).astype(np.float32)]
+    packs = [orc.pack_int8_rows(W) for W in Ws]
+    ew8 = np.concatenate([q.ravel() for q, _ in packs])
+    ers = np.concatenate([s for _, s in packs])
+    D = [q.astype(np.float64) * s[:, None].astype(np.float64) for q, s in packs]
+    p4 = [orc.pack_int4_rows(W) for W in Ws]
+    ew4 = np.concatenate([p.ravel() for p, _ in p4])
+    ers4 = np.concatenate([s for _, s in p4])
+    for trial in range(4):
+        x = g.standard_normal(H).astype(np.float32)
+        qx, dx = orc.q8_0(x)
+        r = orc.expert_ffn(ew8, ers, H, F, qx, dx, wbits=8)
+        y_ref, _ = _swiglu64(D[0], D[1], D[2], x.astype(np.float64))
+        ex = _rel_rms(qx * np.repeat(dx, 32).astype(np.float64), x.astype(np.float64))
+        eh = _rel_rms(r["qh"] * np.repeat(r["dh"], 32).astype(np.float64), r["h"].astype(np.float64))
+        pred = math.sqrt((2 * ex) ** 2 + eh ** 2)
+        assert _rel_rms(r["y"].astype(np.float64), y_ref) <= 2 * pred
+        y32, _ = _swiglu64(*(W.astype(np.float64) for W in Ws), x.astype(np.float64))
+        ew = np.mean([_rel_rms(Dm, W.astype(np.float64)) for Dm, W in zip(D, Ws)])
+        pred_w = math.sqrt(3 * ew ** 2 + pred ** 2)
+        err8 = _rel_rms(r["y"].astype(np.float64), y32)
+        assert err8 <= 2 * pred_w
+        r4 = orc.expert_ffn(ew4, ers4, H, F, qx, dx, wbits=4)
+        assert err8 < _rel_rms(r4["y"].astype(np.float64), y32)
