@@ -200,9 +200,13 @@ long long coli_moe_launch_count(void);
  * library until exit; larger n_tok or E return COLI_E_INVAL.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current, so make that first call before any stream capture.  All
- * calls share the one array: calls that overlap on the GPU (different
- * streams, or different host threads) race on it. */
+ * device current, so make that first call before any stream capture.  CUDA
+ * loads module code and data lazily by default, so that first call is also
+ * when the array's device memory is committed: make it before reserving the
+ * rest of device memory (or set CUDA_MODULE_LOADING=EAGER).  The cached
+ * address is invalid after cudaDeviceReset().  All calls share the one
+ * array: calls that overlap on the GPU (different streams, or different host
+ * threads) race on it. */
 #define COLI_STATIC_MAX_TOK 64
 int coli_moe_route_noalloc(const coli_moe_shape *s, const float *x, int n_tok,
                            const float *router_w, const float *router_bias, int32_t *idx, float *w,

@@ -243,12 +243,28 @@ def route_noalloc(x, router_w, router_bias, hidden, n_experts, top_k, routed_sca
     """Router for callers that cannot allocate device memory (see the header):
     no configure() needed; scratch is a static device array of the library.
     ``idx``/``w`` may be given pre-allocated by the caller."""
+    if x.dim() != 2 or x.shape[1] != hidden:
+        raise ValueError(f"x must be [n_tok][{hidden}]")
     T = x.shape[0]
-    s = _Shape(hidden, 0, n_experts, top_k, routed_scale, 0)
+    if tuple(router_w.shape) != (n_experts, hidden):
+        raise ValueError(f"router_w must be [{n_experts}][{hidden}]")
+    if router_bias.numel() != n_experts:
+        raise ValueError(f"router_bias must hold {n_experts} values")
+    for name, t in (("x", x), ("router_w", router_w), ("router_bias", router_bias)):
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
     if idx is None:
         idx = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
     if w is None:
         w = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    if idx.dtype != torch.int32 or idx.numel() < T * top_k:
+        raise ValueError(f"idx must be int32 with at least n_tok*top_k = {T * top_k} elements")
+    if w.dtype != torch.float32 or w.numel() < T * top_k:
+        raise ValueError(f"w must be float32 with at least n_tok*top_k = {T * top_k} elements")
+    for name, t in (("x", x), ("router_w", router_w), ("router_bias", router_bias), ("idx", idx), ("w", w)):
+        if not t.is_cuda or t.device != x.device:
+            raise ValueError(f"{name} must be on x's CUDA device")
+    s = _Shape(hidden, 0, n_experts, top_k, routed_scale, 0)
     _check(_lib.coli_moe_route_noalloc(ctypes.byref(s), _ptr(x), T, _ptr(router_w), _ptr(router_bias),
                                        _ptr(idx), _ptr(w), _stream(stream)), "route_noalloc")
     return idx, w

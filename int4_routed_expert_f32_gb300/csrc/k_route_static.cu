@@ -9,6 +9,7 @@
 // prior coli_moe_configure() call.  The array is sized for at most
 // COLI_STATIC_MAX_TOK tokens and 256 experts and stays resident on every GPU
 // that loads this library until the process exits.
+#include <atomic>
 #include <cstdio>
 
 #include "../../include/coli_moe.h"
@@ -27,8 +28,19 @@ static __device__ __align__(256) float g_static_logits[STATIC_MAX_TOK * STATIC_M
 
 // Device address of g_static_logits per device.  In host code the array's
 // name is a host-side stand-in, not a device address, so the address is
-// looked up once per device (with that device current) and cached.
-static float *g_static_logits_dev[MAX_DEVICES];
+// looked up once per device (with that device current) and cached.  The
+// entries are atomics: two host threads making their first call on the same
+// device look up the same address, and either store is correct.  A cached
+// address belongs to the device's current context: after cudaDeviceReset()
+// it is stale, and the library must be reloaded before this call is used
+// again on that device.
+//
+// CUDA loads a module's device code and data lazily by default, so the first
+// call on a device (the symbol lookup or the first launch) is when the
+// array's device memory is committed.  A caller that reserves all remaining
+// device memory, or captures streams, should make one call first (or run
+// with CUDA_MODULE_LOADING=EAGER).
+static std::atomic<float *> g_static_logits_dev[MAX_DEVICES];
 
 static int static_scratch(float **out)
 {
@@ -37,15 +49,17 @@ static int static_scratch(float **out)
         (void)cudaGetLastError();
         return COLI_E_CUDA;
     }
-    if (!g_static_logits_dev[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_logits) != cudaSuccess || !p) {
+    float *p = g_static_logits_dev[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_static_logits) != cudaSuccess || !a) {
             (void)cudaGetLastError();
             return COLI_E_CUDA;
         }
-        g_static_logits_dev[dev] = static_cast<float *>(p);
+        p = static_cast<float *>(a);
+        g_static_logits_dev[dev].store(p, std::memory_order_release);
     }
-    *out = g_static_logits_dev[dev];
+    *out = p;
     return COLI_OK;
 }
 

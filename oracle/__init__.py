@@ -50,6 +50,7 @@ def lib():
             L.orc_pack_int8_rows.argtypes = [P, i, i, P, P]
             L.orc_block_dots_w8.argtypes = [P, i, i, P, P]
             L.orc_expert_ffn_w.argtypes = [P, i, P, i, i, P, P, P, P, P, P, P, P]
+            L.orc_expert_ffn_w.restype = i
             L.orc_moe_forward_w.argtypes = [P, i, i, i, i, i, f, P, P, i, P, P, P, P, P,
                                             P, P, P, P, P, P]
             L.orc_moe_forward_w.restype = i
@@ -227,12 +228,29 @@ def rows_dot(w4, s, q, d):
     return out
 
 
+_E_WBITS = -1000000   # orc_moe_forward_w: weight container other than 4 or 8 bits
+
+
+def _weight_bytes(w, H, F, wbits):
+    """One expert's weights as flat bytes, checked against the container's
+    size (3*F*H*wbits/8 bytes: gate, up and down)."""
+    if wbits not in (4, 8):
+        raise ValueError(f"oracle: unsupported weight container wbits={wbits} (4 or 8)")
+    a = np.ascontiguousarray(w).view(np.uint8).reshape(-1)
+    want = 3 * F * H * wbits // 8
+    if a.size != want:
+        raise ValueError(f"expert weights: {a.size} bytes, expected 3*F*H*{wbits}/8 = {want}")
+    return a
+
+
 def expert_ffn(ew4, ers, H, F, qx, dx, wbits=4):
     """O5 for one expert and one token: returns dict(qh, dh, y, g, u, h).
     ``wbits`` is the weight container: 4 (packed int4 bytes, 3*F*H/2) or 8
     (int8 codes as bytes, 3*F*H)."""
-    ew4 = np.ascontiguousarray(ew4).view(np.uint8).reshape(-1)
+    ew4 = _weight_bytes(ew4, H, F, wbits)
     ers = _c(ers, np.float32).reshape(-1)
+    if ers.size != 2 * F + H:
+        raise ValueError(f"row scales: {ers.size} values, expected 2F+H = {2 * F + H}")
     qx = _c(qx, np.int8)
     dx = _c(dx, np.float32)
     qh = np.empty(F, np.int8)
@@ -241,8 +259,9 @@ def expert_ffn(ew4, ers, H, F, qx, dx, wbits=4):
     g = np.empty(F, np.float32)
     u = np.empty(F, np.float32)
     h = np.empty(F, np.float32)
-    lib().orc_expert_ffn_w(_p(ew4), int(wbits), _p(ers), H, F, _p(qx), _p(dx), _p(qh), _p(dh), _p(y),
-                           _p(g), _p(u), _p(h))
+    if lib().orc_expert_ffn_w(_p(ew4), int(wbits), _p(ers), H, F, _p(qx), _p(dx), _p(qh), _p(dh), _p(y),
+                              _p(g), _p(u), _p(h)) != 0:
+        raise ValueError(f"oracle: unsupported weight container wbits={wbits}")
     return dict(qh=qh, dh=dh, y=y, g=g, u=u, h=h)
 
 
@@ -266,15 +285,19 @@ def moe_forward(x, router_w, router_b, experts_w4, experts_rs, shared_w4, shared
             W4[e] = None
             RS[e] = None
         else:
-            a = np.ascontiguousarray(experts_w4[e]).view(np.uint8)
+            a = _weight_bytes(experts_w4[e], H, F, wbits)
             b = _c(experts_rs[e], np.float32)
+            if b.size != 2 * F + H:
+                raise ValueError(f"expert {e}: {b.size} row scales, expected 2F+H = {2 * F + H}")
             keep += [a, b]
             W4[e] = a.ctypes.data
             RS[e] = b.ctypes.data
     rw = _c(router_w, np.float32)
     rb = _c(router_b, np.float32)
-    sw = np.ascontiguousarray(shared_w4).view(np.uint8)
+    sw = _weight_bytes(shared_w4, H, F, wbits)
     srs = _c(shared_rs, np.float32)
+    if srs.size != 2 * F + H:
+        raise ValueError(f"shared expert: {srs.size} row scales, expected 2F+H = {2 * F + H}")
     out = np.empty((T, H), np.float32)
     qx = np.empty((T, H), np.int8) if intermediates else None
     dx = np.empty((T, H // 32), np.float32) if intermediates else None
@@ -286,6 +309,8 @@ def moe_forward(x, router_w, router_b, experts_w4, experts_rs, shared_w4, shared
                                  ctypes.cast(W4, ctypes.c_void_p), ctypes.cast(RS, ctypes.c_void_p),
                                  _p(sw), _p(srs), _p(out), _p(qx), _p(dx), _p(idx), _p(w),
                                  _p(yr), _p(ys))
+    if st == _E_WBITS:
+        raise ValueError(f"oracle: unsupported weight container wbits={wbits}")
     if st != 0:
         raise ValueError(f"oracle: routed expert {-st - 1} was selected but not supplied")
     if intermediates:

@@ -42,6 +42,8 @@
 #include <string.h>
 
 #define ORC_API __attribute__((visibility("default")))
+/* status of orc_moe_forward_w for a weight container other than 4 or 8 bits */
+#define ORC_E_WBITS (-1000000)
 
 /* ------------------------------------------------------------------------- */
 /* Bit helpers                                                               */
@@ -401,10 +403,12 @@ ORC_API void orc_rows_dot(const uint8_t *w4, const float *s, int rows, int K, co
  * [gate F | up F | down H].  g_i, u_i by orc_row_dot over qx; h_i = (g_i *
  * sigma(g_i)) * u_i; h is Q8_0-quantised (F/32 blocks) into qh, dh; then
  * y_j = orc_row_dot(down_j) over qh.  Optional outputs g, u, h may be NULL. */
-ORC_API void orc_expert_ffn_w(const uint8_t *ew, int wbits, const float *ers, int H, int F,
-                              const int8_t *qx, const float *dx, int8_t *qh, float *dh, float *y,
-                              float *g_out, float *u_out, float *h_out)
+ORC_API int orc_expert_ffn_w(const uint8_t *ew, int wbits, const float *ers, int H, int F,
+                             const int8_t *qx, const float *dx, int8_t *qh, float *dh, float *y,
+                             float *g_out, float *u_out, float *h_out)
 {
+    /* the two containers: 4 (packed nibbles) or 8 (one int8 code per byte) */
+    if (wbits != 4 && wbits != 8) return -1;
     /* a row of K weights takes K * wbits / 8 bytes */
     const size_t rh = (size_t)H * wbits / 8, rf = (size_t)F * wbits / 8;
     const uint8_t *gate = ew;
@@ -423,13 +427,14 @@ ORC_API void orc_expert_ffn_w(const uint8_t *ew, int wbits, const float *ers, in
     for (int j = 0; j < H; ++j)
         y[j] = orc_row_dot_w(down + (size_t)j * rf, wbits, ers[2 * F + j], F, qh, dh);
     free(h);
+    return 0;
 }
 
 ORC_API void orc_expert_ffn(const uint8_t *ew4, const float *ers, int H, int F,
                             const int8_t *qx, const float *dx, int8_t *qh, float *dh, float *y,
                             float *g_out, float *u_out, float *h_out)
 {
-    orc_expert_ffn_w(ew4, 4, ers, H, F, qx, dx, qh, dh, y, g_out, u_out, h_out);
+    (void)orc_expert_ffn_w(ew4, 4, ers, H, F, qx, dx, qh, dh, y, g_out, u_out, h_out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -440,7 +445,8 @@ ORC_API void orc_expert_ffn(const uint8_t *ew4, const float *ers, int H, int F,
  * has weight 1 (DeepSeek-V3 heritage; the pages are silent).  Expert weights
  * are given per expert (ew4[e], ers[e]); a NULL entry is allowed for an expert
  * no token selects, so callers may supply only the experts a sample touches.
- * Returns 0, or -(1 + e) if a selected expert e was not supplied.
+ * Returns 0, -(1 + e) if a selected expert e was not supplied, or
+ * ORC_E_WBITS for a container other than 4 or 8 bits.
  * Optional intermediates (NULL to skip): qx [T][H], dx [T][H/32], idx [T][k],
  * w [T][k], y_routed [T][k][H] (pair order), y_shared [T][H]. */
 ORC_API int orc_moe_forward_w(const float *x, int T, int H, int F, int E, int k, float routed_scale,
@@ -450,6 +456,7 @@ ORC_API int orc_moe_forward_w(const float *x, int T, int H, int F, int E, int k,
                               int8_t *qx_out, float *dx_out, int32_t *idx_out, float *w_out,
                               float *yr_out, float *ys_out)
 {
+    if (wbits != 4 && wbits != 8) return ORC_E_WBITS;
     int8_t *qx = (int8_t *)malloc((size_t)T * H);
     float *dx = (float *)malloc(sizeof(float) * (size_t)T * (H / 32));
     int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k);
@@ -470,12 +477,12 @@ ORC_API int orc_moe_forward_w(const float *x, int T, int H, int F, int E, int k,
         float *dh = (float *)malloc(sizeof(float) * (F / 32));
         if (p < T * k) {
             int t = p / k, e = idx[p];
-            orc_expert_ffn_w(ew4[e], wbits, ers[e], H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
-                             qh, dh, yr + (size_t)p * H, NULL, NULL, NULL);
+            (void)orc_expert_ffn_w(ew4[e], wbits, ers[e], H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
+                                   qh, dh, yr + (size_t)p * H, NULL, NULL, NULL);
         } else {
             int t = p - T * k;
-            orc_expert_ffn_w(sw4, wbits, srs, H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
-                             qh, dh, ys + (size_t)t * H, NULL, NULL, NULL);
+            (void)orc_expert_ffn_w(sw4, wbits, srs, H, F, qx + (size_t)t * H, dx + (size_t)t * (H / 32),
+                                   qh, dh, ys + (size_t)t * H, NULL, NULL, NULL);
         }
         free(qh); free(dh);
     }

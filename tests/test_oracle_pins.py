@@ -538,11 +538,13 @@ def test_int8_block_dots_bruteforce(orc):
 
 
 def test_int4_codes_in_the_int8_container_give_identical_bits(orc):
-    """The pages report the int4 packing verified bit-identical to the int8
-    container.  Here: an expert's int4 codes, widened into the int8 container
+    """Container-equivalence pin of the oracle's two weight paths (a guard on
+    the shared row-dot code, not a check of the pages' claim, which holds here
+    by construction): an expert's int4 codes, widened into the int8 container
     with the same row scales, give the same block dots, the same expert
     outputs (g, u, h, the requantised h and y) and the same layer output, bit
-    for bit, through the int8 path."""
+    for bit, through the int8 path.  The GPU-side counterpart compares the
+    device's int4 and int8-container kernels."""
     H, F = TINY.hidden, TINY.ffn
     g = np.random.default_rng(23)
     mats = [(g.standard_normal((F, H)) * 0.02).astype(np.float32),
@@ -603,3 +605,20 @@ def test_int8_expert_ffn_against_float_swiglu(orc):
         assert err8 <= 2 * pred_w
         r4 = orc.expert_ffn(ew4, ers4, H, F, qx, dx, wbits=4)
         assert err8 < _rel_rms(r4["y"].astype(np.float64), y32)
+
+
+def test_oracle_rejects_unsupported_weight_containers(orc):
+    """Only the 4- and 8-bit containers exist: any other width, or a weight
+    buffer whose size does not match the container, is refused before the C
+    code could read past it."""
+    H, F = TINY.hidden, TINY.ffn
+    ers = np.ones(2 * F + H, np.float32)
+    qx = np.zeros(H, np.int8)
+    dx = np.zeros(H // 32, np.float32)
+    for wbits in (2, 16, 0):
+        with pytest.raises(ValueError):
+            orc.expert_ffn(np.zeros(3 * F * H, np.uint8), ers, H, F, qx, dx, wbits=wbits)
+    with pytest.raises(ValueError):
+        orc.expert_ffn(np.zeros(3 * F * H // 2 - 1, np.uint8), ers, H, F, qx, dx, wbits=4)
+    with pytest.raises(ValueError):
+        orc.expert_ffn(np.zeros(3 * F * H // 2, np.uint8), ers, H, F, qx, dx, wbits=8)
