@@ -8,9 +8,15 @@ combine).  L2 is flushed (a 512 MiB write) between timed steps, outside the
 timed region, so the shared expert and router weights are re-read from HBM
 like in a real multi-layer decode.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|verify|prefill]
-                  [--path auto|gemv|gemm]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|verify|prefill|sweep]
+                  [--path auto|gemv|gemm] [--sub verify,prefill,sweep|none]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+The default decode run also measures, in the same process and printed as
+sub-records of the one JSON line: "verify" (4 correlated tokens per forward on
+the same resident weights), "prefill" (2048 tokens, Zipf-skewed routing, the
+same weights) and "sweep" (8 stacked layers at batches 1, 8, 32 and 128).
+Each sub-record carries its own roofline, clocks, e2e and cpu_baseline.
 
 The 2048-token prefill workload runs the grouped tensor-core GEMM (auto path);
 its roofline line is the gate/up GEMM's FLOP/s against the measured bf16 dense
@@ -232,17 +238,19 @@ def _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens,
 CPU_SAMPLE_TOKENS = {"prefill": 24, "sweep": 1}   # bounded oracle sample per forward (tokens)
 
 
-def cpu_baseline_line(wl, n_forwards: int, min_seconds: float):
-    """The oracle on all of the host's cores, plus a shorter single-thread
-    sample, with the host's machine type."""
+def cpu_baseline_line(wl, n_forwards: int, min_seconds: float, single_thread: bool = True):
+    """The oracle on all of the host's cores, plus (optionally) a shorter
+    single-thread sample, with the host's machine type."""
     import platform
     mt = CPU_SAMPLE_TOKENS.get(wl.name, 0)
     tps, cores, sample = oracle_baseline(wl, n_forwards, max_tokens=mt, min_seconds=min_seconds)
-    st_tps, _, st_sample = oracle_baseline(wl, max(1, n_forwards // 4), max_tokens=mt,
-                                           min_seconds=min_seconds / 3.0, threads=1)
-    return {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample,
-            "machine": platform.machine(),
-            "single_thread": {"value": st_tps, "unit": "tok/s", "sample": st_sample}}
+    rec = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample,
+           "machine": platform.machine()}
+    if single_thread:
+        st_tps, _, st_sample = oracle_baseline(wl, max(1, n_forwards // 4), max_tokens=mt,
+                                               min_seconds=min_seconds / 3.0, threads=1)
+        rec["single_thread"] = {"value": st_tps, "unit": "tok/s", "sample": st_sample}
+    return rec
 
 
 def run_reference(args):
@@ -288,33 +296,36 @@ def workload_config(wl):
             "l2": "flushed between timed steps (512 MiB write, outside the timed region)"}
 
 
-def run(args):
+def _setup(args):
+    """Build the library, set the device and (torchrun) the process group."""
     import torch
     import torch.distributed as dist
 
     import __graft_entry__
     __graft_entry__._builder().build()
-    import int4_routed_expert_f32_gb300 as coli
-    from synth.device import build_device_layer
-
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
-    wl = synth.WORKLOADS[args.workload]
+    return world, rank, local
+
+
+def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single_thread_cpu=True):
+    """One layer workload on resident weights L (router bias `router_b`):
+    the timed forwards, the dominant kernel timed alone, the end-to-end
+    host-I/O forwards and the CPU oracle sample; returns the record."""
+    import torch
+
+    import int4_routed_expert_f32_gb300 as coli
+
     T = wl.n_tok
     coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
     path = {"auto": coli.PATH_AUTO, "gemv": coli.PATH_GEMV, "gemm": coli.PATH_GEMM}[args.path]
     coli.set_path(path)
     use_gemm = path == coli.PATH_GEMM or (path == coli.PATH_AUTO and
                                           coli.auto_uses_gemm(T, wl.top_k, wl.n_experts))
-    t_build = time.perf_counter()
-    L = build_device_layer(wl)
-    W, b = synth.router(wl)
-    L["router_b"] = torch.from_numpy(b).cuda()
-    t_build = time.perf_counter() - t_build
     n_total = args.warmup + args.steps
     # distinct inputs per step (cycled for large batches to bound host time and memory)
     n_in = n_total if T <= 64 else min(n_total, 8)
@@ -327,12 +338,12 @@ def run(args):
     # union of routed experts per step (bookkeeping for weight bytes; not timed)
     unions = []
     for i in range(n_total):
-        idx, _ = coli.dbg_route(xs[i % n_in], L["router_w"], L["router_b"], wl.top_k)
+        idx, _ = coli.dbg_route(xs[i % n_in], L["router_w"], router_b, wl.top_k)
         unions.append(len(set(idx.cpu().numpy().ravel().tolist())))
     torch.cuda.synchronize()
 
     def fwd(i):
-        coli.layer_forward(xs[i % n_in], L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+        coli.layer_forward(xs[i % n_in], L["router_w"], router_b, L["expert_w4"], L["expert_rs"],
                            L["shared_w4"], L["shared_rs"], out=out)
 
     for i in range(args.warmup):
@@ -344,6 +355,7 @@ def run(args):
           for _ in range(args.steps)]
     coli.launch_count()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -378,17 +390,18 @@ def run(args):
     xh = xh.pin_memory()
     oh = torch.empty((T, wl.hidden), dtype=torch.float32).pin_memory()
     for i in range(min(args.warmup, 5)):
-        coli.layer_forward_hostio(xh[i % n_h], L["router_w"], L["router_b"], L["expert_w4"],
+        coli.layer_forward_hostio(xh[i % n_h], L["router_w"], router_b, L["expert_w4"],
                                   L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
     e2e_s = 0.0
     for s in range(args.steps):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        coli.layer_forward_hostio(xh[s % n_h], L["router_w"], L["router_b"], L["expert_w4"],
+        coli.layer_forward_hostio(xh[s % n_h], L["router_w"], router_b, L["expert_w4"],
                                   L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
         e2e_s += time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world)
+    coli.set_path(coli.PATH_AUTO)
 
     hbm_peak, bf16_peak, peak_kind = peaks()
     ub = np.array(unions[args.warmup:], dtype=np.float64)
@@ -415,64 +428,105 @@ def run(args):
                     "kernel": "k_experts (gate/up + SiLU*up requant + down + combine), timed alone",
                     "algorithmic_bytes_per_launch": bytes_per_fwd,
                     "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} hbm_gbs"}
-    line = {
+    step_s = total_ms / args.steps * 1e-3
+    rec = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32", "data": "synthetic",
         "config": workload_config(wl),
         "roofline": roofline,
         "expert_path": "gemm" if use_gemm else "gemv",
-        "weight_gbs_layer": bytes_per_fwd / (total_ms / args.steps * 1e-3) / 1e9,
-        "tops_layer": 2.0 * macs_layer / (total_ms / args.steps * 1e-3) / 1e12,
+        "weight_gbs_layer": bytes_per_fwd / step_s / 1e9,
+        "tops_layer": 2.0 * macs_layer / step_s / 1e12,
         # whole-layer bound: max(weight bytes / HBM peak, ops / bf16 peak) over the step time
         "layer_roofline_frac": max(bytes_per_fwd / (hbm_peak * 1e9), 2.0 * macs_layer / (bf16_peak * 1e12))
-                               / (total_ms / args.steps * 1e-3),
+                               / step_s,
+        "union_mean": float(np.mean(ub)),
         "e2e": {"value": world * args.steps * T / e2e_s, "unit": "tok/s",
                 "h2d_bytes_per_step": T * wl.hidden * 4, "d2h_bytes_per_step": T * wl.hidden * 4},
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "device_status": status,
-        "setup_s": round(t_build, 1),
         "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
     }
+    if use_gemm:
+        rec["layer_roofline_terms_ms"] = {"weights_at_hbm_peak": bytes_per_fwd / (hbm_peak * 1e9) * 1e3,
+                                          "ops_at_bf16_peak": 2.0 * macs_layer / (bf16_peak * 1e12) * 1e3}
     if rank == 0 and not args.no_cpu_baseline:
         nf = args.cpu_forwards if T <= 64 else 1
-        line["cpu_baseline"] = cpu_baseline_line(wl, nf, args.cpu_seconds)
+        rec["cpu_baseline"] = cpu_baseline_line(wl, nf, cpu_seconds, single_thread=single_thread_cpu)
+    del xs, out, flush
+    return rec
+
+
+SUB_WORKLOADS = ("verify", "prefill", "sweep")
+
+
+def run(args):
+    import torch
+
+    from synth.device import build_device_layer
+
+    world, rank, local = _setup(args)
+    wl = synth.WORKLOADS[args.workload]
+    t_build = time.perf_counter()
+    L = build_device_layer(wl)
+    t_build = time.perf_counter() - t_build
+    _, b = synth.router(wl)
+    line = measure_layer(args, wl, L, torch.from_numpy(b).cuda(), world, rank, local, args.cpu_seconds)
+    line["setup_s"] = round(t_build, 1)
+    subs = [w for w in args.sub.split(",") if w] if args.sub != "none" else []
+    bad = [w for w in subs if w not in SUB_WORKLOADS]
+    if bad:
+        raise SystemExit(f"unknown sub-record(s) {bad}; choose from {SUB_WORKLOADS}")
+    subs = sorted(set(subs), key=SUB_WORKLOADS.index)     # the sweep (which frees L) last
+    if subs and wl.name == "decode":
+        for name in subs:
+            t0 = time.perf_counter()
+            if name == "sweep":
+                del L
+                torch.cuda.empty_cache()
+                rec = measure_sweep(args, world, rank, local, args.cpu_seconds / 2)
+            else:
+                swl = synth.WORKLOADS[name]
+                _, sb = synth.router(swl)          # same weights; prefill's bias is Zipf-skewed
+                rec = measure_layer(args, swl, L, torch.from_numpy(sb).cuda(), world, rank, local,
+                                    args.cpu_seconds / 2, single_thread_cpu=False)
+            for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "dtype", "data",
+                      "warmup"):
+                rec.pop(k, None)
+            rec["wall_s"] = round(time.perf_counter() - t0, 1)
+            line[name] = rec
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
+        import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def run_sweep(args):
+def measure_sweep(args, world, rank, local, cpu_seconds):
     """Multi-layer decode sweep: the stacked layers (residual add fused into
     each layer's combine) at each batch size; one step = one pass through all
     layers.  `value` is tokens/s through the stack at batch 1; the per-batch
-    figures are in "sweep"."""
+    figures are in "sweep"; the roofline is the expert kernel's weight
+    stream at batch 1 (every layer's launch, timed alone)."""
     import torch
 
-    import __graft_entry__
-    __graft_entry__._builder().build()
     import int4_routed_expert_f32_gb300 as coli
     from synth.device import build_device_layer
 
-    import torch.distributed as dist
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
     wl = synth.WORKLOADS["sweep"]
     t_build = time.perf_counter()
     layers = [build_device_layer(wl, layer=l) for l in range(wl.layers)]
     t_build = time.perf_counter() - t_build
     coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, max(wl.batches))
+    coli.set_path(coli.PATH_AUTO)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     st = torch.cuda.current_stream()
     hbm_peak, _, peak_kind = peaks()
     per_b = []
     launches_total = 0
+    kernel_b1 = None
     with ClockSampler(local) as clocks:
         for B in wl.batches:
             n_in = 4
@@ -511,6 +565,7 @@ def run_sweep(args):
             torch.cuda.synchronize()
             coli.launch_count()
             if world > 1:
+                import torch.distributed as dist
                 dist.barrier()
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
@@ -526,11 +581,28 @@ def run_sweep(args):
             ub = [unions[k % n_in] for k in range(args.steps)]
             bytes_step = float(np.mean([sum(u_ + 1 for u_ in uu) for uu in ub])) * expert_bytes(wl)
             gbs = bytes_step / (t * 1e-3) / 1e9
+            # the expert kernel of every layer, timed alone (a second pass)
+            coli.timing_read()
+            coli.timing_enable(True)
+            for k in range(args.steps):
+                flush.zero_()
+                stack(xs[k % n_in])
+            torch.cuda.synchronize()
+            coli.timing_enable(False)
+            k_ms, k_n = coli.timing_read()
+            k_gbs = bytes_step / (k_ms * 1e-3 / max(args.steps, 1)) / 1e9
             per_b.append({"batch": B, "ms_per_step": t, "tok_s": world * B / (t * 1e-3),
                           "weight_gbs_per_gpu": gbs, "weight_frac_of_hbm": gbs / hbm_peak,
+                          "expert_kernel_gbs": k_gbs, "expert_kernel_frac_of_hbm": k_gbs / hbm_peak,
                           "union_mean": float(np.mean([np.mean(uu) for uu in ub])),
                           "routing_overlap_prev_layer": float(np.mean(overlaps)),
                           "step_ms_p10_p50_p90": [float(np.percentile(ms, q)) for q in (10, 50, 90)]})
+            if B == wl.batches[0]:
+                kernel_b1 = {"bound": "hbm", "achieved": k_gbs, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": k_gbs / hbm_peak, "traffic": None, "traffic_unit": "bytes per launch",
+                             "kernel": f"k_experts of each of the {wl.layers} layers at batch {B}, timed alone",
+                             "algorithmic_bytes_per_launch": bytes_step / wl.layers,
+                             "avg_launch_ms": k_ms / max(k_n, 1), "peak_kind": f"{peak_kind} hbm_gbs"}
     status = coli.get_device_status()
     # end to end at batch 1: pinned host x in, the stack, host out
     B = wl.batches[0]
@@ -562,12 +634,13 @@ def run_sweep(args):
         e2e_s += time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world)
     b1 = per_b[0]
-    line = {
+    rec = {
         "metric": METRIC, "value": b1["tok_s"], "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": b1["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32",
         "data": "synthetic",
         "config": workload_config(wl),
+        "roofline": kernel_b1,
         "sweep": per_b,
         "e2e": {"value": world * n_e2e * B / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": B * wl.hidden * 4,
                 "d2h_bytes_per_step": B * wl.hidden * 4},
@@ -578,10 +651,19 @@ def run_sweep(args):
         "peak_kind": f"{peak_kind} hbm_gbs",
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_line(wl, 2, args.cpu_seconds)
+        rec["cpu_baseline"] = cpu_baseline_line(wl, 2, cpu_seconds, single_thread=False)
+    del layers, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_sweep(args):
+    world, rank, local = _setup(args)
+    line = measure_sweep(args, world, rank, local, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
+        import torch.distributed as dist
         dist.destroy_process_group()
 
 
@@ -598,6 +680,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum oracle time of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sub", default=",".join(SUB_WORKLOADS),
+                    help="with the decode workload: comma-separated sub-records measured in the same run "
+                         f"({', '.join(SUB_WORKLOADS)}), or 'none'")
     args = ap.parse_args()
     big = synth.WORKLOADS[args.workload].n_tok > 64
     if args.steps is None:

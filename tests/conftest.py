@@ -22,3 +22,11 @@ def orc():
 
 def golden_path(name: str) -> str:
     return os.path.join(ROOT, "tests", "golden", name)
+
+
+@pytest.fixture(scope="session")
+def glm_expert_cache():
+    """Oracle-packed experts of the GLM-5.2-shaped layer (weight seed 1),
+    shared by every test module that checks the decode, verify or prefill
+    workloads (about 4.9 GB of host memory once all are packed)."""
+    return {}

@@ -2,8 +2,6 @@
 parity tolerance."""
 from __future__ import annotations
 
-import functools
-
 import numpy as np
 
 import synth
@@ -23,25 +21,37 @@ def oracle_expert(wl: synth.Workload, e: int, layer: int = 0):
 
 
 class OracleLayer:
-    """Lazily packs only the experts a sample touches."""
+    """Lazily packs only the experts a sample touches (several at a time, on
+    a thread pool: the draws and the oracle's C packer release the GIL).
 
-    def __init__(self, wl: synth.Workload, layer: int = 0):
+    ``cache``: an expert cache to share with other instances over the same
+    weights (the decode, verify and prefill workloads share one layer's
+    experts and differ only in the router bias)."""
+
+    def __init__(self, wl: synth.Workload, layer: int = 0, cache: dict | None = None):
         self.wl = wl
         self.layer = layer
         self.W, self.b = synth.router(wl, layer)
-        self.shared = oracle_expert(wl, wl.n_experts, layer)
-        self._cache = {}
+        self._cache = {} if cache is None else cache
+        self.shared = self.expert(wl.n_experts)
 
     def expert(self, e):
         if e not in self._cache:
             self._cache[e] = oracle_expert(self.wl, e, self.layer)
         return self._cache[e]
 
+    def prefetch(self, experts):
+        todo = sorted(set(int(e) for e in experts) - set(self._cache))
+        if todo:
+            for e, v in zip(todo, synth.parallel_map(lambda e: oracle_expert(self.wl, e, self.layer), todo)):
+                self._cache[e] = v
+
     def forward(self, x, intermediates=False):
         import oracle
         wl = self.wl
         idx, _ = oracle.route(x, self.W, self.b, wl.top_k, wl.routed_scale)
         need = set(int(v) for v in idx.ravel())
+        self.prefetch(need)
         w4 = [None] * wl.n_experts
         rs = [None] * wl.n_experts
         for e in need:

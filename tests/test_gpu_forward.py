@@ -130,10 +130,10 @@ def test_hostio_pinned_and_pageable_outputs(coli, tiny, path):
 # GLM-5.2-shaped layer (256 experts + shared, all resident)                    #
 # --------------------------------------------------------------------------- #
 @pytest.fixture(scope="module")
-def glm(coli):
+def glm(coli, glm_expert_cache):
     from synth.device import build_device_layer
     wl = synth.WORKLOADS["decode"]
-    return build_device_layer(wl), OracleLayer(wl)
+    return build_device_layer(wl), OracleLayer(wl, cache=glm_expert_cache)
 
 
 def test_decode_batch1(coli, glm):
@@ -161,27 +161,48 @@ def test_verify_batch4(coli, glm):
         np.testing.assert_array_equal(got, want)
 
 
-def test_prefill_2048_sampled(coli, glm, orc):
-    L, ref = glm
+@pytest.fixture(scope="module")
+def prefill_ref(glm, glm_expert_cache):
+    """The oracle's whole 2048-token prefill forward (Zipf-skewed routing),
+    with every pair's expert output: computed once for the module."""
     wl = synth.WORKLOADS["prefill"]
-    _configure(coli, wl, 2048)
-    W, b = synth.router(wl)
-    bd = _cuda(b)
+    ref = OracleLayer(wl, cache=glm_expert_cache)
     x = synth.activations(wl, 0)
-    got = _forward(coli, L, x, router_b=bd).cpu().numpy()
-    # routing of every token, bit-exact
-    idx, w = coli.dbg_route(_cuda(x), L["router_w"], bd, wl.top_k)
-    ridx, rw = orc.route(x, W, b, wl.top_k, wl.routed_scale)
-    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
-    counts = np.bincount(ridx.ravel(), minlength=wl.n_experts)
+    out, it = ref.forward(x, intermediates=True)
+    return wl, ref, x, out, it
+
+
+@pytest.mark.parametrize("path", ["auto", "gemv"])
+def test_prefill_2048_every_token(coli, glm, prefill_ref, path):
+    """Every one of the 2048 prefill tokens, bit for bit against the oracle:
+    routing, each (token, expert) pair's output y (all routed pairs and every
+    token of the shared expert, i.e. each of its 16 tiles of 128 tokens) and
+    the combined output.  AUTO runs the grouped tensor-core GEMM at this size;
+    the streaming GEMV path is checked on the same batch."""
+    L, _ = glm
+    wl, ref, x, want, it = prefill_ref
+    _configure(coli, wl, 2048)
+    assert coli.auto_uses_gemm(wl.n_tok, wl.top_k, wl.n_experts)
+    coli.set_path(coli.PATH_AUTO if path == "auto" else coli.PATH_GEMV)
+    try:
+        r = coli.dbg_forward_intermediates(_cuda(x), L["router_w"], _cuda(ref.b), L["expert_w4"],
+                                           L["expert_rs"], L["shared_w4"], L["shared_rs"],
+                                           wl.hidden, wl.ffn, wl.top_k)
+        assert coli.get_device_status() == coli.OK
+    finally:
+        coli.set_path(coli.PATH_AUTO)
+    idx = r["idx"].cpu().numpy()
+    np.testing.assert_array_equal(idx, it["idx"])
+    np.testing.assert_array_equal(r["w"].cpu().numpy(), it["w"])
+    counts = np.bincount(idx.ravel(), minlength=wl.n_experts)
     assert counts.max() >= 100, counts.max()          # the Zipf skew is in effect
-    # outputs of sampled tokens (each token's result does not depend on the batch)
-    ref_p = OracleLayer(wl)
-    ref_p._cache = ref._cache
-    sample = [0, 1, 777, 1500, 2046, 2047]
-    want = ref_p.forward(x[sample])
-    assert_float_close(got[sample], want)
-    np.testing.assert_array_equal(got[sample], want)
+    T, k, H = wl.n_tok, wl.top_k, wl.hidden
+    y = r["y"].cpu().numpy()
+    np.testing.assert_array_equal(y[:T * k].reshape(T, k, H), it["y_routed"])
+    np.testing.assert_array_equal(y[T * k:], it["y_shared"])
+    got = r["out"].cpu().numpy()
+    assert_float_close(got, want)
+    np.testing.assert_array_equal(got, want)
 
 
 @pytest.mark.parametrize("path", ["gemv", "gemm"])

@@ -1,8 +1,7 @@
 """Multi-layer decode sweep: 8 stacked GLM-5.2-shaped layers (~39 GB of int4
 experts resident), x <- x + MoE(RMSNorm(x)) between layers, Zipf-skewed routing
-correlated with the previous layer's.  Each layer is checked against the
-oracle fed the GPU's input of that layer, on sampled tokens (a token's
-result does not depend on the rest of the batch)."""
+correlated with the previous layer's.  Every layer is checked against the
+oracle fed the GPU's input of that layer, on every token of the batch."""
 import numpy as np
 import pytest
 import torch
@@ -31,15 +30,15 @@ def test_sweep_stack_matches_oracle_per_layer(stack, B):
     coli, wl, layers = stack
     coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, max(wl.batches))
     x = torch.from_numpy(synth.activations(wl, 3, n_tok=B)).cuda()
-    sample = [0, B - 1]
     for l, L in enumerate(layers):
         out = coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
                                           L["shared_w4"], L["shared_rs"])
         assert coli.get_device_status() == coli.OK
-        xs = x.cpu().numpy()[sample]
-        ref = OracleLayer(wl, layer=l)
+        xs = x.cpu().numpy()
+        ref = OracleLayer(wl, layer=l)     # one layer's experts at a time (host memory)
         want = (xs + ref.forward(oracle.rmsnorm(xs))).astype(np.float32)
-        got = out.cpu().numpy()[sample]
+        del ref
+        got = out.cpu().numpy()
         assert_float_close(got, want, what=f"layer {l}")
-        np.testing.assert_array_equal(got, want)
+        np.testing.assert_array_equal(got, want, err_msg=f"layer {l}")
         x = out
