@@ -104,8 +104,10 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def expert_bytes(wl):
-    return wl.expert_bytes + 4 * wl.expert_scales
+def expert_bytes(wl, wbits=4):
+    """Algorithmic bytes of one expert: its weight container (3*F*H*wbits/8)
+    plus its F32 row scales."""
+    return 3 * wl.ffn * wl.hidden * wbits // 8 + 4 * wl.expert_scales
 
 
 class ClockSampler:
@@ -174,7 +176,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- #
 def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: int = 0,
-                    min_seconds: float = 0.0, threads: int = 0):
+                    min_seconds: float = 0.0, threads: int = 0, wbits: int = 4):
     """Time the CPU oracle on a bounded sample of the workload (forwards of the
     same shape, or the first `max_tokens` tokens of each when that is set: the
     oracle's cost is per token and expert, so a token subset keeps its rate);
@@ -186,12 +188,12 @@ def oracle_baseline(wl, n_forwards: int, seed_base: int = 900000, max_tokens: in
     oracle.build()
     oracle.set_threads(threads)
     try:
-        return _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens, min_seconds)
+        return _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens, min_seconds, wbits)
     finally:
         oracle.set_threads(0)
 
 
-def _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens, min_seconds):
+def _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens, min_seconds, wbits=4):
     xs = [synth.activations(wl, seed_base + i) for i in range(n_forwards)]
     if max_tokens > 0:
         xs = [x[:max_tokens] for x in xs]
@@ -214,7 +216,7 @@ def _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens,
         toks = n_forwards * xs[0].shape[0]
         return toks / dt, oracle.num_threads(), (f"{n_forwards} passes x {xs[0].shape[0]} token(s) through the "
                                                  f"{wl.layers}-layer {wl.name} stack ({dt:.1f} s)")
-    ref = OracleLayer(wl)
+    ref = OracleLayer(wl, wbits=wbits)
     # pack the experts the sample touches before timing (the oracle's converter)
     for x in xs:
         idx, _ = oracle.route(x, ref.W, ref.b, wl.top_k, wl.routed_scale)
@@ -238,12 +240,12 @@ def _oracle_baseline(oracle, OracleLayer, wl, n_forwards, seed_base, max_tokens,
 CPU_SAMPLE_TOKENS = {"prefill": 24, "sweep": 1}   # bounded oracle sample per forward (tokens)
 
 
-def cpu_baseline_line(wl, n_forwards: int, min_seconds: float, single_thread: bool = True):
+def cpu_baseline_line(wl, n_forwards: int, min_seconds: float, single_thread: bool = True, wbits: int = 4):
     """The oracle on all of the host's cores, plus (optionally) a shorter
     single-thread sample, with the host's machine type."""
     import platform
     mt = CPU_SAMPLE_TOKENS.get(wl.name, 0)
-    tps, cores, sample = oracle_baseline(wl, n_forwards, max_tokens=mt, min_seconds=min_seconds)
+    tps, cores, sample = oracle_baseline(wl, n_forwards, max_tokens=mt, min_seconds=min_seconds, wbits=wbits)
     rec = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample,
            "machine": platform.machine()}
     if single_thread:
@@ -279,7 +281,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(wl):
+def workload_config(wl, wbits=4):
     if wl.layers > 1:
         return {"workload": f"{wl.name}: {wl.layers} stacked GLM-5.2-shaped MoE layers (hidden {wl.hidden}, "
                             f"expert FFN {wl.ffn}, {wl.n_experts} experts top-{wl.top_k} + 1 shared), residual "
@@ -292,7 +294,8 @@ def workload_config(wl):
     return {"workload": f"{wl.name}: GLM-5.2-shaped MoE layer, hidden {wl.hidden}, expert FFN {wl.ffn}, "
                         f"{wl.n_experts} routed experts top-{wl.top_k} + 1 shared, {wl.n_tok} token(s) per forward",
             "hidden": wl.hidden, "ffn": wl.ffn, "n_experts": wl.n_experts, "top_k": wl.top_k,
-            "tokens_per_forward": wl.n_tok, "weights": "int4 + F32 row scales, all experts resident in HBM",
+            "tokens_per_forward": wl.n_tok,
+            "weights": f"int{wbits} + F32 row scales, all experts resident in HBM",
             "l2": "flushed between timed steps (512 MiB write, outside the timed region)"}
 
 
@@ -312,16 +315,18 @@ def _setup(args):
     return world, rank, local
 
 
-def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single_thread_cpu=True):
-    """One layer workload on resident weights L (router bias `router_b`):
-    the timed forwards, the dominant kernel timed alone, the end-to-end
-    host-I/O forwards and the CPU oracle sample; returns the record."""
+def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single_thread_cpu=True, wbits=4):
+    """One layer workload on resident weights L (router bias `router_b`;
+    weight container `wbits`): the timed forwards, the dominant kernel timed
+    alone, the end-to-end host-I/O forwards and the CPU oracle sample;
+    returns the record."""
     import torch
 
     import int4_routed_expert_f32_gb300 as coli
 
     T = wl.n_tok
     coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
+    coli.set_weight_bits(wbits)
     path = {"auto": coli.PATH_AUTO, "gemv": coli.PATH_GEMV, "gemm": coli.PATH_GEMM}[args.path]
     coli.set_path(path)
     use_gemm = path == coli.PATH_GEMM or (path == coli.PATH_AUTO and
@@ -402,10 +407,11 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
         e2e_s += time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world)
     coli.set_path(coli.PATH_AUTO)
+    coli.set_weight_bits(4)
 
     hbm_peak, bf16_peak, peak_kind = peaks()
     ub = np.array(unions[args.warmup:], dtype=np.float64)
-    bytes_per_fwd = float(np.mean((ub + 1) * expert_bytes(wl)))
+    bytes_per_fwd = float(np.mean((ub + 1) * expert_bytes(wl, wbits)))
     k_avg_ms = k_ms / max(k_n, 1)
     value = world * args.steps * T / (total_ms * 1e-3)
     # multiply-adds of one forward: (T*k routed + T shared) rows x (2F*H + H*F)
@@ -422,7 +428,7 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
                     "avg_launch_ms": k_avg_ms, "peak_kind": f"{peak_kind} bf16_tflops (burst)"}
     else:
         achieved = bytes_per_fwd / (k_avg_ms * 1e-3) / 1e9
-        traffic = kernel_traffic("k_experts", wl.name)
+        traffic = kernel_traffic("k_experts", wl.name) if wbits == 4 else None
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "traffic": traffic, "traffic_unit": "bytes per launch",
                     "kernel": "k_experts (gate/up + SiLU*up requant + down + combine), timed alone",
@@ -432,8 +438,8 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
     rec = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8->f32", "data": "synthetic",
-        "config": workload_config(wl),
+        "scaling": "weak", "vs_baseline": None, "dtype": f"int{wbits}xint8->f32", "data": "synthetic",
+        "config": workload_config(wl, wbits),
         "roofline": roofline,
         "expert_path": "gemm" if use_gemm else "gemv",
         "weight_gbs_layer": bytes_per_fwd / step_s / 1e9,
@@ -454,12 +460,60 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
                                           "ops_at_bf16_peak": 2.0 * macs_layer / (bf16_peak * 1e12) * 1e3}
     if rank == 0 and not args.no_cpu_baseline:
         nf = args.cpu_forwards if T <= 64 else 1
-        rec["cpu_baseline"] = cpu_baseline_line(wl, nf, cpu_seconds, single_thread=single_thread_cpu)
+        rec["cpu_baseline"] = cpu_baseline_line(wl, nf, cpu_seconds, single_thread=single_thread_cpu, wbits=wbits)
     del xs, out, flush
     return rec
 
 
-SUB_WORKLOADS = ("verify", "prefill", "sweep")
+def measure_tier(args, wl, L, router_b, world, rank, local, n_slots=64):
+    """The decode layer with its routed experts in host memory (page-locked)
+    and an LRU cache of n_slots experts in HBM (coli_moe_tier_forward): every
+    step routes, copies in the experts it misses and runs the expert kernel on
+    the slots.  Reports tok/s, the hit rate and the host-to-HBM copy rate."""
+    import torch
+
+    import int4_routed_expert_f32_gb300 as coli
+
+    T = wl.n_tok
+    coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
+    hw = L["expert_w4"].cpu().pin_memory()
+    hrs = L["expert_rs"].cpu().pin_memory()
+    coli.tier_configure(n_slots)
+    n_total = args.warmup + args.steps
+    xs = torch.from_numpy(np.stack([synth.activations(wl, 50_000 + rank * 100_000 + i)
+                                    for i in range(n_total)])).cuda()
+    out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
+    for i in range(args.warmup):
+        coli.tier_forward(xs[i], L["router_w"], router_b, hw, hrs, L["shared_w4"], L["shared_rs"], out=out)
+    torch.cuda.synchronize()
+    h0, m0, b0, _ = coli.tier_stats()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        for s_ in range(args.steps):
+            coli.tier_forward(xs[args.warmup + s_], L["router_w"], router_b, hw, hrs, L["shared_w4"],
+                              L["shared_rs"], out=out)
+        torch.cuda.synchronize()
+        dt = max_over_ranks(time.perf_counter() - t0, world)
+    h1, m1, b1, res = coli.tier_stats()
+    status = coli.get_device_status()
+    coli.tier_release()
+    hits, misses, nbytes = h1 - h0, m1 - m0, b1 - b0
+    return {"value": world * args.steps * T / dt, "unit": "tok/s", "steps": args.steps,
+            "ms_per_step": dt / args.steps * 1e3,
+            "config": {"workload": f"decode layer (hidden {wl.hidden}, expert FFN {wl.ffn}, {wl.n_experts} experts "
+                                   f"top-{wl.top_k} + 1 shared), routed experts in page-locked host memory, "
+                                   f"LRU cache of {n_slots} experts in HBM, 1 token per forward, fresh activations",
+                       "hbm_slots": n_slots, "host_expert_bytes": int(hw.numel())},
+            "hit_rate": hits / max(hits + misses, 1), "misses_per_step": misses / args.steps,
+            "h2d_gbs": nbytes / dt / 1e9, "h2d_bytes_per_step": nbytes / args.steps,
+            "resident_experts": res, "clocks": clocks.summary(), "device_status": status,
+            "timing": "host wall clock around the steps (each step synchronises once, after routing)"}
+
+
+# sub-records of the default decode run: the verify batch and the prefill on
+# the same resident weights, the decode layer with int8-container experts, the
+# decode layer with its experts in host memory, and the stacked-layer sweep
+SUB_WORKLOADS = ("verify", "prefill", "decode_int8", "tier", "sweep")
 
 
 def run(args):
@@ -487,6 +541,14 @@ def run(args):
                 del L
                 torch.cuda.empty_cache()
                 rec = measure_sweep(args, world, rank, local, args.cpu_seconds / 2)
+            elif name == "tier":
+                rec = measure_tier(args, wl, L, torch.from_numpy(b).cuda(), world, rank, local)
+            elif name == "decode_int8":
+                L8 = build_device_layer(wl, wbits=8)
+                rec = measure_layer(args, wl, L8, torch.from_numpy(b).cuda(), world, rank, local,
+                                    args.cpu_seconds / 2, single_thread_cpu=False, wbits=8)
+                del L8
+                torch.cuda.empty_cache()
             else:
                 swl = synth.WORKLOADS[name]
                 _, sb = synth.router(swl)          # same weights; prefill's bias is Zipf-skewed
@@ -534,7 +596,7 @@ def measure_sweep(args, world, rank, local, cpu_seconds):
                   for i in range(n_in)]
             bufs = [torch.empty((B, wl.hidden), dtype=torch.float32, device="cuda") for _ in range(2)]
 
-            def stack(x0, record_unions=None, record_idx=None):
+            def stack(x0, record_unions=None, record_idx=None, prefetch=True):
                 x = x0
                 for l, L in enumerate(layers):
                     if record_unions is not None:
@@ -545,8 +607,15 @@ def measure_sweep(args, world, rank, local, cpu_seconds):
                         if record_idx is not None:
                             record_idx.append(idx)
                     out = bufs[l & 1]
-                    coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"],
-                                                L["expert_rs"], L["shared_w4"], L["shared_rs"], out=out)
+                    nxt = layers[l + 1] if prefetch and l + 1 < len(layers) else None
+                    if nxt is not None:
+                        # layer-ahead L2 prefetch of the next layer's router and shared expert
+                        coli.layer_forward_residual_prefetch(x, L["router_w"], L["router_b"], L["expert_w4"],
+                                                             L["expert_rs"], L["shared_w4"], L["shared_rs"],
+                                                             nxt["router_w"], nxt["shared_w4"], out=out)
+                    else:
+                        coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"],
+                                                    L["expert_rs"], L["shared_w4"], L["shared_rs"], out=out)
                     x = out
                 return x
 
@@ -591,7 +660,18 @@ def measure_sweep(args, world, rank, local, cpu_seconds):
             coli.timing_enable(False)
             k_ms, k_n = coli.timing_read()
             k_gbs = bytes_step / (k_ms * 1e-3 / max(args.steps, 1)) / 1e9
+            # the same stack without the layer-ahead prefetch, for comparison
+            ev0 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for k in range(args.steps):
+                flush.zero_()
+                ev0[k][0].record(st)
+                stack(xs[k % n_in], prefetch=False)
+                ev0[k][1].record(st)
+            torch.cuda.synchronize()
+            t0 = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev0])), world)
             per_b.append({"batch": B, "ms_per_step": t, "tok_s": world * B / (t * 1e-3),
+                          "tok_s_without_layer_prefetch": world * B / (t0 * 1e-3),
                           "weight_gbs_per_gpu": gbs, "weight_frac_of_hbm": gbs / hbm_peak,
                           "expert_kernel_gbs": k_gbs, "expert_kernel_frac_of_hbm": k_gbs / hbm_peak,
                           "union_mean": float(np.mean([np.mean(uu) for uu in ub])),
@@ -616,8 +696,14 @@ def measure_sweep(args, world, rank, local, cpu_seconds):
         x = x_dev
         for l, L in enumerate(layers):
             out = bufs[l & 1]
-            coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
-                                        L["shared_w4"], L["shared_rs"], out=out)
+            nxt = layers[l + 1] if l + 1 < len(layers) else None
+            if nxt is not None:
+                coli.layer_forward_residual_prefetch(x, L["router_w"], L["router_b"], L["expert_w4"],
+                                                     L["expert_rs"], L["shared_w4"], L["shared_rs"],
+                                                     nxt["router_w"], nxt["shared_w4"], out=out)
+            else:
+                coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                                            L["shared_w4"], L["shared_rs"], out=out)
             x = out
         oh.copy_(x, non_blocking=True)
         torch.cuda.synchronize()

@@ -56,8 +56,11 @@ typedef enum {
     COLI_E_DEVICE = -7     /* device status word reports a bad index          */
 } coli_status;
 
-/* Layer shape.  Limits: hidden % 128 == 0, ffn % 128 == 0, 1 <= top_k <= 16,
- * top_k <= n_experts <= 256, 1 <= max_tok <= 65536, routed_scale finite > 0. */
+/* Layer shape.  Limits: hidden % 128 == 0, ffn % 32 == 0, 1 <= top_k <= 16,
+ * top_k <= n_experts <= 256, 1 <= max_tok <= 65536, routed_scale finite > 0.
+ * The grouped tensor-core path needs ffn % 128 == 0: with another ffn, AUTO
+ * always takes the streaming path and COLI_PATH_GEMM forwards return
+ * COLI_E_UNIMPL. */
 typedef struct {
     int hidden;          /* H: model width                                     */
     int ffn;             /* F: expert FFN width                                */
@@ -115,6 +118,26 @@ int coli_moe_layer_forward_residual(const float *x, int n_tok,
                                     const uint8_t *shared_w4, const float *shared_rowscale,
                                     float *out, void *stream);
 
+/* coli_moe_layer_forward_residual with a layer-ahead prefetch for stacked
+ * decode: while this layer's expert kernel finishes its last units, its
+ * blocks that have run out of work pull the NEXT layer's router weights
+ * (next_router_w, [E][H] F32) and shared expert (next_shared_w4, [3FH/2]
+ * bytes) into L2.  Neither depends on the next layer's routing (the pages'
+ * engine reads ahead asynchronously and reports router choices largely
+ * predictable one layer ahead: "Colibri: an AI engine running a 744B model in
+ * 25GB of RAM" (alphamatch.ai), section "Real performance"; only this
+ * routing-independent part is prefetched here).  Results are identical to
+ * coli_moe_layer_forward_residual.  Either next pointer may be NULL (nothing
+ * of it is prefetched); both must be 16-byte aligned device pointers.  The
+ * prefetch runs on the streaming path only (a prefill-sized batch takes the
+ * grouped GEMM, which ignores them). */
+int coli_moe_layer_forward_residual_prefetch(const float *x, int n_tok,
+                                             const float *router_w, const float *router_bias,
+                                             const uint8_t *expert_w4, const float *expert_rowscale,
+                                             const uint8_t *shared_w4, const float *shared_rowscale,
+                                             const float *next_router_w, const uint8_t *next_shared_w4,
+                                             float *out, void *stream);
+
 /* The same forward with x and out in HOST memory (pinned memory gives
  * asynchronous copies).  Copies x into a library-owned device buffer, runs the
  * forward and synchronises `stream` before returning, so out_host is valid on
@@ -137,7 +160,8 @@ int coli_moe_layer_forward_hostio(const float *x_host, int n_tok,
  * COLI_GEMM_MIN_PAIRS_PER_EXPERT * n_experts, i.e. an average of 7 routed
  * tokens per expert (224 tokens for 256 experts top-8; measured crossover on
  * that shape between 192 and 256).  Returns COLI_E_INVAL for an unknown path.
- * Takes effect at the next forward. */
+ * Takes effect at the next forward; a forward with COLI_PATH_GEMM on a shape
+ * whose ffn % 128 != 0 returns COLI_E_UNIMPL. */
 #define COLI_GEMM_MIN_PAIRS_PER_EXPERT 7
 int coli_moe_set_path(int path, int gemm_min_tokens);
 
@@ -161,6 +185,26 @@ void coli_moe_release(void);
 int coli_moe_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *scale,
                        void *stream);
 
+/* The int8 weight container, on the GPU: w [rows][K] F32 (K % 32 == 0) ->
+ * q [rows][K] int8 codes, scale [rows] F32, s = max|row| / 127 (IEEE
+ * divide), q = clamp(lrintf(w / s), -127, 127); an all-zero row gives s = 0
+ * and codes 0.  The int4 container's rule with 127 in place of 7: the pages
+ * name an int8 container (to which the int4 packing decodes bit-identically)
+ * and an int8 MTP head ("colibri: a pure-C inference engine ..."
+ * (discuss.pytorch.kr), section "Key features"; "Open-source engine that ran
+ * 744B GLM-5.2 ..." (jeff.news), section "MTP is sensitive").  One expert in
+ * this container is gate [F][H], up [F][H], down [H][F] int8 codes back to
+ * back (3*F*H bytes) with the same row scales [2F+H].  Independent of
+ * coli_moe_configure(). */
+int coli_moe_pack_int8(const float *w, int rows, int K, int8_t *q, float *scale, void *stream);
+
+/* Weight container of later forwards: 4 (packed int4, the default) or 8 (the
+ * int8 container of coli_moe_pack_int8; expert_w4 / shared_w4 then point at
+ * 3*F*H bytes per expert).  Everything else is unchanged: Q8_0 activations,
+ * int32 block dots, the same F32 fold and combine, on both expert paths.
+ * Returns COLI_E_INVAL for other values. */
+int coli_moe_set_weight_bits(int bits);
+
 /* Kernel timing for measurement: when enabled, the library records CUDA events
  * around its dominant kernel (the expert gate/up + down matmuls) on the
  * forward's stream.  coli_moe_timing_read() synchronises, returns the summed
@@ -182,6 +226,44 @@ int coli_moe_trace_read(unsigned long long *host, long long capacity, int *block
 
 /* Number of kernels the library launched since the last call (then reset). */
 long long coli_moe_launch_count(void);
+
+/* ---- host-memory expert tier -------------------------------------------------
+ * The pages keep the dense weights in RAM and stream the routed experts from
+ * disk on demand into RAM caches ("colibri: a pure-C inference engine ..."
+ * (discuss.pytorch.kr), section "Core idea: dense in RAM, experts on disk";
+ * "Open-source engine that ran 744B GLM-5.2 ..." (jeff.news), section
+ * "Bottleneck: disk and RAM cache").  This tier is the same idea one level up:
+ * the routed experts live in host memory (page-locked memory, read over the
+ * host link: NVLink-C2C on a Grace host), and an LRU cache of them lives in a
+ * pool of HBM slots.  Each forward routes on the GPU, brings the forward's
+ * chosen experts to the host, copies every one that is not resident into the
+ * least recently used slot not taken by this forward, and runs the expert
+ * kernels on the slots.  The shared expert and the router stay in HBM.
+ *
+ * coli_moe_tier_configure(n_slots): after coli_moe_configure() (and
+ *   coli_moe_set_weight_bits()): allocate n_slots HBM expert slots
+ *   (1 <= n_slots <= n_experts; replaces an earlier tier).  COLI_E_NOMEM if
+ *   the pool cannot be allocated.  coli_moe_configure() and
+ *   coli_moe_release() free the tier.
+ * coli_moe_tier_forward(): coli_moe_layer_forward's arguments, with the
+ *   routed experts' weights and row scales in HOST memory:
+ *   host_expert_w [E][3FH*bits/8], host_expert_rowscale [E][2F+H]
+ *   (page-locked memory gives asynchronous copies).  Synchronises `stream`
+ *   once, after routing, to read the choices; the expert launches follow
+ *   asynchronously.  COLI_E_INVAL if one forward's union of experts exceeds
+ *   the slots (before any copy or expert launch), or if the weight bits
+ *   changed since the tier was configured.  Results are identical to
+ *   coli_moe_layer_forward with the same weights in HBM.
+ * coli_moe_tier_stats(): cumulative hits and misses (experts found resident
+ *   or copied in), bytes copied to HBM, and the number of resident experts
+ *   (any pointer may be NULL).
+ * coli_moe_tier_release(): free the pool. */
+int coli_moe_tier_configure(int n_slots);
+int coli_moe_tier_forward(const float *x, int n_tok, const float *router_w, const float *router_bias,
+                          const uint8_t *host_expert_w, const float *host_expert_rowscale,
+                          const uint8_t *shared_w4, const float *shared_rowscale, float *out, void *stream);
+int coli_moe_tier_stats(long long *hits, long long *misses, long long *bytes_h2d, int *resident);
+void coli_moe_tier_release(void);
 
 /* ---- routing without any device allocation --------------------------------
  * This entry point has no counterpart in the colibri pages: it is a service
@@ -212,6 +294,36 @@ int coli_moe_route_noalloc(const coli_moe_shape *s, const float *x, int n_tok,
                            const float *router_w, const float *router_bias, int32_t *idx, float *w,
                            void *stream);
 
+/* ---- failure injection (tests) -------------------------------------------
+ * Makes the library's own failure paths run without faulting or hanging the
+ * GPU: every injected failure is decided on the host, or is a device-side wait
+ * with a short bound that a test makes run out.  The pages' engine guards its
+ * own resources the same way (it sizes its caches from MemAvailable so that
+ * it never runs out of memory: "colibri: a pure-C inference engine ..."
+ * (discuss.pytorch.kr), section "Core idea"); this library reports each
+ * failure as a status and stays usable afterwards.
+ *   COLI_INJECT_NONE          clear every injection (arg ignored)
+ *   COLI_INJECT_ALLOC_FAIL    the next `arg` workspace allocations of
+ *                             coli_moe_configure fail as if cudaMalloc had:
+ *                             it returns COLI_E_NOMEM and leaves the library
+ *                             unconfigured (no cudaMalloc is called)
+ *   COLI_INJECT_LAUNCH_FAIL   the `arg`-th kernel launch from now (1 = the
+ *                             next) is skipped and reported as a launch
+ *                             failure: the call returns COLI_E_CUDA
+ *   COLI_INJECT_WAIT_TIMEOUT  in the next streaming-path forward every down
+ *                             unit waits for one more gate/up unit than its
+ *                             tile has, with a bound of `arg` microseconds
+ *                             instead of 2 s: each wait runs out, the
+ *                             forward completes, and
+ *                             coli_moe_get_device_status() then returns
+ *                             COLI_E_TIMEOUT
+ * 0 <= arg <= 1000000.  Returns COLI_E_INVAL for an unknown kind. */
+#define COLI_INJECT_NONE 0
+#define COLI_INJECT_ALLOC_FAIL 1
+#define COLI_INJECT_LAUNCH_FAIL 2
+#define COLI_INJECT_WAIT_TIMEOUT 3
+int coli_moe_dbg_inject(int what, long long arg);
+
 /* ---- stage entry points (tests; same conventions, configured shape) ------- */
 
 /* Q8_0 of n floats (n % 32 == 0): q [n] int8, d [n/32] F32 (same rule as the
@@ -237,6 +349,10 @@ int coli_moe_dbg_dispatch(const int32_t *idx, int n_tok, int32_t *counts, int32_
  * (K % 32 == 0) with one int8 vector q [K]: I_out [rows][K/32]. */
 int coli_moe_dbg_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q,
                             int32_t *I_out, void *stream);
+
+/* The same for rows of the int8 container: w8 [rows][K] int8 codes. */
+int coli_moe_dbg_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *q, int32_t *I_out,
+                               void *stream);
 
 /* Run a full forward and copy out its intermediates (any pointer may be NULL):
  * qx [n_tok][H] int8, dx [n_tok][H/32], idx/w [n_tok][k],

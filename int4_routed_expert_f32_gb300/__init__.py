@@ -39,8 +39,12 @@ EXPORTS = (
     "coli_moe_dbg_quantize", "coli_moe_dbg_route",
     "coli_moe_dbg_dispatch", "coli_moe_dbg_rmsnorm", "coli_moe_dbg_block_dots",
     "coli_moe_dbg_forward_intermediates",
-    "coli_moe_dbg_expert_hidden", "coli_moe_route_noalloc",
+    "coli_moe_dbg_expert_hidden", "coli_moe_route_noalloc", "coli_moe_dbg_inject",
+    "coli_moe_layer_forward_residual_prefetch", "coli_moe_pack_int8", "coli_moe_set_weight_bits",
+    "coli_moe_dbg_block_dots_w8", "coli_moe_tier_configure", "coli_moe_tier_forward", "coli_moe_tier_stats",
+    "coli_moe_tier_release",
 )
+INJECT_NONE, INJECT_ALLOC_FAIL, INJECT_LAUNCH_FAIL, INJECT_WAIT_TIMEOUT = 0, 1, 2, 3
 
 
 class ColiError(RuntimeError):
@@ -86,6 +90,15 @@ def _load():
         "coli_moe_dbg_forward_intermediates": ([P, i, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P], i),
         "coli_moe_dbg_expert_hidden": ([P, P, P, P, i, P, P, P, P], i),
         "coli_moe_route_noalloc": ([ctypes.POINTER(_Shape), P, i, P, P, P, P, P], i),
+        "coli_moe_dbg_inject": ([i, ctypes.c_longlong], i),
+        "coli_moe_layer_forward_residual_prefetch": ([P, i, P, P, P, P, P, P, P, P, P, P], i),
+        "coli_moe_pack_int8": ([P, i, i, P, P, P], i),
+        "coli_moe_set_weight_bits": ([i], i),
+        "coli_moe_dbg_block_dots_w8": ([P, i, i, P, P, P], i),
+        "coli_moe_tier_configure": ([i], i),
+        "coli_moe_tier_forward": ([P, i, P, P, P, P, P, P, P, P], i),
+        "coli_moe_tier_stats": ([ctypes.POINTER(ctypes.c_longlong)] * 3 + [ctypes.POINTER(ctypes.c_int)], i),
+        "coli_moe_tier_release": ([], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -177,6 +190,54 @@ def layer_forward_residual(x, router_w, router_bias, expert_w4, expert_rowscale,
     return out
 
 
+def layer_forward_residual_prefetch(x, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                                    shared_rowscale, next_router_w=None, next_shared_w4=None, out=None,
+                                    stream=None):
+    """layer_forward_residual, plus an L2 prefetch of the next layer's router
+    weights and shared expert during this layer's expert-kernel tail."""
+    if out is None:
+        out = torch.empty_like(x)
+    n_tok = x.shape[0] if x.dim() == 2 else 0
+    _check(_lib.coli_moe_layer_forward_residual_prefetch(
+        _ptr(x), n_tok, _ptr(router_w), _ptr(router_bias), _ptr(expert_w4), _ptr(expert_rowscale),
+        _ptr(shared_w4), _ptr(shared_rowscale), _ptr(next_router_w), _ptr(next_shared_w4), _ptr(out),
+        _stream(stream)), "layer_forward_residual_prefetch")
+    return out
+
+
+def tier_configure(n_slots: int):
+    """Host-memory expert tier: an LRU cache of n_slots experts in HBM."""
+    _check(_lib.coli_moe_tier_configure(int(n_slots)), "tier_configure")
+
+
+def tier_forward(x, router_w, router_bias, host_expert_w, host_expert_rowscale, shared_w4, shared_rowscale,
+                 out=None, stream=None):
+    """The layer forward with the routed experts in host memory (host tensors,
+    pinned for asynchronous copies); x, the router and the shared expert on
+    the device."""
+    if out is None:
+        out = torch.empty_like(x)
+    n_tok = x.shape[0] if x.dim() == 2 else 0
+    _check(_lib.coli_moe_tier_forward(_ptr(x), n_tok, _ptr(router_w), _ptr(router_bias),
+                                      _host_ptr(host_expert_w), _host_ptr(host_expert_rowscale),
+                                      _ptr(shared_w4), _ptr(shared_rowscale), _ptr(out), _stream(stream)),
+           "tier_forward")
+    return out
+
+
+def tier_stats():
+    """(hits, misses, bytes copied to HBM, resident experts)."""
+    h, m, b = ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_longlong(0)
+    r = ctypes.c_int(0)
+    _check(_lib.coli_moe_tier_stats(ctypes.byref(h), ctypes.byref(m), ctypes.byref(b), ctypes.byref(r)),
+           "tier_stats")
+    return h.value, m.value, b.value, r.value
+
+
+def tier_release():
+    _lib.coli_moe_tier_release()
+
+
 def layer_forward_hostio(x_host, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
                          shared_rowscale, out_host, stream=None):
     _check(_lib.coli_moe_layer_forward_hostio(_host_ptr(x_host), x_host.shape[0], _ptr(router_w),
@@ -201,6 +262,22 @@ def pack_int4(w, packed=None, scale=None, stream=None):
     _check(_lib.coli_moe_pack_int4(_ptr(w), rows, K, _ptr(packed), _ptr(scale), _stream(stream)),
            "pack_int4")
     return packed, scale
+
+
+def pack_int8(w, q=None, scale=None, stream=None):
+    """The int8 weight container: F32 rows [rows][K] -> (int8 codes, scales)."""
+    rows, K = w.shape
+    if q is None:
+        q = torch.empty((rows, K), dtype=torch.int8, device=w.device)
+    if scale is None:
+        scale = torch.empty((rows,), dtype=torch.float32, device=w.device)
+    _check(_lib.coli_moe_pack_int8(_ptr(w), rows, K, _ptr(q), _ptr(scale), _stream(stream)), "pack_int8")
+    return q, scale
+
+
+def set_weight_bits(bits: int):
+    """Weight container of later forwards: 4 (packed int4) or 8 (int8 codes)."""
+    _check(_lib.coli_moe_set_weight_bits(int(bits)), "set_weight_bits")
 
 
 def timing_enable(on: bool = True):
@@ -270,6 +347,13 @@ def route_noalloc(x, router_w, router_bias, hidden, n_experts, top_k, routed_sca
     return idx, w
 
 
+def dbg_inject(what: int, arg: int = 0):
+    """Failure injection for tests (see the header): INJECT_ALLOC_FAIL,
+    INJECT_LAUNCH_FAIL, INJECT_WAIT_TIMEOUT (arg in microseconds) or
+    INJECT_NONE to clear."""
+    _check(_lib.coli_moe_dbg_inject(int(what), int(arg)), "dbg_inject")
+
+
 # ---- stage entry points ---------------------------------------------------- #
 def dbg_quantize(x, stream=None):
     n = x.numel()
@@ -307,6 +391,14 @@ def dbg_block_dots(w4, q, stream=None):
     I = torch.empty((rows, 2 * K2 // 32), dtype=torch.int32, device=w4.device)
     _check(_lib.coli_moe_dbg_block_dots(_ptr(w4), rows, 2 * K2, _ptr(q), _ptr(I), _stream(stream)),
            "dbg_block_dots")
+    return I
+
+
+def dbg_block_dots_w8(w8, q, stream=None):
+    rows, K = w8.shape
+    I = torch.empty((rows, K // 32), dtype=torch.int32, device=w8.device)
+    _check(_lib.coli_moe_dbg_block_dots_w8(_ptr(w8), rows, K, _ptr(q), _ptr(I), _stream(stream)),
+           "dbg_block_dots_w8")
     return I
 
 

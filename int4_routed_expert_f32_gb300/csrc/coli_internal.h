@@ -22,7 +22,8 @@ struct ExpertArgs {
     int H, F, E, k;
     int n_tok;                      // T
     int P;                          // T * k (routed pairs); shared rows follow at P + t
-    int KC;                         // bytes of a weight row per pipeline stage (128 or 64)
+    int KC;                         // bytes of a weight row per TMA box (128, 64, 32 or 16)
+    int wbits;                      // weight container: 4 (packed int4) or 8 (int8 codes)
     int nstage;                     // ring depth (set by the launcher)
     int gate_up_only;               // 1: stop after h (stage tests)
     const float *expert_rs;         // [E][2F+H]
@@ -52,12 +53,22 @@ struct ExpertArgs {
     int *status;
     unsigned long long *trace;      // optional per-block event log (null: off)
     int trace_cap;                  // events per block
+    unsigned long long wait_ns;     // bound of a down unit's wait for its tile's gate/up units
+    int gdone_extra;                // test injection: added to the gate/up count that wait needs (0)
+    // layer-ahead L2 prefetch (stacked decode): the next layer's router
+    // weights and shared expert, pulled into L2 by blocks that ran out of units
+    const unsigned char *next_rw;   // null: none
+    size_t next_rw_bytes;
+    const unsigned char *next_sw;   // null: none
+    size_t next_sw_bytes;
+    const int32_t *slot_of;         // optional [E]: routed expert e lives at index slot_of[e] of
+                                    // expert_w4 / expert_rs (host-memory tier); null: at index e
 };
 
 // Tensor maps of one grouped-GEMM launch: the bf16 activation codes by
 // dispatch position (2-D, box 64 x 128, 128-byte swizzle) and the packed
-// weight rows of the routed experts and of the shared expert (3-D, box
-// 32 bytes x 128 or 256 rows x 1, no swizzle).
+// weight rows of the routed experts and of the shared expert (3-D, box of 64
+// weights' bytes x 128 or 256 rows x 1, no swizzle).
 struct GemmMaps {
     CUtensorMap act;
     CUtensorMap w;
@@ -81,6 +92,7 @@ struct GemmArgs {
     float *h_dbg;                    // optional [P+T][F]
     float *y;                        // [P+T][H]
     int *status;
+    const int32_t *slot_of;          // optional [E]: index of routed expert e in the weight arrays
     unsigned long long *trace;       // optional per-block stage log (null: off)
     int trace_cap;                   // events per block (four roles, a quarter each)
 };
@@ -116,7 +128,9 @@ int launch_q8_0(const float *x, long n, int8_t *q, float *d, cudaStream_t st);
 constexpr float RMSNORM_EPS = 1e-6f;
 int launch_rmsnorm(const float *x, int T, int H, float eps, float *xn, cudaStream_t st);
 int launch_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *scale, cudaStream_t st);
+int launch_pack_int8(const float *w, int rows, int K, int8_t *q, float *scale, cudaStream_t st);
 int launch_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q, int32_t *I, cudaStream_t st);
+int launch_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *q, int32_t *I, cudaStream_t st);
 
 int launch_router_logits(const float *x, int T, int H, const float *W, int E, float *logits,
                          cudaStream_t st);
@@ -149,7 +163,7 @@ int launch_gather_x(const int8_t *qx, const int32_t *pos_token, const int32_t *o
                     int T, int H, uint16_t *xg, int *status, cudaStream_t st);
 int launch_gemm_items(const int32_t *counts, const int32_t *offsets, int E, int T, int P, int32_t *item_expert,
                       int32_t *item_pos0, int32_t *item_m, int32_t *n_items, cudaStream_t st);
-int launch_gemm(bool gateup, const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st);
+int launch_gemm(bool gateup, int wbits, const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st);
 int launch_combine(const float *y, const int32_t *inv, const float *wts, int T, int k, int P, int H,
                    const float *res, float *out, cudaStream_t st);
 

@@ -71,15 +71,68 @@ struct State {
     // tensor maps of the last weights seen (re-encoded when a pointer changes)
     ExpertMaps maps{};
     const void *maps_key[2] = {nullptr, nullptr};
+    int maps_wbits = 0;
+    int maps_extent = 0;
     bool maps_valid = false;
-    // grouped-GEMM maps: activations (fixed workspace buffers) and weights
+    int wbits = 4;                   // weight container of later forwards (coli_moe_set_weight_bits)
+    // grouped-GEMM maps: activations (fixed workspace buffers, encoded at
+    // configure) and weights (re-encoded when a pointer, the weight
+    // container or the weight array's extent changes)
     CUtensorMap act_x{}, act_h{};
     GemmMaps gemm_gu{}, gemm_dn{};
     const void *gemm_key[2] = {nullptr, nullptr};
+    int gemm_wbits = 0;
+    int gemm_extent = 0;
     bool gemm_valid = false;
 };
 
 static State g;
+
+// Host-memory expert tier: routed experts live in host memory; an LRU cache
+// of them lives in a pool of HBM slots (coli_moe_tier_*).
+struct Tier {
+    int n_slots = 0;
+    int E = 0;
+    int wbits = 4;
+    size_t stride = 0;               // bytes of one expert's weights
+    size_t rs_len = 0;               // row scales of one expert (2F + H)
+    uint8_t *pool_w = nullptr;       // device [n_slots][stride]
+    float *pool_rs = nullptr;        // device [n_slots][rs_len]
+    int32_t *slot_dev = nullptr;     // device [E]: slot of each expert (valid for the forward's experts)
+    int32_t *slot_host = nullptr;    // pinned [E]
+    int32_t *idx_host = nullptr;     // pinned [max_tok * k]
+    std::vector<int> slot_of;        // [E]: -1 when not resident
+    std::vector<int> expert_in;      // [n_slots]: -1 when empty
+    std::vector<long long> stamp;    // [n_slots]: last forward that used the slot (LRU)
+    long long clock = 0, hits = 0, misses = 0, bytes = 0;
+};
+static Tier g_tier;
+
+static void tier_free()
+{
+    if (g_tier.pool_w) cudaFree(g_tier.pool_w);
+    if (g_tier.pool_rs) cudaFree(g_tier.pool_rs);
+    if (g_tier.slot_dev) cudaFree(g_tier.slot_dev);
+    if (g_tier.slot_host) cudaFreeHost(g_tier.slot_host);
+    if (g_tier.idx_host) cudaFreeHost(g_tier.idx_host);
+    g_tier = Tier{};
+}
+
+// Test-only failure injection (coli_moe_dbg_inject): host-side counters, so
+// that nothing ever faults or hangs the GPU.
+struct Inject {
+    int alloc_fail = 0;          // workspace allocations that fail (no cudaMalloc call)
+    int launch_fail_at = 0;      // the n-th launch from now reports failure (0: off)
+    long long wait_us = 0;       // next streaming forward: unreachable gate/up wait, bound in us
+};
+static Inject g_inj;
+
+// True when the injected launch failure is due now (the launch is skipped).
+static bool inject_launch_failure()
+{
+    if (g_inj.launch_fail_at <= 0) return false;
+    return --g_inj.launch_fail_at == 0;
+}
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -96,11 +149,12 @@ static int cuda_fail(cudaError_t e)
         if (e_ != cudaSuccess) return cuda_fail(e_);   \
     } while (0)
 
-#define LAUNCH_OK(call)                                        \
-    do {                                                       \
-        if ((call) != 0) return cuda_fail(cudaErrorUnknown);   \
-        cudaError_t e_ = cudaGetLastError();                   \
-        if (e_ != cudaSuccess) return cuda_fail(e_);           \
+#define LAUNCH_OK(call)                                                        \
+    do {                                                                       \
+        if (inject_launch_failure()) return cuda_fail(cudaErrorLaunchFailure); \
+        if ((call) != 0) return cuda_fail(cudaErrorUnknown);                   \
+        cudaError_t e_ = cudaGetLastError();                                   \
+        if (e_ != cudaSuccess) return cuda_fail(e_);                           \
     } while (0)
 
 static void free_workspace()
@@ -136,8 +190,23 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Bytes of a weight row moved per pipeline stage.
-static int stage_kc(int H, int F) { return ((H / 2) % 128 == 0 && (F / 2) % 128 == 0) ? 128 : 64; }
+// Bytes of a weight row per TMA box of the streaming kernel: the widest of
+// 128 (128-byte swizzled boxes), 64, 32 and 16 that divides both row lengths
+// in bytes (H * wbits / 8 and F * wbits / 8; H % 128 == 0 and F % 32 == 0).
+// The kernel is instantiated for 128, 64 and 16 with int4 weights (F / 2 is a
+// multiple of 16, and of 32 only when it is one of 64) and for 128, 64 and 32
+// with int8 weights.
+static int stage_kc(int H, int F, int wbits)
+{
+    const int rh = H * wbits / 8, rf = F * wbits / 8;
+    if (rh % 128 == 0 && rf % 128 == 0) return 128;
+    if (rf % 64 == 0) return 64;
+    return wbits == 8 ? 32 : 16;
+}
+
+// The grouped GEMM's tiles need F % 128 == 0 (gate/up tiles of 128 hidden
+// units; the down GEMM's K = F in stages of 64).
+static bool gemm_shape_ok(int F) { return F % 128 == 0; }
 
 // rows of `row_bytes` bytes, `n_exp` experts `exp_stride` bytes apart; box =
 // kc bytes x box_rows rows of one expert
@@ -160,21 +229,25 @@ static bool encode_rows(CUtensorMap *m, const void *base, uint64_t row_bytes, ui
 // Maps for routed experts at `ew4` ([E][3FH/2]) and the shared expert at `sw4`.
 static bool expert_maps(const uint8_t *ew4, int E, const uint8_t *sw4, ExpertMaps *out)
 {
-    if (g.maps_valid && g.maps_key[0] == ew4 && g.maps_key[1] == sw4) {
+    if (g.maps_valid && g.maps_key[0] == ew4 && g.maps_key[1] == sw4 && g.maps_wbits == g.wbits &&
+        g.maps_extent == E) {
         *out = g.maps;
         return true;
     }
-    const uint64_t H = g.s.hidden, F = g.s.ffn, stride = 3 * F * H / 2;
-    const uint32_t kc = (uint32_t)stage_kc((int)H, (int)F);
+    const uint64_t H = g.s.hidden, F = g.s.ffn, wb = (uint64_t)g.wbits;
+    const uint64_t rh = H * wb / 8, rf = F * wb / 8, stride = 3 * F * H * wb / 8;
+    const uint32_t kc = (uint32_t)stage_kc((int)H, (int)F, g.wbits);
     ExpertMaps m;
-    bool ok = encode_rows(&m.gu, ew4, H / 2, 2 * F, (uint64_t)E, stride, 32, kc) &&
-              encode_rows(&m.dn, ew4 + F * H, F / 2, H, (uint64_t)E, stride, 64, kc) &&
-              encode_rows(&m.sgu, sw4, H / 2, 2 * F, 1, stride, 32, kc) &&
-              encode_rows(&m.sdn, sw4 + F * H, F / 2, H, 1, stride, 64, kc);
+    bool ok = encode_rows(&m.gu, ew4, rh, 2 * F, (uint64_t)E, stride, 32, kc) &&
+              encode_rows(&m.dn, ew4 + 2 * F * rh, rf, H, (uint64_t)E, stride, 64, kc) &&
+              encode_rows(&m.sgu, sw4, rh, 2 * F, 1, stride, 32, kc) &&
+              encode_rows(&m.sdn, sw4 + 2 * F * rh, rf, H, 1, stride, 64, kc);
     if (!ok) return false;
     g.maps = m;
     g.maps_key[0] = ew4;
     g.maps_key[1] = sw4;
+    g.maps_wbits = g.wbits;
+    g.maps_extent = E;
     g.maps_valid = true;
     *out = m;
     return true;
@@ -195,25 +268,35 @@ static bool encode_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t ro
     return r == CUDA_SUCCESS;
 }
 
-// Weight maps of the grouped GEMM: 32 bytes (64 weights) of a row per stage,
-// 128 rows per box for gate/up (two boxes: gate rows, then the matching up
-// rows), 256 rows for down (rows past the matrix read as zeros).
+// Weight maps of the grouped GEMM: the packed bytes of 64 weights of a row
+// per stage (32 for int4, 64 for int8), 128 rows per box for gate/up (two
+// boxes: gate rows, then the matching up rows), 256 rows for down (rows past
+// the matrix read as zeros).  `E` is the extent of the routed-weight array.
 static bool gemm_weight_maps(const uint8_t *ew4, int E, const uint8_t *sw4)
 {
-    if (g.gemm_valid && g.gemm_key[0] == ew4 && g.gemm_key[1] == sw4) return true;
-    const uint64_t H = g.s.hidden, F = g.s.ffn, stride = 3 * F * H / 2;
+    if (g.gemm_valid && g.gemm_key[0] == ew4 && g.gemm_key[1] == sw4 && g.gemm_wbits == g.wbits &&
+        g.gemm_extent == E)
+        return true;
+    const uint64_t H = g.s.hidden, F = g.s.ffn, wb = (uint64_t)g.wbits;
+    const uint64_t rh = H * wb / 8, rf = F * wb / 8, stride = 3 * F * H * wb / 8;
+    const uint32_t rb = (uint32_t)(64 * wb / 8);
     GemmMaps gu{}, dn{};
-    bool ok = encode_rows(&gu.w, ew4, H / 2, 2 * F, (uint64_t)E, stride, 128, 32) &&
-              encode_rows(&gu.sw, sw4, H / 2, 2 * F, 1, stride, 128, 32) &&
-              encode_rows(&dn.w, ew4 + F * H, F / 2, H, (uint64_t)E, stride, 256, 32) &&
-              encode_rows(&dn.sw, sw4 + F * H, F / 2, H, 1, stride, 256, 32);
-    if (!ok) return false;
+    bool ok = encode_rows(&gu.w, ew4, rh, 2 * F, (uint64_t)E, stride, 128, rb) &&
+              encode_rows(&gu.sw, sw4, rh, 2 * F, 1, stride, 128, rb) &&
+              encode_rows(&dn.w, ew4 + 2 * F * rh, rf, H, (uint64_t)E, stride, 256, rb) &&
+              encode_rows(&dn.sw, sw4 + 2 * F * rh, rf, H, 1, stride, 256, rb);
+    if (!ok) {
+        g.gemm_valid = false;
+        return false;
+    }
     gu.act = g.act_x;
     dn.act = g.act_h;
     g.gemm_gu = gu;
     g.gemm_dn = dn;
     g.gemm_key[0] = ew4;
     g.gemm_key[1] = sw4;
+    g.gemm_wbits = g.wbits;
+    g.gemm_extent = E;
     g.gemm_valid = true;
     return true;
 }
@@ -222,7 +305,7 @@ static int check_shape(const coli_moe_shape *s)
 {
     if (!s) return COLI_E_INVAL;
     if (s->hidden <= 0 || s->hidden % 128 != 0 || s->hidden > 16384) return COLI_E_INVAL;
-    if (s->ffn <= 0 || s->ffn % 128 != 0 || s->ffn > 16384) return COLI_E_INVAL;
+    if (s->ffn <= 0 || s->ffn % 32 != 0 || s->ffn > 16384) return COLI_E_INVAL;
     if (s->n_experts < 1 || s->n_experts > 256) return COLI_E_INVAL;
     if (s->top_k < 1 || s->top_k > 16 || s->top_k > s->n_experts) return COLI_E_INVAL;
     if (s->max_tok < 1 || s->max_tok > 65536) return COLI_E_INVAL;
@@ -253,9 +336,66 @@ const char *coli_moe_strerror(int code)
 
 void coli_moe_release(void)
 {
-    if (g.ws.base) cudaDeviceSynchronize();
+    if (g.ws.base || g_tier.pool_w) cudaDeviceSynchronize();
+    tier_free();
     free_workspace();
     g.configured = false;
+}
+
+void coli_moe_tier_release(void)
+{
+    if (g_tier.pool_w) cudaDeviceSynchronize();
+    tier_free();
+}
+
+int coli_moe_tier_configure(int n_slots)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    if (n_slots < 1 || n_slots > g.s.n_experts) return COLI_E_INVAL;
+    coli_moe_tier_release();
+    const coli_moe_shape &s = g.s;
+    Tier t;
+    t.n_slots = n_slots;
+    t.E = s.n_experts;
+    t.wbits = g.wbits;
+    t.stride = (size_t)3 * s.ffn * s.hidden * g.wbits / 8;
+    t.rs_len = (size_t)2 * s.ffn + s.hidden;
+    const size_t n_idx = (size_t)s.max_tok * s.top_k;
+    bool ok = cudaMalloc(&t.pool_w, t.stride * n_slots) == cudaSuccess &&
+              cudaMalloc(&t.pool_rs, t.rs_len * sizeof(float) * n_slots) == cudaSuccess &&
+              cudaMalloc(&t.slot_dev, sizeof(int32_t) * t.E) == cudaSuccess &&
+              cudaMallocHost(&t.slot_host, sizeof(int32_t) * t.E) == cudaSuccess &&
+              cudaMallocHost(&t.idx_host, sizeof(int32_t) * n_idx) == cudaSuccess;
+    if (!ok) {
+        (void)cudaGetLastError();
+        g_tier = t;
+        tier_free();
+        return COLI_E_NOMEM;
+    }
+    if (cudaMemset(t.slot_dev, 0, sizeof(int32_t) * t.E) != cudaSuccess) {
+        g_tier = t;
+        tier_free();
+        return cuda_fail(cudaErrorUnknown);
+    }
+    t.slot_of.assign(t.E, -1);
+    t.expert_in.assign(n_slots, -1);
+    t.stamp.assign(n_slots, -1);
+    g_tier = std::move(t);
+    return COLI_OK;
+}
+
+int coli_moe_tier_stats(long long *hits, long long *misses, long long *bytes_h2d, int *resident)
+{
+    if (!g_tier.pool_w) return COLI_E_NOSHAPE;
+    if (hits) *hits = g_tier.hits;
+    if (misses) *misses = g_tier.misses;
+    if (bytes_h2d) *bytes_h2d = g_tier.bytes;
+    if (resident) {
+        int n = 0;
+        for (int e : g_tier.expert_in) n += e >= 0;
+        *resident = n;
+    }
+    return COLI_OK;
 }
 
 int coli_moe_configure(const coli_moe_shape *s)
@@ -313,6 +453,10 @@ int coli_moe_configure(const coli_moe_shape *s)
     size_t total = 0;
     for (auto &p : pieces) total += align_up(p.bytes, 256);
     void *base = nullptr;
+    if (g_inj.alloc_fail > 0) {
+        --g_inj.alloc_fail;        // injected: behave as a failed cudaMalloc
+        return COLI_E_NOMEM;
+    }
     if (cudaMalloc(&base, total) != cudaSuccess) {
         (void)cudaGetLastError();
         return COLI_E_NOMEM;
@@ -331,7 +475,7 @@ int coli_moe_configure(const coli_moe_shape *s)
     CUDA_OK(cudaDeviceSynchronize());
     w.n_sync = (int)(tiles + H / 64 + 2);
     w.rows_alloc = (int)Ra;
-    if (!encode_act(&g.act_x, w.xg, H, Ra) || !encode_act(&g.act_h, w.qhb, F, Ra)) {
+    if (gemm_shape_ok((int)F) && (!encode_act(&g.act_x, w.xg, H, Ra) || !encode_act(&g.act_h, w.qhb, F, Ra))) {
         cudaFree(base);
         return COLI_E_CUDA;
     }
@@ -344,6 +488,29 @@ int coli_moe_configure(const coli_moe_shape *s)
     g.num_sms = sms;
     g.configured = true;
     return COLI_OK;
+}
+
+int coli_moe_dbg_inject(int what, long long arg)
+{
+    switch (what) {
+    case COLI_INJECT_NONE:
+        g_inj = Inject{};
+        return COLI_OK;
+    case COLI_INJECT_ALLOC_FAIL:
+        if (arg < 0 || arg > 1000000) return COLI_E_INVAL;
+        g_inj.alloc_fail = (int)arg;
+        return COLI_OK;
+    case COLI_INJECT_LAUNCH_FAIL:
+        if (arg < 0 || arg > 1000000) return COLI_E_INVAL;
+        g_inj.launch_fail_at = (int)arg;
+        return COLI_OK;
+    case COLI_INJECT_WAIT_TIMEOUT:
+        if (arg < 0 || arg > 1000000) return COLI_E_INVAL;
+        g_inj.wait_us = arg;
+        return COLI_OK;
+    default:
+        return COLI_E_INVAL;
+    }
 }
 
 int coli_moe_set_path(int path, int gemm_min_tokens)
@@ -458,6 +625,36 @@ int coli_moe_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *
     return COLI_OK;
 }
 
+int coli_moe_pack_int8(const float *w, int rows, int K, int8_t *q, float *scale, void *stream)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0) return COLI_E_INVAL;
+    if (rows == 0) return COLI_OK;
+    if (!w || !q || !scale) return COLI_E_INVAL;
+    LAUNCH_OK(launch_pack_int8(w, rows, K, q, scale, (cudaStream_t)stream));
+    return COLI_OK;
+}
+
+int coli_moe_set_weight_bits(int bits)
+{
+    if (bits != 4 && bits != 8) return COLI_E_INVAL;
+    if (bits != g.wbits) {
+        g.wbits = bits;
+        g.maps_valid = false;
+        g.gemm_valid = false;
+    }
+    return COLI_OK;
+}
+
+int coli_moe_dbg_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *q, int32_t *I_out,
+                               void *stream)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0) return COLI_E_INVAL;
+    if (rows == 0) return COLI_OK;
+    if (!w8 || !q || !I_out || !aligned16(w8) || !aligned16(q)) return COLI_E_INVAL;
+    LAUNCH_OK(launch_block_dots_w8(w8, rows, K, q, I_out, (cudaStream_t)stream));
+    return COLI_OK;
+}
+
 int coli_moe_dbg_quantize(const float *x, int n, int8_t *q, float *d, void *stream)
 {
     if (n < 0 || n % 32 != 0) return COLI_E_INVAL;
@@ -534,7 +731,8 @@ static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *
     ExpertArgs a{};
     a.H = s.hidden; a.F = s.ffn; a.E = s.n_experts; a.k = s.top_k;
     a.n_tok = T; a.P = T * s.top_k;
-    a.KC = stage_kc(s.hidden, s.ffn);
+    a.KC = stage_kc(s.hidden, s.ffn, g.wbits);
+    a.wbits = g.wbits;
     a.gate_up_only = 0;
     a.expert_rs = expert_rowscale; a.shared_rs = shared_rowscale;
     a.shared_w4 = nullptr;
@@ -552,29 +750,44 @@ static ExpertArgs expert_args(int T, const float *expert_rowscale, const float *
     a.status = w.status;
     a.trace = g.trace;
     a.trace_cap = g.trace_cap;
+    a.wait_ns = 2000000000ull;     // 2 s
+    a.gdone_extra = 0;
+    a.next_rw = a.next_sw = nullptr;
+    a.next_rw_bytes = a.next_sw_bytes = 0;
     return a;
 }
 
-// The forward body.
-static int forward_impl(const float *x, int n_tok, const float *router_w, const float *router_bias,
-                        const uint8_t *expert_w4, const float *expert_rowscale,
-                        const uint8_t *shared_w4, const float *shared_rowscale, float *out,
-                        cudaStream_t st, const float *res = nullptr)
+// The forward, in three phases: the plan (expert path and weight maps), the
+// routing launches, and the expert launches.  `n_w` is the extent of the
+// routed-weight arrays (E, or the slots of the host-memory tier, whose
+// `slot_of` table maps each routed expert to its slot).
+struct FwdPlan {
+    bool use_gemm = false;
+    ExpertMaps maps{};
+};
+
+static int plan_forward(int T, const uint8_t *expert_w4, int n_w, const uint8_t *shared_w4, FwdPlan *p)
+{
+    const coli_moe_shape &s = g.s;
+    const int E = s.n_experts, k = s.top_k;
+    const bool big = g.gemm_min_tokens > 0 ? T >= g.gemm_min_tokens
+                                           : (long)T * k >= (long)COLI_GEMM_MIN_PAIRS_PER_EXPERT * E;
+    const bool gemm_ok = gemm_shape_ok(s.ffn);
+    if (g.path == COLI_PATH_GEMM && !gemm_ok) return COLI_E_UNIMPL;
+    p->use_gemm = g.path == COLI_PATH_GEMM || (g.path == COLI_PATH_AUTO && big && gemm_ok);
+    if (p->use_gemm) {
+        if (!gemm_weight_maps(expert_w4, n_w, shared_w4)) return COLI_E_CUDA;
+    } else if (!expert_maps(expert_w4, n_w, shared_w4, &p->maps)) {
+        return COLI_E_CUDA;
+    }
+    return COLI_OK;
+}
+
+static int route_phase(const float *x, int T, const float *router_w, const float *router_bias, cudaStream_t st)
 {
     const coli_moe_shape &s = g.s;
     Workspace &w = g.ws;
-    const int T = n_tok, H = s.hidden, E = s.n_experts, k = s.top_k;
-
-    const bool big = g.gemm_min_tokens > 0 ? T >= g.gemm_min_tokens
-                                           : (long)T * k >= (long)COLI_GEMM_MIN_PAIRS_PER_EXPERT * E;
-    const bool use_gemm = g.path == COLI_PATH_GEMM || (g.path == COLI_PATH_AUTO && big);
-    ExpertMaps maps;
-    if (use_gemm) {
-        if (!gemm_weight_maps(expert_w4, E, shared_w4)) return COLI_E_CUDA;
-    } else if (!expert_maps(expert_w4, E, shared_w4, &maps)) {
-        return COLI_E_CUDA;
-    }
-
+    const int H = s.hidden, E = s.n_experts, k = s.top_k;
     if (T <= ROUTE_SMALL_MAX_T) {
         RouteArgs r{};
         r.x = x; r.T = T; r.H = H; r.E = E; r.k = k; r.routed_scale = s.routed_scale;
@@ -597,9 +810,18 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
                                   w.tile_expert, w.tile_pos0, w.tile_m, w.n_tiles, w.sync, w.n_sync,
                                   w.status, st));
     }
+    return COLI_OK;
+}
 
+static int expert_phase(const FwdPlan &p, int T, const float *expert_rowscale, const uint8_t *shared_w4,
+                        const float *shared_rowscale, float *out, cudaStream_t st, const float *res,
+                        const float *next_rw, const uint8_t *next_sw, const int32_t *slot_of)
+{
+    const coli_moe_shape &s = g.s;
+    Workspace &w = g.ws;
+    const int H = s.hidden, E = s.n_experts, k = s.top_k;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (use_gemm) {
+    if (p.use_gemm) {
         const int P = T * k, F = s.ffn;
         LAUNCH_OK(launch_gather_x(w.qx, w.pos_token, w.offsets, E, P, P + T, T, H, w.xg, w.status, st));
         LAUNCH_OK(launch_gemm_items(w.counts, w.offsets, E, T, P, w.item_expert, w.item_pos0, w.item_m,
@@ -611,17 +833,18 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
         ga.expert_rs = expert_rowscale; ga.shared_rs = shared_rowscale;
         ga.qh = w.qh; ga.dh = w.dh; ga.qhb = w.qhb; ga.h_dbg = nullptr; ga.y = w.y;
         ga.status = w.status;
-        ga.trace = g.trace;
+        ga.slot_of = slot_of;
+        ga.trace = g.trace;            // the stage log covers the gate/up launch
         ga.trace_cap = g.trace_cap;
         if (g.timing) {
             int r = timing_events(&e0, &e1);
             if (r != COLI_OK) return r;
             CUDA_OK(cudaEventRecord(e0, st));
         }
-        LAUNCH_OK(launch_gemm(true, g.gemm_gu, ga, g.num_sms, st));
+        LAUNCH_OK(launch_gemm(true, g.wbits, g.gemm_gu, ga, g.num_sms, st));
         if (g.timing) CUDA_OK(cudaEventRecord(e1, st));
-        ga.trace = nullptr;   // the stage log covers the gate/up kernel
-        LAUNCH_OK(launch_gemm(false, g.gemm_dn, ga, g.num_sms, st));
+        ga.trace = nullptr;
+        LAUNCH_OK(launch_gemm(false, g.wbits, g.gemm_dn, ga, g.num_sms, st));
         LAUNCH_OK(launch_combine(w.y, w.inv, w.wts, T, k, P, H, res, out, st));
         return COLI_OK;
     }
@@ -630,14 +853,106 @@ static int forward_impl(const float *x, int n_tok, const float *router_w, const 
     a.out = out;
     a.res = res;
     a.shared_w4 = shared_w4;
+    a.slot_of = slot_of;
+    if (next_rw) {
+        a.next_rw = reinterpret_cast<const unsigned char *>(next_rw);
+        a.next_rw_bytes = (size_t)E * H * sizeof(float);
+    }
+    if (next_sw) {
+        a.next_sw = next_sw;
+        a.next_sw_bytes = (size_t)3 * s.ffn * H * g.wbits / 8;
+    }
+    if (g_inj.wait_us > 0) {
+        // injected: every down unit waits for one gate/up unit more than its
+        // tile has, so each wait runs out after the short bound
+        a.wait_ns = (unsigned long long)g_inj.wait_us * 1000ull;
+        a.gdone_extra = 1;
+        g_inj.wait_us = 0;
+    }
     if (g.timing) {
         int r = timing_events(&e0, &e1);
         if (r != COLI_OK) return r;
         CUDA_OK(cudaEventRecord(e0, st));
     }
-    LAUNCH_OK(launch_experts(maps, a, g.num_sms, st));
+    LAUNCH_OK(launch_experts(p.maps, a, g.num_sms, st));
     if (g.timing) CUDA_OK(cudaEventRecord(e1, st));
     return COLI_OK;
+}
+
+static int forward_impl(const float *x, int n_tok, const float *router_w, const float *router_bias,
+                        const uint8_t *expert_w4, const float *expert_rowscale,
+                        const uint8_t *shared_w4, const float *shared_rowscale, float *out,
+                        cudaStream_t st, const float *res = nullptr, const float *next_rw = nullptr,
+                        const uint8_t *next_sw = nullptr)
+{
+    FwdPlan p;
+    int r = plan_forward(n_tok, expert_w4, g.s.n_experts, shared_w4, &p);
+    if (r != COLI_OK) return r;
+    r = route_phase(x, n_tok, router_w, router_bias, st);
+    if (r != COLI_OK) return r;
+    return expert_phase(p, n_tok, expert_rowscale, shared_w4, shared_rowscale, out, st, res, next_rw, next_sw,
+                        nullptr);
+}
+
+int coli_moe_tier_forward(const float *x, int n_tok, const float *router_w, const float *router_bias,
+                          const uint8_t *host_expert_w, const float *host_expert_rowscale,
+                          const uint8_t *shared_w4, const float *shared_rowscale, float *out, void *stream)
+{
+    if (!g.configured || !g_tier.pool_w) return COLI_E_NOSHAPE;
+    Tier &t = g_tier;
+    if (t.wbits != g.wbits || t.E != g.s.n_experts) return COLI_E_INVAL;   // reconfigure the tier
+    int st = check_forward_args(x, n_tok, router_w, router_bias, t.pool_w, t.pool_rs, shared_w4,
+                                shared_rowscale, out);
+    if (st != COLI_OK || n_tok == 0) return st;
+    if (!host_expert_w || !host_expert_rowscale) return COLI_E_INVAL;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const int k = g.s.top_k, E = t.E;
+    FwdPlan p;
+    st = plan_forward(n_tok, t.pool_w, t.n_slots, shared_w4, &p);
+    if (st != COLI_OK) return st;
+    st = route_phase(x, n_tok, router_w, router_bias, cs);
+    if (st != COLI_OK) return st;
+    // the routing's expert choices, on the host
+    CUDA_OK(cudaMemcpyAsync(t.idx_host, g.ws.idx, sizeof(int32_t) * n_tok * k, cudaMemcpyDeviceToHost, cs));
+    CUDA_OK(cudaStreamSynchronize(cs));
+    std::vector<char> need(E, 0);
+    int n_need = 0;
+    for (int i = 0; i < n_tok * k; ++i) {
+        const int e = t.idx_host[i];
+        if (e >= 0 && e < E && !need[e]) {   // an index out of range is the kernels' to report
+            need[e] = 1;
+            ++n_need;
+        }
+    }
+    if (n_need > t.n_slots) return COLI_E_INVAL;      // one forward's union must fit in the slots
+    ++t.clock;
+    for (int e = 0; e < E; ++e)
+        if (need[e] && t.slot_of[e] >= 0) {
+            ++t.hits;
+            t.stamp[t.slot_of[e]] = t.clock;
+        }
+    for (int e = 0; e < E; ++e) {
+        if (!need[e] || t.slot_of[e] >= 0) continue;
+        // least recently used slot not taken by this forward (empty slots first)
+        int v = -1;
+        for (int q = 0; q < t.n_slots; ++q)
+            if (t.stamp[q] < t.clock && (v < 0 || t.stamp[q] < t.stamp[v])) v = q;
+        if (v < 0) return COLI_E_INVAL;
+        if (t.expert_in[v] >= 0) t.slot_of[t.expert_in[v]] = -1;
+        CUDA_OK(cudaMemcpyAsync(t.pool_w + (size_t)v * t.stride, host_expert_w + (size_t)e * t.stride, t.stride,
+                                cudaMemcpyHostToDevice, cs));
+        CUDA_OK(cudaMemcpyAsync(t.pool_rs + (size_t)v * t.rs_len, host_expert_rowscale + (size_t)e * t.rs_len,
+                                t.rs_len * sizeof(float), cudaMemcpyHostToDevice, cs));
+        t.slot_of[e] = v;
+        t.expert_in[v] = e;
+        t.stamp[v] = t.clock;
+        ++t.misses;
+        t.bytes += (long long)(t.stride + t.rs_len * sizeof(float));
+    }
+    for (int e = 0; e < E; ++e) t.slot_host[e] = t.slot_of[e] >= 0 ? t.slot_of[e] : 0;
+    CUDA_OK(cudaMemcpyAsync(t.slot_dev, t.slot_host, sizeof(int32_t) * E, cudaMemcpyHostToDevice, cs));
+    return expert_phase(p, n_tok, t.pool_rs, shared_w4, shared_rowscale, out, cs, nullptr, nullptr, nullptr,
+                        t.slot_dev);
 }
 
 int coli_moe_layer_forward(const float *x, int n_tok, const float *router_w,
@@ -664,6 +979,23 @@ int coli_moe_layer_forward_residual(const float *x, int n_tok, const float *rout
     LAUNCH_OK(launch_rmsnorm(x, n_tok, g.s.hidden, RMSNORM_EPS, g.ws.xn, cs));
     return forward_impl(g.ws.xn, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
                         shared_rowscale, out, cs, x);
+}
+
+int coli_moe_layer_forward_residual_prefetch(const float *x, int n_tok, const float *router_w,
+                                             const float *router_bias, const uint8_t *expert_w4,
+                                             const float *expert_rowscale, const uint8_t *shared_w4,
+                                             const float *shared_rowscale, const float *next_router_w,
+                                             const uint8_t *next_shared_w4, float *out, void *stream)
+{
+    int st = check_forward_args(x, n_tok, router_w, router_bias, expert_w4, expert_rowscale,
+                                shared_w4, shared_rowscale, out);
+    if (st != COLI_OK || n_tok == 0) return st;
+    if ((next_router_w && !aligned16(next_router_w)) || (next_shared_w4 && !aligned16(next_shared_w4)))
+        return COLI_E_INVAL;
+    cudaStream_t cs = (cudaStream_t)stream;
+    LAUNCH_OK(launch_rmsnorm(x, n_tok, g.s.hidden, RMSNORM_EPS, g.ws.xn, cs));
+    return forward_impl(g.ws.xn, n_tok, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,
+                        shared_rowscale, out, cs, x, next_router_w, next_shared_w4);
 }
 
 int coli_moe_dbg_rmsnorm(const float *x, int n_tok, int hidden, float *xn, void *stream)

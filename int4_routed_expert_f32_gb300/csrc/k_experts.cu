@@ -10,8 +10,9 @@
 //
 // Structure: several small blocks per SM, each 2 consumer warps + 1 producer
 // warp, all blocks resident (the grid is sized by the occupancy calculator).
-//   * Work units, claimed in increasing order from a global counter (the
-//     next one with the current unit's last copy): first
+//   * Work units, claimed in increasing order (block b starts with unit b,
+//     then takes the next one from a global counter with the current unit's
+//     last copy): first
 //     every gate/up unit (a tile of <= GEMV_MT tokens of one expert x 32
 //     hidden units = 32 gate rows + 32 up rows), then every down unit (a tile x
 //     64 output rows).
@@ -55,7 +56,7 @@ constexpr int CONSUMER_WARPS = 2;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;     // one lane per stage row
 constexpr int EXPERT_THREADS = CONSUMERS + 32;
 constexpr int BAR_CONSUMERS = 1;                   // named barrier id (0 = __syncthreads)
-constexpr uint64_t WAIT_NS = 2000000000ull;        // 2 s bound on every wait
+constexpr uint64_t WAIT_NS = 2000000000ull;        // 2 s bound on every ring wait
 
 __device__ __forceinline__ uint64_t globaltimer()
 {
@@ -74,6 +75,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (globaltimer() - t0 > WAIT_NS) return false;
     }
 }
+
 
 // Optional event log: per block, trace_cap slots of (globaltimer << 8 | code)
 // followed by the unit; slot 0 counts the events.  Codes: 1 kernel start,
@@ -94,12 +96,12 @@ __device__ __forceinline__ void trace_event(const ExpertArgs &a, int code, long 
     blk[0] = n + 1;
 }
 
-// Bounded spin until *p >= target; false if it gave up.
-__device__ __forceinline__ bool wait_counter(const int *p, int target)
+// Bounded spin until *p >= target; false if it gave up after bound_ns.
+__device__ __forceinline__ bool wait_counter(const int *p, int target, uint64_t bound_ns)
 {
     const uint64_t t0 = globaltimer();
     while (ld_acquire_gpu(p) < target) {
-        if (globaltimer() - t0 > WAIT_NS) return false;
+        if (globaltimer() - t0 > bound_ns) return false;
         nanosleep_ns(64);
     }
     return true;
@@ -157,11 +159,14 @@ static int ring_stages(int H, int F, int mt)
 
 size_t experts_smem_bytes(int H, int F) { return experts_smem_bytes_mt(H, F, GEMV_MT, ring_stages(H, F, GEMV_MT)); }
 
-// Split-form activations of one tile into shared memory (see block_dot):
-// xlo/xhi/xcd are [MT][NB]; xcd holds (MAGIC_I - 8 * sum of the codes, the
-// block's F32 scale bits) so one 8-byte load serves both.  Loads are issued SU at a time per thread so
-// that a tile's staging costs about one L2 round trip.
-template <int MT>
+// Activations of one tile into shared memory, xlo/xhi/xcd [MT][NB].  For
+// int4 weights (WB = 4) the codes are held in split form (see block_dot) and
+// xcd holds (MAGIC_I - 8 * sum of the codes, the block's F32 scale bits), the
+// nibble offset folded in; for int8 weights (WB = 8) xlo/xhi hold the block's
+// codes 0..15 and 16..31 as they are and xcd (MAGIC_I, scale bits).  One
+// 8-byte load serves both halves of xcd.  Loads are issued SU at a time per
+// thread so that a tile's staging costs about one L2 round trip.
+template <int MT, int WB>
 __device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const float *__restrict__ d,
                                            int K, int m, const int *rows, int row_limit,
                                            uint4 *xlo, uint4 *xhi, int2 *xcd, int *status)
@@ -195,12 +200,18 @@ __device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const f
         for (int uu = 0; uu < SU; ++uu) {
             const int i = i0 + uu * CONSUMERS;
             if (i < MT * NB) {
-                uint4 lo, hi;
-                int sum;
-                split_block(va[uu], vb[uu], &lo, &hi, &sum);
-                xlo[i] = lo;
-                xhi[i] = hi;
-                xcd[i] = make_int2(MAGIC_I - 8 * sum, __float_as_int(vd[uu]));
+                if (WB == 4) {
+                    uint4 lo, hi;
+                    int sum;
+                    split_block(va[uu], vb[uu], &lo, &hi, &sum);
+                    xlo[i] = lo;
+                    xhi[i] = hi;
+                    xcd[i] = make_int2(MAGIC_I - 8 * sum, __float_as_int(vd[uu]));
+                } else {
+                    xlo[i] = va[uu];
+                    xhi[i] = vb[uu];
+                    xcd[i] = make_int2(MAGIC_I, __float_as_int(vd[uu]));
+                }
             }
         }
     }
@@ -223,21 +234,42 @@ __device__ __forceinline__ int block_dot_i(uint4 w, uint4 lo, uint4 hi, int cb)
     return (a0 + a1) + ((h0 + h1) >> 4);
 }
 
+// Integer dot of a block of 32 int8 weights (two 16-byte chunks) with the
+// block's 32 int8 codes (xlo: codes 0..15, xhi: 16..31).  Returns MAGIC_I + I
+// when cb = MAGIC_I (|I| <= 32 * 127 * 127 < 2^22).
+__device__ __forceinline__ int block_dot_i8(uint4 w0, uint4 w1, uint4 lo, uint4 hi, int cb)
+{
+    int a0 = __dp4a((int)w0.x, (int)lo.x, cb);
+    int a1 = __dp4a((int)w0.y, (int)lo.y, 0);
+    int a2 = __dp4a((int)w0.z, (int)lo.z, 0);
+    int a3 = __dp4a((int)w0.w, (int)lo.w, 0);
+    a0 = __dp4a((int)w1.x, (int)hi.x, a0);
+    a1 = __dp4a((int)w1.y, (int)hi.y, a1);
+    a2 = __dp4a((int)w1.z, (int)hi.z, a2);
+    a3 = __dp4a((int)w1.w, (int)hi.w, a3);
+    return (a0 + a1) + (a2 + a3);
+}
+
 // One stage for this lane's row: the NSUB x BPS block dots of every token,
-// then their in-order fold into acc.  All trip counts are compile-time
+// then their in-order fold into acc.  A block is one 16-byte chunk of the
+// row for int4 weights, two for int8 (CPB chunks per block; woff holds the
+// row's eight chunk offsets in the box).  All trip counts are compile-time
 // constants, so the block dots form one straight-line region the scheduler
 // can interleave.
-template <int MT, int NSUB, int BPS>
+template <int MT, int NSUB, int BPS, int WB>
 __device__ __forceinline__ void stage_rows(const unsigned char *base, const int (&woff)[8], const uint4 *xlo,
                                            const uint4 *xhi, const int2 *xcd, int NB, int b0, int m,
                                            float (&acc)[MT])
 {
-    uint4 wv[NSUB][BPS];
+    constexpr int CPB = WB == 4 ? 1 : 2;
+    uint4 wv[NSUB][BPS][CPB];
 #pragma unroll
     for (int c = 0; c < NSUB; ++c)
 #pragma unroll
         for (int jj = 0; jj < BPS; ++jj)
-            wv[c][jj] = *reinterpret_cast<const uint4 *>(base + c * SUB_BYTES + woff[jj]);
+#pragma unroll
+            for (int p = 0; p < CPB; ++p)
+                wv[c][jj][p] = *reinterpret_cast<const uint4 *>(base + c * SUB_BYTES + woff[jj * CPB + p]);
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
         if (t < m) {
@@ -250,7 +282,10 @@ __device__ __forceinline__ void stage_rows(const unsigned char *base, const int 
                 for (int jj = 0; jj < BPS; ++jj) {
                     const int xb = xb0 + c * BPS + jj;
                     const int2 cd = xcd[xb];
-                    I[c][jj] = block_dot_i(wv[c][jj], xlo[xb], xhi[xb], cd.x);
+                    if (WB == 4)
+                        I[c][jj] = block_dot_i(wv[c][jj][0], xlo[xb], xhi[xb], cd.x);
+                    else
+                        I[c][jj] = block_dot_i8(wv[c][jj][0], wv[c][jj][CPB - 1], xlo[xb], xhi[xb], cd.x);
                     dd[c][jj] = __int_as_float(cd.y);
                 }
             float cacc = acc[t];
@@ -261,6 +296,18 @@ __device__ __forceinline__ void stage_rows(const unsigned char *base, const int 
                     cacc = __fmaf_rn(dd[c][jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
             acc[t] = cacc;
         }
+    }
+}
+
+// L2 prefetch of [lo, hi) clipped to a region of `bytes` bytes (offsets and
+// sizes multiples of 16, the base 16-byte aligned).
+__device__ __forceinline__ void prefetch_part(const unsigned char *base, size_t bytes, size_t lo, size_t hi)
+{
+    if (!base || lo >= bytes) return;
+    if (hi > bytes) hi = bytes;
+    for (size_t o = lo; o < hi; o += 16384) {
+        const size_t n = hi - o < 16384 ? hi - o : 16384;
+        prefetch_l2_bulk(base + o, (uint32_t)n);
     }
 }
 
@@ -275,8 +322,10 @@ __device__ __forceinline__ void decode_unit(long u, long n_gu, int G, int CH, bo
 }
 
 // MT: bound on the tokens of any tile in this launch (1, 2 or 4; <= GEMV_MT).
-// BPS: 32-weight blocks per 128- or 64-byte box row (8 or 4).
-template <int MT, int BPS>
+// BPS: 32-weight blocks per box row of KC bytes (int4: 8, 4 or 1 for KC =
+// 128, 64 or 16; int8: 4, 2 or 1 for KC = 128, 64 or 32).
+// WB: weight container, 4 (packed nibbles) or 8 (one int8 code per byte).
+template <int MT, int BPS, int WB>
 __global__ void __launch_bounds__(EXPERT_THREADS)
 k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 {
@@ -296,9 +345,11 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, F = a.F, KC = a.KC;
     const int G = F / 32, CH = H / 64;
-    // boxes along K per stage (2 when the row's box count is even)
-    const int nsub_gu = (((H / 2) / KC) % 2 == 0) ? 2 : 1, nsub_dn = (((F / 2) / KC) % 2 == 0) ? 2 : 1;
-    const int nst_gu = (H / 2) / (KC * nsub_gu), nst_dn = (F / 2) / (KC * nsub_dn);
+    // bytes of a gate/up and of a down row; boxes along K per stage (2 when
+    // the row's box count is even)
+    const int rb_gu = H * WB / 8, rb_dn = F * WB / 8;
+    const int nsub_gu = ((rb_gu / KC) % 2 == 0) ? 2 : 1, nsub_dn = ((rb_dn / KC) % 2 == 0) ? 2 : 1;
+    const int nst_gu = rb_gu / (KC * nsub_gu), nst_dn = rb_dn / (KC * nsub_dn);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstage; ++s) {
@@ -319,7 +370,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     // packed weights over themselves, so that its units read from L2 and HBM
     // does not sit idle during routing.
     if (a.shared_w4 && threadIdx.x == 32 * CONSUMER_WARPS) {
-        const size_t total_b = (size_t)3 * F * H / 2;            // multiple of 16 (H, F % 128 == 0)
+        const size_t total_b = (size_t)3 * F * H * WB / 8;      // multiple of 16 (H % 128, F % 32 == 0)
         const size_t per = ((total_b / gridDim.x) + 4095) & ~(size_t)4095;
         const size_t b0 = (size_t)blockIdx.x * per;
         const size_t b1 = b0 + per < total_b ? b0 + per : total_b;
@@ -343,7 +394,10 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             int slot = 0;
             uint32_t phase = 0;       // parity of the ring's current round
             bool first_round = true;
-            long u = atomicAdd(a.work_counter, 1);
+            // every block is resident: the first unit of block b is unit b
+            // (no atomic round trip at the start), later claims come from
+            // the counter, offset by the grid
+            long u = blockIdx.x;
             for (;;) {
                 const bool done = u >= total || S.abort;
                 bool gu = false;
@@ -358,7 +412,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 const bool shared = (e == a.E);
                 const void *m = gu ? (shared ? (const void *)&maps.sgu : (const void *)&maps.gu)
                                    : (shared ? (const void *)&maps.sdn : (const void *)&maps.dn);
-                const int z = shared ? 0 : e;
+                const int z = shared ? 0 : (a.slot_of ? __ldg(a.slot_of + e) : e);
                 bool stop = false;
                 for (int s = 0; s < nst; ++s) {
                     const unsigned long long w0 = a.trace ? globaltimer() : 0;
@@ -399,10 +453,24 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                     // ring, and units are handed out in the order in which
                     // blocks run out of work (claimed at the start of a unit,
                     // a block's second unit was fixed before its first ran)
-                    if (s == nst - 1) u_next = atomicAdd(a.work_counter, 1);
+                    if (s == nst - 1) u_next = (long)gridDim.x + atomicAdd(a.work_counter, 1);
                 }
                 if (stop) break;
                 u = u_next;
+            }
+            // Layer-ahead prefetch (stacked decode): a block with no unit
+            // left pulls its share of the next layer's router weights and
+            // shared expert into L2.  Neither depends on the next layer's
+            // routing, and HBM is partly idle while the rest of the grid
+            // finishes this layer's last down units.
+            if ((a.next_rw || a.next_sw) && !S.abort) {
+                const size_t total_b = a.next_rw_bytes + a.next_sw_bytes;
+                const size_t per = ((total_b / gridDim.x) + 4095) & ~(size_t)4095;
+                const size_t lo = (size_t)blockIdx.x * per, hi = lo + per;
+                prefetch_part(a.next_rw, a.next_rw_bytes, lo, hi);
+                if (hi > a.next_rw_bytes)
+                    prefetch_part(a.next_sw, a.next_sw_bytes, lo > a.next_rw_bytes ? lo - a.next_rw_bytes : 0,
+                                  hi - a.next_rw_bytes);
             }
             if (a.trace) {
                 // the producer's lane logs its waiting time in the block's last slot
@@ -459,7 +527,8 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             nst = gu ? nst_gu : nst_dn;
             nsub = gu ? nsub_gu : nsub_dn;
             NB = gu ? H / 32 : F / 32;
-            ers = (e == a.E) ? a.shared_rs : a.expert_rs + (size_t)e * (2 * F + H);
+            ers = (e == a.E) ? a.shared_rs
+                             : a.expert_rs + (size_t)(a.slot_of ? __ldg(a.slot_of + e) : e) * (2 * F + H);
             // activations: x codes of the tile's tokens for gate/up (kept while
             // the token set is unchanged), h codes of the tile for down
             bool restage;
@@ -473,15 +542,16 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             }
             if (restage) {
                 if (threadIdx.x == 0) {
-                    if (!gu && !wait_counter(&a.g_done[tile], G)) set_status(a.status, ST_TIMEOUT);
+                    if (!gu && !wait_counter(&a.g_done[tile], G + a.gdone_extra, a.wait_ns))
+                        set_status(a.status, ST_TIMEOUT);
                     for (int t = 0; t < GEMV_MT; ++t)
                         S.tok[t] = (t < m) ? (gu ? __ldg(a.pos_token + pos0 + t) : pos0 + t) : 0;
                 }
                 named_barrier(BAR_CONSUMERS, CONSUMERS);
                 if (gu)
-                    stage_acts<MT>(a.qx, a.dx, H, m, S.tok, a.n_tok, xlo, xhi, xcd, a.status);
+                    stage_acts<MT, WB>(a.qx, a.dx, H, m, S.tok, a.n_tok, xlo, xhi, xcd, a.status);
                 else
-                    stage_acts<MT>(a.qh, a.dh, F, m, S.tok, a.P + a.n_tok, xlo, xhi, xcd, a.status);
+                    stage_acts<MT, WB>(a.qh, a.dh, F, m, S.tok, a.P + a.n_tok, xlo, xhi, xcd, a.status);
 #pragma unroll
                 for (int t = 0; t < GEMV_MT; ++t) staged_tok[t] = gu ? S.tok[t] : -1;
                 staged_m = gu ? m : -1;
@@ -498,9 +568,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             const unsigned char *base = ring + slot * STAGE_BYTES;
             const int b0 = s * nsub * BPS;
             if (nsub == 2)
-                stage_rows<MT, 2, BPS>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
+                stage_rows<MT, 2, BPS, WB>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
             else
-                stage_rows<MT, 1, BPS>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
+                stage_rows<MT, 1, BPS, WB>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -606,7 +676,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     }
 }
 
-template <int MT, int BPS>
+template <int MT, int BPS, int WB>
 static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int num_sms, cudaStream_t st)
 {
     static size_t configured = 0;
@@ -615,10 +685,10 @@ static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int
     a.nstage = ring_stages(a.H, a.F, MT);
     const size_t smem = experts_smem_bytes_mt(a.H, a.F, MT, a.nstage);
     if (smem != configured) {
-        if (cudaFuncSetAttribute(k_experts<MT, BPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        if (cudaFuncSetAttribute(k_experts<MT, BPS, WB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return -1;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k_experts<MT, BPS>, EXPERT_THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k_experts<MT, BPS, WB>, EXPERT_THREADS,
                                                           smem) != cudaSuccess ||
             blocks_per_sm < 1)
             return -1;
@@ -635,25 +705,33 @@ static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_experts<MT, BPS>, maps, a) != cudaSuccess) return -1;
+    if (cudaLaunchKernelEx(&cfg, k_experts<MT, BPS, WB>, maps, a) != cudaSuccess) return -1;
     count_launch();
     return 0;
 }
 
-template <int BPS>
+template <int BPS, int WB>
 static int launch_experts_bps(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
 {
     // tiles hold at most min(T, GEMV_MT) tokens
     const int mt = a.n_tok < GEMV_MT ? a.n_tok : GEMV_MT;
-    if (mt <= 1) return launch_experts_mt<1, BPS>(maps, a, num_sms, st);
-    if (mt <= 2) return launch_experts_mt<2, BPS>(maps, a, num_sms, st);
-    return launch_experts_mt<4, BPS>(maps, a, num_sms, st);
+    if (mt <= 1) return launch_experts_mt<1, BPS, WB>(maps, a, num_sms, st);
+    if (mt <= 2) return launch_experts_mt<2, BPS, WB>(maps, a, num_sms, st);
+    return launch_experts_mt<4, BPS, WB>(maps, a, num_sms, st);
 }
 
 int launch_experts(const ExpertMaps &maps, const ExpertArgs &a, int num_sms, cudaStream_t st)
 {
-    if (a.KC == 128) return launch_experts_bps<8>(maps, a, num_sms, st);
-    return launch_experts_bps<4>(maps, a, num_sms, st);
+    if (a.wbits == 8) {
+        if (a.KC == 128) return launch_experts_bps<4, 8>(maps, a, num_sms, st);
+        if (a.KC == 64) return launch_experts_bps<2, 8>(maps, a, num_sms, st);
+        if (a.KC == 32) return launch_experts_bps<1, 8>(maps, a, num_sms, st);
+        return -1;
+    }
+    if (a.KC == 128) return launch_experts_bps<8, 4>(maps, a, num_sms, st);
+    if (a.KC == 64) return launch_experts_bps<4, 4>(maps, a, num_sms, st);
+    if (a.KC == 16) return launch_experts_bps<1, 4>(maps, a, num_sms, st);
+    return -1;
 }
 
 }  // namespace coli

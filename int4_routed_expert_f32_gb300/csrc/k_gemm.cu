@@ -55,11 +55,18 @@ namespace coli {
 constexpr int GM = 128;                 // positions per tile (MMA M)
 constexpr int GN = 256;                 // weight rows per tile (MMA N)
 constexpr int GK = 64;                  // K per stage (two Q8_0 blocks)
-constexpr int G_STAGES = 4;
+constexpr int G_STAGES = 4;             // pipeline stages (int4 weights; int8 weights take 3)
 constexpr int G_NACC = 2;               // TMEM accumulators (one per block in flight)
 constexpr int A_BYTES = GM * GK * 2;    // 16 KB bf16, swizzled
 constexpr int B_BYTES = GN * GK * 2;    // 32 KB bf16, swizzled
-constexpr int RAW_BYTES = GN * GK / 2;  // 8 KB packed int4
+
+// Stages and packed-weight bytes per stage of each weight container: 8 KB of
+// int4 nibbles or 16 KB of int8 codes (256 rows x 64 weights).
+template <int WB> struct GemmCfg {
+    static constexpr int STAGES = WB == 4 ? 4 : 3;
+    static constexpr int RB = GK * WB / 8;          // packed bytes of a row per stage
+    static constexpr int RAW_BYTES = GN * RB;
+};
 constexpr int G_CONV_WARPS = 2;
 constexpr int G_DRAIN_WARP0 = 4;        // warps 0..3: producer, MMA, two converters
 constexpr int G_DRAIN_WARPS = 16;       // 4 TMEM lane quarters x 4 column groups
@@ -327,17 +334,24 @@ struct GemmSmem {
     int abort;
 };
 
-size_t gemm_smem_bytes()
+template <int WB>
+static size_t gemm_smem_bytes_w()
 {
-    return 1024 + (size_t)G_STAGES * (A_BYTES + B_BYTES + RAW_BYTES) + sizeof(GemmSmem);
+    return 1024 + (size_t)GemmCfg<WB>::STAGES * (A_BYTES + B_BYTES + GemmCfg<WB>::RAW_BYTES) + sizeof(GemmSmem);
 }
+
+size_t gemm_smem_bytes() { return gemm_smem_bytes_w<4>(); }
 
 // GATEUP: A = gathered x codes (K = H), B = gate/up rows; epilogue SiLU*up and
 // Q8_0 of h.  Otherwise A = h codes (K = F), B = down rows; epilogue y.
-template <bool GATEUP>
+// WB: weight container, 4 (packed int4) or 8 (int8 codes).
+template <bool GATEUP, int WB>
 __global__ void __launch_bounds__(G_THREADS, 1)
 k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
 {
+    constexpr int G_STAGES = GemmCfg<WB>::STAGES;
+    constexpr int RB = GemmCfg<WB>::RB;
+    constexpr int RAW_BYTES = GemmCfg<WB>::RAW_BYTES;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char *sA = smem;                                   // [G_STAGES][A_BYTES]
@@ -403,7 +417,7 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                 const int e = g.item_expert[item], pos0 = g.item_pos0[item];
                 const bool shared = (e == g.E);
                 const void *wmap = shared ? (const void *)&maps.sw : (const void *)&maps.w;
-                const int z = shared ? 0 : e;
+                const int z = shared ? 0 : (g.slot_of ? g.slot_of[e] : e);
                 for (int s = 0; s < nst; ++s, ++sc) {
                     const int slot = sc % G_STAGES;
                     const int rnd = sc / G_STAGES;
@@ -417,12 +431,11 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                     tma_load_2d(sA + slot * A_BYTES, &maps.act, s * GK, pos0, &S.full[slot]);
                     unsigned char *raw = sRaw + slot * RAW_BYTES;
                     if (GATEUP) {
-                        // 128 gate rows, then the 128 matching up rows (32 bytes each)
-                        tma_load_3d(raw, wmap, s * (GK / 2), (GN / 2) * j, z, &S.full[slot], pol);
-                        tma_load_3d(raw + (GN / 2) * (GK / 2), wmap, s * (GK / 2), F + (GN / 2) * j, z,
-                                    &S.full[slot], pol);
+                        // 128 gate rows, then the 128 matching up rows (RB bytes each)
+                        tma_load_3d(raw, wmap, s * RB, (GN / 2) * j, z, &S.full[slot], pol);
+                        tma_load_3d(raw + (GN / 2) * RB, wmap, s * RB, F + (GN / 2) * j, z, &S.full[slot], pol);
                     } else {
-                        tma_load_3d(raw, wmap, s * (GK / 2), GN * j, z, &S.full[slot], pol);
+                        tma_load_3d(raw, wmap, s * RB, GN * j, z, &S.full[slot], pol);
                     }
                 }
             }
@@ -484,11 +497,11 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
         }
     } else {
         // ------------------------------ converters ------------------------------
-        // packed weights [GN rows][GK/2 bytes] -> bf16 [GN][GK] in the swizzled layout
+        // packed weights [GN rows][RB bytes] -> bf16 [GN][GK] in the swizzled layout
         const int ct = threadIdx.x - 32 * 2;        // 0 .. 63
-        constexpr int PIECES = GN * 2;              // (row, block) pieces of 16 packed bytes per stage
+        constexpr int PIECES = GN * 2;              // (row, block) pieces of RB/2 packed bytes per stage
         constexpr int PER = PIECES / (32 * G_CONV_WARPS);
-        constexpr int BATCH = 4;                    // packed loads in flight per thread
+        constexpr int BATCH = WB == 4 ? 4 : 2;      // packed loads in flight per thread
         static_assert(PER % BATCH == 0, "converter batches");
         int sc = 0;
         int ntr = 0;
@@ -510,20 +523,30 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
                 unsigned char *bt = sB + slot * B_BYTES;
 #pragma unroll 1
                 for (int p0 = 0; p0 < PER; p0 += BATCH) {
-                    uint4 w[BATCH];
+                    // piece (row n, block blk) is RB/2 bytes at n * RB + blk * RB / 2 = piece * RB / 2
+                    uint4 w[BATCH][WB / 4];
 #pragma unroll
                     for (int i = 0; i < BATCH; ++i)
-                        w[i] = *reinterpret_cast<const uint4 *>(raw + (size_t)(ct + 64 * (p0 + i)) * 16);
+#pragma unroll
+                        for (int h = 0; h < WB / 4; ++h)
+                            w[i][h] = *reinterpret_cast<const uint4 *>(raw + (size_t)(ct + 64 * (p0 + i)) * (RB / 2) +
+                                                                        16 * h);
 #pragma unroll
                     for (int i = 0; i < BATCH; ++i) {
                         const int piece = ct + 64 * (p0 + i);
                         const int n = piece >> 1, blk = piece & 1;
-                        const uint32_t wv[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int c = blk * 4 + q;   // 8-element chunk along K
-                            *reinterpret_cast<uint4 *>(bt + n * 128 + ((c ^ (n & 7)) << 4)) =
-                                nibbles_to_bf16_chunk(wv[q]);
+                            uint4 o;
+                            if (WB == 4) {
+                                const uint32_t wv[4] = {w[i][0].x, w[i][0].y, w[i][0].z, w[i][0].w};
+                                o = nibbles_to_bf16_chunk(wv[q]);
+                            } else {
+                                const uint4 &hv = w[i][(WB / 4 - 1) & (q >> 1)];
+                                o = codes_to_bf16_chunk((q & 1) ? make_uint2(hv.z, hv.w) : make_uint2(hv.x, hv.y));
+                            }
+                            *reinterpret_cast<uint4 *>(bt + n * 128 + ((c ^ (n & 7)) << 4)) = o;
                         }
                     }
                 }
@@ -610,7 +633,8 @@ k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs g)
             }
             const bool live = !*abort;
             // ---- epilogue ----
-            const float *ers = (e == g.E) ? g.shared_rs : g.expert_rs + (size_t)e * (2 * F + H);
+            const float *ers = (e == g.E) ? g.shared_rs
+                                          : g.expert_rs + (size_t)(g.slot_of ? g.slot_of[e] : e) * (2 * F + H);
             if (GATEUP) {
                 if (live && valid) {
                     // hidden units 128j + 32cq .. +31 of this token: one Q8_0 block of h
@@ -722,34 +746,36 @@ int max_gemm_items(int T, int k, int E)
 
 int gemm_tile_rows() { return GM; }
 
-template <bool GATEUP>
+template <bool GATEUP, int WB>
 static int launch_gemm_t(const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st)
 {
     static int configured_device = -1;
-    const size_t smem = gemm_smem_bytes();
+    const size_t smem = gemm_smem_bytes_w<WB>();
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (configured_device != dev) {
         // setmaxnreg.inc waits until enough registers are free: the warpgroups'
         // shares after the split must fit in what the CTA is launched with
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, k_gemm<GATEUP>) != cudaSuccess) return -1;
+        if (cudaFuncGetAttributes(&fa, k_gemm<GATEUP, WB>) != cudaSuccess) return -1;
         const long have = (long)fa.numRegs * G_THREADS;
         const long need = 32L * G_DRAIN_WARP0 * G_REGS_CTRL + 32L * G_DRAIN_WARPS * G_REGS_DRAIN;
         if (fa.numRegs < G_REGS_CTRL || fa.numRegs > G_REGS_DRAIN || need > have) return -1;
-        if (cudaFuncSetAttribute(k_gemm<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        if (cudaFuncSetAttribute(k_gemm<GATEUP, WB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return -1;
         configured_device = dev;
     }
-    k_gemm<GATEUP><<<num_sms, G_THREADS, smem, st>>>(maps, g);
+    k_gemm<GATEUP, WB><<<num_sms, G_THREADS, smem, st>>>(maps, g);
     count_launch();
     return 0;
 }
 
-int launch_gemm(bool gateup, const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st)
+int launch_gemm(bool gateup, int wbits, const GemmMaps &maps, const GemmArgs &g, int num_sms, cudaStream_t st)
 {
-    return gateup ? launch_gemm_t<true>(maps, g, num_sms, st) : launch_gemm_t<false>(maps, g, num_sms, st);
+    if (wbits == 8)
+        return gateup ? launch_gemm_t<true, 8>(maps, g, num_sms, st) : launch_gemm_t<false, 8>(maps, g, num_sms, st);
+    return gateup ? launch_gemm_t<true, 4>(maps, g, num_sms, st) : launch_gemm_t<false, 4>(maps, g, num_sms, st);
 }
 
 }  // namespace coli

@@ -53,6 +53,55 @@ __global__ void __launch_bounds__(256) k_pack_int4(const float *__restrict__ w, 
     }
 }
 
+// The int8 weight container, one warp per row: s = max|row| / 127 (IEEE
+// divide), q = clamp(rint(w / s), -127, 127) as two's-complement bytes; an
+// all-zero row gives s = 0 and codes 0.  The same rule as the int4 container
+// with 127 in place of 7 (the pages name an int8 container and an int8 head:
+// "colibri: a pure-C inference engine ..." (discuss.pytorch.kr), section
+// "Key features").
+__global__ void __launch_bounds__(256) k_pack_int8(const float *__restrict__ w, int rows, int K,
+                                                   int8_t *__restrict__ q, float *__restrict__ scale)
+{
+    int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float *wr = w + (size_t)row * K;
+    float a = 0.0f;
+    for (int k = lane; k < K; k += 32) a = fmaxf(a, fabsf(wr[k]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(FULL, a, o));
+    float s = __fdiv_rn(a, 127.0f);
+    if (lane == 0) scale[row] = s;
+    int8_t *qr = q + (size_t)row * K;
+    for (int k = lane; k < K; k += 32) {
+        int v = 0;
+        if (s > 0.0f) v = max(-127, min(127, __float2int_rn(__fdiv_rn(wr[k], s))));
+        qr[k] = (int8_t)v;
+    }
+}
+
+// Stage kernel: I[r][b] of int8-container rows against one int8 vector.
+__global__ void __launch_bounds__(256) k_block_dots_w8(const int8_t *__restrict__ w8, int rows, int K,
+                                                       const int8_t *__restrict__ q, int32_t *__restrict__ I)
+{
+    int nb = K / 32;
+    long id = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (id >= (long)rows * nb) return;
+    int r = (int)(id / nb), b = (int)(id % nb);
+    const int4 *xq = reinterpret_cast<const int4 *>(q + (size_t)b * 32);
+    const int4 *wq = reinterpret_cast<const int4 *>(w8 + (size_t)r * K + (size_t)b * 32);
+    int acc = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int4 x = xq[h], w = wq[h];
+        acc = __dp4a(w.x, x.x, acc);
+        acc = __dp4a(w.y, x.y, acc);
+        acc = __dp4a(w.z, x.z, acc);
+        acc = __dp4a(w.w, x.w, acc);
+    }
+    I[id] = acc;
+}
+
 // Stage kernel: I[r][b] for packed rows against one int8 vector, through the
 // same block_dot used by the expert kernels.  One thread per (row, block).
 __global__ void __launch_bounds__(256) k_block_dots(const uint8_t *__restrict__ w4, int rows, int K,
@@ -87,6 +136,24 @@ int launch_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *sc
     if (rows == 0) return 0;
     unsigned grid = (unsigned)(((long)rows * 32 + 255) / 256);
     k_pack_int4<<<grid, 256, 0, st>>>(w, rows, K, packed, scale);
+    count_launch();
+    return 0;
+}
+
+int launch_pack_int8(const float *w, int rows, int K, int8_t *q, float *scale, cudaStream_t st)
+{
+    if (rows == 0) return 0;
+    unsigned grid = (unsigned)(((long)rows * 32 + 255) / 256);
+    k_pack_int8<<<grid, 256, 0, st>>>(w, rows, K, q, scale);
+    count_launch();
+    return 0;
+}
+
+int launch_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *q, int32_t *I, cudaStream_t st)
+{
+    long n = (long)rows * (K / 32);
+    if (n == 0) return 0;
+    k_block_dots_w8<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(w8, rows, K, q, I);
     count_launch();
     return 0;
 }

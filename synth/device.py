@@ -16,17 +16,19 @@ import synth
 
 
 def build_device_layer(wl: synth.Workload, layer: int = 0, device: str = "cuda",
-                       workers: int | None = None, experts=None):
+                       workers: int | None = None, experts=None, wbits: int = 4):
     """Return a dict of device tensors for one layer:
-    router_w [E][H], router_b [E], expert_w4 [E][3FH/2] uint8, expert_rs [E][2F+H],
-    shared_w4 [3FH/2] uint8, shared_rs [2F+H].
+    router_w [E][H], router_b [E], expert_w4 [E][3FH*wbits/8] uint8, expert_rs [E][2F+H],
+    shared_w4 [3FH*wbits/8] uint8, shared_rs [2F+H].
 
+    ``wbits``: the weight container, 4 (packed int4, the library's pack_int4)
+    or 8 (int8 codes, pack_int8), packed from the same F32 draw.
     ``experts``: optional iterable of routed expert ids to fill; the others are
     left as zero bytes (used by small tests that know which experts run)."""
     import int4_routed_expert_f32_gb300 as coli
 
     H, F, E = wl.hidden, wl.ffn, wl.n_experts
-    stride = wl.expert_bytes
+    stride = 3 * F * H * wbits // 8
     W, b = synth.router(wl, layer)
     out = dict(
         router_w=torch.from_numpy(W).to(device),
@@ -47,10 +49,14 @@ def build_device_layer(wl: synth.Workload, layer: int = 0, device: str = "cuda",
         mats = ((0, F, H), (F * H, F, H), (2 * F * H, H, F))
         w4off, rsoff = 0, 0
         for off, rows, K in mats:
-            coli.pack_int4(staging[off:off + rows * K].view(rows, K),
-                           w4[w4off:w4off + rows * K // 2].view(rows, K // 2),
-                           rs[rsoff:rsoff + rows])
-            w4off += rows * K // 2
+            nb = rows * K * wbits // 8
+            if wbits == 8:
+                coli.pack_int8(staging[off:off + rows * K].view(rows, K),
+                               w4[w4off:w4off + nb].view(torch.int8).view(rows, K), rs[rsoff:rsoff + rows])
+            else:
+                coli.pack_int4(staging[off:off + rows * K].view(rows, K),
+                               w4[w4off:w4off + nb].view(rows, K // 2), rs[rsoff:rsoff + rows])
+            w4off += nb
             rsoff += rows
         torch.cuda.current_stream().synchronize()
 

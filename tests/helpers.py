@@ -7,16 +7,18 @@ import numpy as np
 import synth
 
 
-def oracle_expert(wl: synth.Workload, e: int, layer: int = 0):
-    """(packed bytes [3FH/2], row scales [2F+H]) of expert e (E = shared),
-    packed by the oracle's own converter from the seeded F32 draw."""
+def oracle_expert(wl: synth.Workload, e: int, layer: int = 0, wbits: int = 4):
+    """(weight bytes [3FH*wbits/8], row scales [2F+H]) of expert e (E =
+    shared), packed by the oracle's own converter from the seeded F32 draw
+    into the int4 (wbits 4) or int8 (wbits 8) container."""
     import oracle
     F, H = wl.ffn, wl.hidden
     flat = synth.expert_f32_rows(wl, e, layer)
-    pg, sg = oracle.pack_int4_rows(flat[:F * H].reshape(F, H))
-    pu, su = oracle.pack_int4_rows(flat[F * H:2 * F * H].reshape(F, H))
-    pd, sd = oracle.pack_int4_rows(flat[2 * F * H:].reshape(H, F))
-    return (np.concatenate([pg.ravel(), pu.ravel(), pd.ravel()]),
+    pack = oracle.pack_int4_rows if wbits == 4 else oracle.pack_int8_rows
+    pg, sg = pack(flat[:F * H].reshape(F, H))
+    pu, su = pack(flat[F * H:2 * F * H].reshape(F, H))
+    pd, sd = pack(flat[2 * F * H:].reshape(H, F))
+    return (np.concatenate([pg.ravel(), pu.ravel(), pd.ravel()]).view(np.uint8),
             np.concatenate([sg, su, sd]))
 
 
@@ -28,22 +30,24 @@ class OracleLayer:
     weights (the decode, verify and prefill workloads share one layer's
     experts and differ only in the router bias)."""
 
-    def __init__(self, wl: synth.Workload, layer: int = 0, cache: dict | None = None):
+    def __init__(self, wl: synth.Workload, layer: int = 0, cache: dict | None = None, wbits: int = 4):
         self.wl = wl
         self.layer = layer
+        self.wbits = wbits
         self.W, self.b = synth.router(wl, layer)
         self._cache = {} if cache is None else cache
         self.shared = self.expert(wl.n_experts)
 
     def expert(self, e):
         if e not in self._cache:
-            self._cache[e] = oracle_expert(self.wl, e, self.layer)
+            self._cache[e] = oracle_expert(self.wl, e, self.layer, self.wbits)
         return self._cache[e]
 
     def prefetch(self, experts):
         todo = sorted(set(int(e) for e in experts) - set(self._cache))
         if todo:
-            for e, v in zip(todo, synth.parallel_map(lambda e: oracle_expert(self.wl, e, self.layer), todo)):
+            packed = synth.parallel_map(lambda e: oracle_expert(self.wl, e, self.layer, self.wbits), todo)
+            for e, v in zip(todo, packed):
                 self._cache[e] = v
 
     def forward(self, x, intermediates=False):
@@ -58,7 +62,7 @@ class OracleLayer:
             w4[e], rs[e] = self.expert(e)
         return oracle.moe_forward(x, self.W, self.b, w4, rs, self.shared[0], self.shared[1],
                                   wl.hidden, wl.ffn, wl.top_k, wl.routed_scale,
-                                  intermediates=intermediates)
+                                  intermediates=intermediates, wbits=self.wbits)
 
 
 # Float outputs must agree within max|err| <= 1e-3 * rms(oracle output).

@@ -45,7 +45,8 @@ def test_shape_validation_without_gpu(lib):
     import int4_routed_expert_f32_gb300 as coli
     bad = [
         (255, 128, 8, 2, 2.5, 4),     # hidden not a multiple of 128
-        (256, 100, 8, 2, 2.5, 4),     # ffn not a multiple of 128
+        (256, 100, 8, 2, 2.5, 4),     # ffn not a multiple of 32
+        (256, 144, 8, 2, 2.5, 4),     # ffn a multiple of 16 but not of 32
         (256, 128, 300, 2, 2.5, 4),   # too many experts
         (256, 128, 8, 9, 2.5, 4),     # top_k > n_experts
         (256, 128, 8, 2, 0.0, 4),     # routed_scale must be > 0
@@ -76,3 +77,11 @@ def test_calls_before_configure_report_noshape(lib):
     assert L.coli_moe_dbg_quantize(None, 31, None, None, None) == coli.E_INVAL
     assert L.coli_moe_set_path(7, 0) == coli.E_INVAL
     assert L.coli_moe_strerror(coli.E_NOSHAPE) == b"layer shape not configured"
+
+
+def test_injection_kinds_are_checked(lib):
+    import int4_routed_expert_f32_gb300 as coli
+    L = coli.lib()
+    assert L.coli_moe_dbg_inject(99, 0) == coli.E_INVAL
+    assert L.coli_moe_dbg_inject(coli.INJECT_LAUNCH_FAIL, -1) == coli.E_INVAL
+    assert L.coli_moe_dbg_inject(coli.INJECT_NONE, 0) == coli.OK

@@ -209,3 +209,36 @@ def test_one_token_tied_keys(coli, path, E, k):
     want = oracle.moe_forward(x, np.zeros_like(ref.W), b, w4, rs, ref.shared[0], ref.shared[1],
                               wl.hidden, wl.ffn, k, wl.routed_scale)
     np.testing.assert_array_equal(got, want)
+
+
+# --------------------------------------------------------------------------- #
+# expert FFN widths that are a multiple of 32 but not of 128                   #
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("F,T", [(160, 5), (96, 1), (224, 300)])
+def test_ffn_multiple_of_32(coli, F, T):
+    """An FFN width of 32 * odd (or 32 * 3, 32 * 7) runs on the streaming
+    path with 16-byte weight stages, bit-exact; AUTO picks that path even for a
+    batch large enough for the grouped GEMM, and a forward forced onto the
+    GEMM (whose tiles need F % 128 == 0) is refused with COLI_E_UNIMPL before
+    any launch."""
+    from synth.device import build_device_layer
+    wl = synth.Workload(f"ffn{F}", 256, F, 8, 2, T, 950 + F)
+    L = build_device_layer(wl)
+    x = synth.activations(wl, 1)
+    want = OracleLayer(wl).forward(x)
+    got = _run(coli, "gemv", wl, L, x)
+    np.testing.assert_array_equal(got, want)
+    coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, T)
+    coli.set_path(coli.PATH_AUTO, 1)          # AUTO would take the GEMM from one token on
+    try:
+        got = coli.layer_forward(torch.from_numpy(x).cuda(), L["router_w"], L["router_b"], L["expert_w4"],
+                                 L["expert_rs"], L["shared_w4"], L["shared_rs"]).cpu().numpy()
+        np.testing.assert_array_equal(got, want)
+        coli.set_path(coli.PATH_GEMM)
+        with pytest.raises(coli.ColiError) as ei:
+            coli.layer_forward(torch.from_numpy(x).cuda(), L["router_w"], L["router_b"], L["expert_w4"],
+                               L["expert_rs"], L["shared_w4"], L["shared_rs"])
+        assert ei.value.code == coli.E_UNIMPL
+    finally:
+        coli.set_path(coli.PATH_AUTO, 0)
+    assert coli.get_device_status() == coli.OK

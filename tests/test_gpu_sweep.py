@@ -31,9 +31,17 @@ def test_sweep_stack_matches_oracle_per_layer(stack, B):
     coli.configure(wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.routed_scale, max(wl.batches))
     x = torch.from_numpy(synth.activations(wl, 3, n_tok=B)).cuda()
     for l, L in enumerate(layers):
-        out = coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
-                                          L["shared_w4"], L["shared_rs"])
+        nxt = layers[l + 1] if l + 1 < len(layers) else None
+        # the stacked-decode forward with the next layer's router weights and
+        # shared expert prefetched into L2: identical to the plain residual
+        # forward
+        out = coli.layer_forward_residual_prefetch(
+            x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"], L["shared_w4"], L["shared_rs"],
+            nxt["router_w"] if nxt else None, nxt["shared_w4"] if nxt else None)
+        plain = coli.layer_forward_residual(x, L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"],
+                                            L["shared_w4"], L["shared_rs"])
         assert coli.get_device_status() == coli.OK
+        assert torch.equal(out, plain)
         xs = x.cpu().numpy()
         ref = OracleLayer(wl, layer=l)     # one layer's experts at a time (host memory)
         want = (xs + ref.forward(oracle.rmsnorm(xs))).astype(np.float32)
