@@ -55,17 +55,17 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "3714d7666e6b66a88fa19d75bce10a9a1db24152765af8f15ef9da896aee0ac5",
-        "bytes_per_launch": 173673216,   # 170.81 MB read + 2.86 MB written
-        # a launch of the 16-expert profile workload streams 8 routed + 1 shared
-        # expert, the same units as one decode forward over 256 experts
+        "sha256": "a383bb7857f769033bcd5869167c0f7a8453a2276b75646cb59b1cab06b2f750",
+        "bytes_per_launch": 171012096,   # 170.94 MB read + 0.07 MB written (median of three launches)
+        # a decode forward streams 8 routed + 1 shared expert; the capture ran
+        # the decode workload itself
         "workloads": ("decode", "profile"),
-        "capture": "profiles/k_experts_decode_profile.md",
+        "capture": "profiles/decode_layer_launches.md",
     },
     "k_gemm_gateup": {
         "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "ce67970fb2ce0f75bd1e8697edca09c50564dc99bdc47febf96ccb0b81fe1ec3",
-        "bytes_per_launch": 5391012352,  # 5295.90 MB read + 95.12 MB written
+        "sha256": "b1e40ff4e99a232e0e8bba063eab4ad066a3dc995f3a68ebad5ffbe23c7dc234",
+        "bytes_per_launch": 5379424000,  # 5284.00 MB read + 95.43 MB written
         "workloads": ("prefill",),
         "capture": "profiles/prefill_layer_launches.md",
     },
@@ -458,6 +458,28 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
     if use_gemm:
         rec["layer_roofline_terms_ms"] = {"weights_at_hbm_peak": bytes_per_fwd / (hbm_peak * 1e9) * 1e3,
                                           "ops_at_bf16_peak": 2.0 * macs_layer / (bf16_peak * 1e12) * 1e3}
+    else:
+        # reference for the expert kernel: one plain pass over the same number
+        # of bytes (a torch reduction over a contiguous device buffer, L2
+        # flushed before each pass), i.e. what a single read of that much
+        # data reaches on this GPU, ramp and tail included
+        nb = int(bytes_per_fwd) // 4 * 4
+        buf = torch.ones(nb // 4, dtype=torch.float32, device="cuda")
+        fl = []
+        for i in range(25):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(st)
+            torch.sum(buf)
+            b_.record(st)
+            fl.append((a_, b_))
+        torch.cuda.synchronize()
+        fms = float(np.median([a_.elapsed_time(b_) for a_, b_ in fl[5:]]))
+        rec["stream_floor"] = {"bytes": nb, "ms": fms, "gbs": nb / (fms * 1e-3) / 1e9,
+                               "frac_of_hbm": nb / (fms * 1e-3) / 1e9 / hbm_peak,
+                               "what": "torch.sum over a contiguous float32 buffer of the forward's algorithmic "
+                                       "bytes, one pass, L2 flushed, median of 20"}
+        del buf
     if rank == 0 and not args.no_cpu_baseline:
         nf = args.cpu_forwards if T <= 64 else 1
         rec["cpu_baseline"] = cpu_baseline_line(wl, nf, cpu_seconds, single_thread=single_thread_cpu, wbits=wbits)
@@ -479,33 +501,42 @@ def measure_tier(args, wl, L, router_b, world, rank, local, n_slots=64):
     hw = L["expert_w4"].cpu().pin_memory()
     hrs = L["expert_rs"].cpu().pin_memory()
     coli.tier_configure(n_slots)
-    n_total = args.warmup + args.steps
+    # every step synchronises the host once, so a single host stall weighs on
+    # a short run: time at least 200 steps (and at least 20 warm-up steps, so
+    # that the cache is full)
+    steps = max(args.steps, 200)
+    warm = max(args.warmup, 20)
+    n_total = warm + steps
     xs = torch.from_numpy(np.stack([synth.activations(wl, 50_000 + rank * 100_000 + i)
                                     for i in range(n_total)])).cuda()
     out = torch.empty((T, wl.hidden), dtype=torch.float32, device="cuda")
-    for i in range(args.warmup):
+    for i in range(warm):
         coli.tier_forward(xs[i], L["router_w"], router_b, hw, hrs, L["shared_w4"], L["shared_rs"], out=out)
     torch.cuda.synchronize()
     h0, m0, b0, _ = coli.tier_stats()
+    step_s = []
     with ClockSampler(local) as clocks:
         t0 = time.perf_counter()
-        for s_ in range(args.steps):
-            coli.tier_forward(xs[args.warmup + s_], L["router_w"], router_b, hw, hrs, L["shared_w4"],
+        for s_ in range(steps):
+            t1 = time.perf_counter()
+            coli.tier_forward(xs[warm + s_], L["router_w"], router_b, hw, hrs, L["shared_w4"],
                               L["shared_rs"], out=out)
-        torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            step_s.append(time.perf_counter() - t1)
         dt = max_over_ranks(time.perf_counter() - t0, world)
     h1, m1, b1, res = coli.tier_stats()
     status = coli.get_device_status()
     coli.tier_release()
     hits, misses, nbytes = h1 - h0, m1 - m0, b1 - b0
-    return {"value": world * args.steps * T / dt, "unit": "tok/s", "steps": args.steps,
-            "ms_per_step": dt / args.steps * 1e3,
+    return {"value": world * steps * T / dt, "unit": "tok/s", "steps": steps, "warmup": warm,
+            "ms_per_step": dt / steps * 1e3,
+            "step_ms_p10_p50_p90": [float(np.percentile(step_s, q)) * 1e3 for q in (10, 50, 90)],
             "config": {"workload": f"decode layer (hidden {wl.hidden}, expert FFN {wl.ffn}, {wl.n_experts} experts "
                                    f"top-{wl.top_k} + 1 shared), routed experts in page-locked host memory, "
                                    f"LRU cache of {n_slots} experts in HBM, 1 token per forward, fresh activations",
                        "hbm_slots": n_slots, "host_expert_bytes": int(hw.numel())},
-            "hit_rate": hits / max(hits + misses, 1), "misses_per_step": misses / args.steps,
-            "h2d_gbs": nbytes / dt / 1e9, "h2d_bytes_per_step": nbytes / args.steps,
+            "hit_rate": hits / max(hits + misses, 1), "misses_per_step": misses / steps,
+            "h2d_gbs": nbytes / dt / 1e9, "h2d_bytes_per_step": nbytes / steps,
             "resident_experts": res, "clocks": clocks.summary(), "device_status": status,
             "timing": "host wall clock around the steps (each step synchronises once, after routing)"}
 
