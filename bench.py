@@ -28,6 +28,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -55,7 +56,7 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "a383bb7857f769033bcd5869167c0f7a8453a2276b75646cb59b1cab06b2f750",
+        "sha256": "d4388ee398f0753c37bf96d151725ffcb2840a69876c23c6e629e54129f2a774",
         "bytes_per_launch": 171012096,   # 170.94 MB read + 0.07 MB written (median of three launches)
         # a decode forward streams 8 routed + 1 shared expert; the capture ran
         # the decode workload itself
@@ -64,7 +65,7 @@ TRAFFIC = {
     },
     "k_gemm_gateup": {
         "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "b1e40ff4e99a232e0e8bba063eab4ad066a3dc995f3a68ebad5ffbe23c7dc234",
+        "sha256": "351881951d6db66c91ddb37435404225509274ec537f86dacadc48b4e7340e5c",
         "bytes_per_launch": 5379424000,  # 5284.00 MB read + 95.43 MB written
         "workloads": ("prefill",),
         "capture": "profiles/prefill_layer_launches.md",
@@ -398,6 +399,7 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
         coli.layer_forward_hostio(xh[i % n_h], L["router_w"], router_b, L["expert_w4"],
                                   L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
     e2e_s = 0.0
+    gc.disable()      # no collector pause inside the host-timed steps
     for s in range(args.steps):
         flush.zero_()
         torch.cuda.synchronize()
@@ -405,6 +407,7 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
         coli.layer_forward_hostio(xh[s % n_h], L["router_w"], router_b, L["expert_w4"],
                                   L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
         e2e_s += time.perf_counter() - t0
+    gc.enable()
     e2e_s = max_over_ranks(e2e_s, world)
     coli.set_path(coli.PATH_AUTO)
     coli.set_weight_bits(4)
@@ -459,27 +462,31 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
         rec["layer_roofline_terms_ms"] = {"weights_at_hbm_peak": bytes_per_fwd / (hbm_peak * 1e9) * 1e3,
                                           "ops_at_bf16_peak": 2.0 * macs_layer / (bf16_peak * 1e12) * 1e3}
     else:
-        # reference for the expert kernel: one plain pass over the same number
-        # of bytes (a torch reduction over a contiguous device buffer, L2
-        # flushed before each pass), i.e. what a single read of that much
-        # data reaches on this GPU, ramp and tail included
-        nb = int(bytes_per_fwd) // 4 * 4
-        buf = torch.ones(nb // 4, dtype=torch.float32, device="cuda")
+        # reference for the expert kernel: one bare read of the same number of
+        # bytes in one launch (coli_moe_dbg_stream_read: bulk copies into the
+        # same per-block rings, no arithmetic), L2 flushed before each pass,
+        # i.e. what a single read of that much data reaches on this GPU, ramp
+        # and tail included
+        nb = int(bytes_per_fwd) // 16 * 16
+        buf = torch.ones(nb // 4, dtype=torch.int32, device="cuda")
+        sink = torch.empty(1, dtype=torch.int64, device="cuda")
         fl = []
         for i in range(25):
             flush.zero_()
             a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a_.record(st)
-            torch.sum(buf)
+            coli.dbg_stream_read(buf, sum_out=sink)
             b_.record(st)
             fl.append((a_, b_))
         torch.cuda.synchronize()
         fms = float(np.median([a_.elapsed_time(b_) for a_, b_ in fl[5:]]))
         rec["stream_floor"] = {"bytes": nb, "ms": fms, "gbs": nb / (fms * 1e-3) / 1e9,
                                "frac_of_hbm": nb / (fms * 1e-3) / 1e9 / hbm_peak,
-                               "what": "torch.sum over a contiguous float32 buffer of the forward's algorithmic "
-                                       "bytes, one pass, L2 flushed, median of 20"}
-        del buf
+                               "expert_kernel_vs_floor": fms / k_avg_ms,
+                               "what": "coli_moe_dbg_stream_read: one launch reading the forward's algorithmic "
+                                       "bytes through bulk copies into per-block shared-memory rings, no "
+                                       "arithmetic, L2 flushed, median of 20"}
+        del buf, sink
     if rank == 0 and not args.no_cpu_baseline:
         nf = args.cpu_forwards if T <= 64 else 1
         rec["cpu_baseline"] = cpu_baseline_line(wl, nf, cpu_seconds, single_thread=single_thread_cpu, wbits=wbits)
@@ -743,12 +750,14 @@ def measure_sweep(args, world, rank, local, cpu_seconds):
         e2e_once()
     e2e_s = 0.0
     n_e2e = min(args.steps, 50)
+    gc.disable()
     for _ in range(n_e2e):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_once()
         e2e_s += time.perf_counter() - t0
+    gc.enable()
     e2e_s = max_over_ranks(e2e_s, world)
     b1 = per_b[0]
     rec = {

@@ -39,6 +39,7 @@
 #ifndef COLI_MOE_H
 #define COLI_MOE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -353,6 +354,17 @@ int coli_moe_dbg_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q,
 /* The same for rows of the int8 container: w8 [rows][K] int8 codes. */
 int coli_moe_dbg_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *q, int32_t *I_out,
                                void *stream);
+
+/* Measurement reference (needs no configure): one launch that streams `bytes`
+ * bytes of the device buffer `buf` from HBM through bulk copies into per-block
+ * shared-memory rings (three blocks of 48 KB per SM, the expert kernel's
+ * arrangement) and does no arithmetic on them but a checksum: *sum (a device
+ * u64, zeroed by the call) receives the sum of the four 32-bit words at every
+ * offset o < bytes with o % 1024 == 0.  buf 16-byte aligned, bytes % 16 == 0,
+ * sum 8-byte aligned; otherwise COLI_E_INVAL.  Its duration is the single-pass
+ * read time of that many bytes, the floor against which the streaming expert
+ * kernel's bandwidth is read. */
+int coli_moe_dbg_stream_read(const void *buf, size_t bytes, unsigned long long *sum, void *stream);
 
 /* Run a full forward and copy out its intermediates (any pointer may be NULL):
  * qx [n_tok][H] int8, dx [n_tok][H/32], idx/w [n_tok][k],

@@ -42,7 +42,7 @@ EXPORTS = (
     "coli_moe_dbg_expert_hidden", "coli_moe_route_noalloc", "coli_moe_dbg_inject",
     "coli_moe_layer_forward_residual_prefetch", "coli_moe_pack_int8", "coli_moe_set_weight_bits",
     "coli_moe_dbg_block_dots_w8", "coli_moe_tier_configure", "coli_moe_tier_forward", "coli_moe_tier_stats",
-    "coli_moe_tier_release",
+    "coli_moe_tier_release", "coli_moe_dbg_stream_read",
 )
 INJECT_NONE, INJECT_ALLOC_FAIL, INJECT_LAUNCH_FAIL, INJECT_WAIT_TIMEOUT = 0, 1, 2, 3
 
@@ -99,6 +99,7 @@ def _load():
         "coli_moe_tier_forward": ([P, i, P, P, P, P, P, P, P, P], i),
         "coli_moe_tier_stats": ([ctypes.POINTER(ctypes.c_longlong)] * 3 + [ctypes.POINTER(ctypes.c_int)], i),
         "coli_moe_tier_release": ([], None),
+        "coli_moe_dbg_stream_read": ([P, ctypes.c_size_t, P, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -400,6 +401,17 @@ def dbg_block_dots_w8(w8, q, stream=None):
     _check(_lib.coli_moe_dbg_block_dots_w8(_ptr(w8), rows, K, _ptr(q), _ptr(I), _stream(stream)),
            "dbg_block_dots_w8")
     return I
+
+
+def dbg_stream_read(buf, n_bytes=None, sum_out=None, stream=None):
+    """One bare read of the first n_bytes of the device tensor buf (default:
+    all of it) in one launch; returns the device u64 checksum tensor (the sum
+    of the four 32-bit words at every 1024-byte offset)."""
+    nb = buf.numel() * buf.element_size() if n_bytes is None else int(n_bytes)
+    if sum_out is None:
+        sum_out = torch.empty(1, dtype=torch.int64, device=buf.device)
+    _check(_lib.coli_moe_dbg_stream_read(_ptr(buf), nb, _ptr(sum_out), _stream(stream)), "dbg_stream_read")
+    return sum_out
 
 
 def dbg_forward_intermediates(x, router_w, router_bias, expert_w4, expert_rowscale, shared_w4,

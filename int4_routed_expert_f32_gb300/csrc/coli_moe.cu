@@ -1007,6 +1007,19 @@ int coli_moe_dbg_rmsnorm(const float *x, int n_tok, int hidden, float *xn, void 
     return COLI_OK;
 }
 
+int coli_moe_dbg_stream_read(const void *buf, size_t bytes, unsigned long long *sum, void *stream)
+{
+    if (!buf || !sum || !aligned16(buf) || bytes % 16 != 0 || ((uintptr_t)sum & 7) != 0) return COLI_E_INVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    CUDA_OK(cudaMemsetAsync(sum, 0, sizeof(unsigned long long), s));
+    if (bytes == 0) return COLI_OK;
+    int dev = 0, sms = 0;
+    CUDA_OK(cudaGetDevice(&dev));
+    CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    LAUNCH_OK(launch_stream_read(buf, bytes, sum, nullptr, sms, s));
+    return COLI_OK;
+}
+
 int coli_moe_layer_forward_hostio(const float *x_host, int n_tok, const float *router_w,
                                   const float *router_bias, const uint8_t *expert_w4,
                                   const float *expert_rowscale, const uint8_t *shared_w4,

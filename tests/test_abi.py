@@ -85,3 +85,16 @@ def test_injection_kinds_are_checked(lib):
     assert L.coli_moe_dbg_inject(99, 0) == coli.E_INVAL
     assert L.coli_moe_dbg_inject(coli.INJECT_LAUNCH_FAIL, -1) == coli.E_INVAL
     assert L.coli_moe_dbg_inject(coli.INJECT_NONE, 0) == coli.OK
+
+
+def test_stream_read_argument_checks(lib):
+    """The bare-read reference rejects unaligned buffers, sizes that are not a
+    multiple of 16 and unaligned result pointers before touching the device."""
+    import int4_routed_expert_f32_gb300 as coli
+    L = coli.lib()
+    aligned, sink = 1 << 20, 1 << 21          # never dereferenced: rejected first
+    assert L.coli_moe_dbg_stream_read(None, 16, sink, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(aligned + 8, 16, sink, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(aligned, 24, sink, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(aligned, 16, sink + 4, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(aligned, 16, None, None) == coli.E_INVAL
