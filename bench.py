@@ -395,17 +395,20 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
     xh = torch.from_numpy(np.stack([synth.activations(wl, 20_000 + i) for i in range(n_h)]))
     xh = xh.pin_memory()
     oh = torch.empty((T, wl.hidden), dtype=torch.float32).pin_memory()
+    # the public call a serving loop makes: a layer prepared once, then one
+    # host-I/O forward per step
+    layer = coli.PreparedLayer(L["router_w"], router_b, L["expert_w4"], L["expert_rs"], L["shared_w4"],
+                               L["shared_rs"])
+    xh_steps = [xh[i] for i in range(n_h)]
     for i in range(min(args.warmup, 5)):
-        coli.layer_forward_hostio(xh[i % n_h], L["router_w"], router_b, L["expert_w4"],
-                                  L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
+        layer.forward_hostio(xh_steps[i % n_h], oh)
     e2e_s = 0.0
     gc.disable()      # no collector pause inside the host-timed steps
     for s in range(args.steps):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        coli.layer_forward_hostio(xh[s % n_h], L["router_w"], router_b, L["expert_w4"],
-                                  L["expert_rs"], L["shared_w4"], L["shared_rs"], oh)
+        layer.forward_hostio(xh_steps[s % n_h], oh)
         e2e_s += time.perf_counter() - t0
     gc.enable()
     e2e_s = max_over_ranks(e2e_s, world)
@@ -479,13 +482,13 @@ def measure_layer(args, wl, L, router_b, world, rank, local, cpu_seconds, single
             b_.record(st)
             fl.append((a_, b_))
         torch.cuda.synchronize()
-        fms = float(np.median([a_.elapsed_time(b_) for a_, b_ in fl[5:]]))
+        fms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in fl[5:]]))
         rec["stream_floor"] = {"bytes": nb, "ms": fms, "gbs": nb / (fms * 1e-3) / 1e9,
                                "frac_of_hbm": nb / (fms * 1e-3) / 1e9 / hbm_peak,
                                "expert_kernel_vs_floor": fms / k_avg_ms,
                                "what": "coli_moe_dbg_stream_read: one launch reading the forward's algorithmic "
                                        "bytes through bulk copies into per-block shared-memory rings, no "
-                                       "arithmetic, L2 flushed, median of 20"}
+                                       "arithmetic, L2 flushed, mean of 20"}
         del buf, sink
     if rank == 0 and not args.no_cpu_baseline:
         nf = args.cpu_forwards if T <= 64 else 1
@@ -551,7 +554,62 @@ def measure_tier(args, wl, L, router_b, world, rank, local, n_slots=64):
 # sub-records of the default decode run: the verify batch and the prefill on
 # the same resident weights, the decode layer with int8-container experts, the
 # decode layer with its experts in host memory, and the stacked-layer sweep
-SUB_WORKLOADS = ("verify", "prefill", "decode_int8", "tier", "sweep")
+SUB_WORKLOADS = ("verify", "prefill", "decode_int8", "tier", "stream", "sweep")
+
+
+def measure_stream(n_bytes: int, big_bytes: int = 1200 << 20):
+    """The single-launch read rate of this GPU: coli_moe_dbg_stream_read over
+    n_bytes (the decode forward's algorithmic bytes) for a grid of copy
+    sizes, ring depths and blocks per SM, and over big_bytes for a few, each
+    the median of 5 launches (after 2) with L2 flushed before each.  The best
+    single-launch read of n_bytes is the ceiling of any one-launch kernel that
+    reads them; the large read shows the per-launch cost that sets it."""
+    import torch
+
+    import int4_routed_expert_f32_gb300 as coli
+
+    hbm_peak, _, peak_kind = peaks()
+    smem_sm = torch.cuda.get_device_properties(0).shared_memory_per_multiprocessor
+    buf = torch.ones(big_bytes // 4, dtype=torch.int32, device="cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.empty(1, dtype=torch.int64, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def timed(nb, chunk, stages, bps):
+        ts = []
+        for i in range(12):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(st)
+            coli.dbg_stream_read(buf, n_bytes=nb, sum_out=sink, chunk=chunk, stages=stages, blocks_per_sm=bps)
+            b_.record(st)
+            ts.append((a_, b_))
+        torch.cuda.synchronize()
+        # the mean: this GPU's event timestamps step by about 2 us, so a
+        # median of a few launches lands on one of those steps
+        ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in ts[2:]]))
+        gbs = nb / (ms * 1e-3) / 1e9
+        return {"chunk": chunk, "stages": stages, "blocks_per_sm": bps, "us": round(ms * 1e3, 2),
+                "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)}
+
+    nb = n_bytes // 16 * 16
+    grid = []
+    for chunk in (8192, 16384, 32768):
+        for stages in (2, 3, 4, 6):
+            for bps in (1, 2, 3, 4, 6):
+                if bps * (chunk * stages + 2048) > smem_sm or chunk * stages > 200 * 1024:
+                    continue
+                grid.append(timed(nb, chunk, stages, bps))
+    best = max(grid, key=lambda r: r["gbs"])
+    default = next(r for r in grid if (r["chunk"], r["stages"], r["blocks_per_sm"]) == (16384, 3, 3))
+    big = [timed(big_bytes, c, s_, b) for c, s_, b in ((16384, 3, 3), (32768, 2, 3), (32768, 3, 2))]
+    del buf, flush, sink
+    torch.cuda.empty_cache()
+    return {"bytes": nb, "peak": hbm_peak, "peak_kind": f"{peak_kind} hbm_gbs", "best": best,
+            "expert_kernel_arrangement": default, "configs": grid,
+            "large_read": {"bytes": big_bytes, "configs": big},
+            "what": "coli_moe_dbg_stream_read: one launch, bulk copies into per-block shared-memory rings, no "
+                    "arithmetic; CUDA events around the launch, L2 flushed before each, mean of 10"}
 
 
 def run(args):
@@ -579,6 +637,8 @@ def run(args):
                 del L
                 torch.cuda.empty_cache()
                 rec = measure_sweep(args, world, rank, local, args.cpu_seconds / 2)
+            elif name == "stream":
+                rec = measure_stream(int(line["roofline"]["algorithmic_bytes_per_launch"]))
             elif name == "tier":
                 rec = measure_tier(args, wl, L, torch.from_numpy(b).cuda(), world, rank, local)
             elif name == "decode_int8":

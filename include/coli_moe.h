@@ -356,15 +356,20 @@ int coli_moe_dbg_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *
                                void *stream);
 
 /* Measurement reference (needs no configure): one launch that streams `bytes`
- * bytes of the device buffer `buf` from HBM through bulk copies into per-block
- * shared-memory rings (three blocks of 48 KB per SM, the expert kernel's
- * arrangement) and does no arithmetic on them but a checksum: *sum (a device
- * u64, zeroed by the call) receives the sum of the four 32-bit words at every
- * offset o < bytes with o % 1024 == 0.  buf 16-byte aligned, bytes % 16 == 0,
- * sum 8-byte aligned; otherwise COLI_E_INVAL.  Its duration is the single-pass
- * read time of that many bytes, the floor against which the streaming expert
- * kernel's bandwidth is read. */
-int coli_moe_dbg_stream_read(const void *buf, size_t bytes, unsigned long long *sum, void *stream);
+ * bytes of the device buffer `buf` from HBM through bulk copies of `chunk`
+ * bytes into per-block shared-memory rings of `stages` chunks, with
+ * `blocks_per_sm` blocks per SM, each block a contiguous range, and does no
+ * arithmetic on the data but a checksum: *sum (a device u64, zeroed by the
+ * call) receives the sum of the four 32-bit words at every offset o < bytes
+ * with o % 1024 == 0.  0 for chunk, stages or blocks_per_sm takes the expert
+ * kernel's arrangement (16384, 3, 3).  Limits: chunk 1024..65536 in steps of
+ * 1024, stages 2..16, chunk * stages <= 200 KB, blocks_per_sm >= 1 and all
+ * blocks resident; buf 16-byte aligned, bytes % 16 == 0, sum 8-byte aligned;
+ * otherwise COLI_E_INVAL.  Its duration is the single-pass read time of that
+ * many bytes, the floor against which the streaming expert kernel's
+ * bandwidth is read. */
+int coli_moe_dbg_stream_read(const void *buf, size_t bytes, int chunk, int stages, int blocks_per_sm,
+                             unsigned long long *sum, void *stream);
 
 /* Run a full forward and copy out its intermediates (any pointer may be NULL):
  * qx [n_tok][H] int8, dx [n_tok][H/32], idx/w [n_tok][k],

@@ -99,7 +99,7 @@ def _load():
         "coli_moe_tier_forward": ([P, i, P, P, P, P, P, P, P, P], i),
         "coli_moe_tier_stats": ([ctypes.POINTER(ctypes.c_longlong)] * 3 + [ctypes.POINTER(ctypes.c_int)], i),
         "coli_moe_tier_release": ([], None),
-        "coli_moe_dbg_stream_read": ([P, ctypes.c_size_t, P, P], i),
+        "coli_moe_dbg_stream_read": ([P, ctypes.c_size_t, i, i, i, P, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -248,6 +248,30 @@ def layer_forward_hostio(x_host, router_w, router_bias, expert_w4, expert_rowsca
                                               _stream(stream)),
            "layer_forward_hostio")
     return out_host
+
+
+class PreparedLayer:
+    """One layer's device weights, checked and converted to C arguments once,
+    for repeated forwards: the per-call marshalling is then the activation and
+    output pointers only.  The tensors are kept alive by the object; they must
+    not be resized or moved while it is used."""
+
+    def __init__(self, router_w, router_bias, expert_w4, expert_rowscale, shared_w4, shared_rowscale):
+        self._tensors = (router_w, router_bias, expert_w4, expert_rowscale, shared_w4, shared_rowscale)
+        self._w = tuple(ctypes.c_void_p(_ptr(t)) for t in self._tensors)
+
+    def forward(self, x, out=None, stream=None):
+        if out is None:
+            out = torch.empty_like(x)
+        n_tok = x.shape[0] if x.dim() == 2 else 0
+        _check(_lib.coli_moe_layer_forward(_ptr(x), n_tok, *self._w, _ptr(out), _stream(stream)), "layer_forward")
+        return out
+
+    def forward_hostio(self, x_host, out_host, stream=None):
+        _check(_lib.coli_moe_layer_forward_hostio(_host_ptr(x_host), x_host.shape[0], *self._w,
+                                                  _host_ptr(out_host), _stream(stream)),
+               "layer_forward_hostio")
+        return out_host
 
 
 def get_device_status(stream=None) -> int:
@@ -403,14 +427,16 @@ def dbg_block_dots_w8(w8, q, stream=None):
     return I
 
 
-def dbg_stream_read(buf, n_bytes=None, sum_out=None, stream=None):
+def dbg_stream_read(buf, n_bytes=None, sum_out=None, chunk=0, stages=0, blocks_per_sm=0, stream=None):
     """One bare read of the first n_bytes of the device tensor buf (default:
-    all of it) in one launch; returns the device u64 checksum tensor (the sum
-    of the four 32-bit words at every 1024-byte offset)."""
+    all of it) in one launch (chunk / stages / blocks_per_sm 0: the expert
+    kernel's arrangement); returns the device u64 checksum tensor (the sum of
+    the four 32-bit words at every 1024-byte offset)."""
     nb = buf.numel() * buf.element_size() if n_bytes is None else int(n_bytes)
     if sum_out is None:
         sum_out = torch.empty(1, dtype=torch.int64, device=buf.device)
-    _check(_lib.coli_moe_dbg_stream_read(_ptr(buf), nb, _ptr(sum_out), _stream(stream)), "dbg_stream_read")
+    _check(_lib.coli_moe_dbg_stream_read(_ptr(buf), nb, chunk, stages, blocks_per_sm, _ptr(sum_out),
+                                         _stream(stream)), "dbg_stream_read")
     return sum_out
 
 

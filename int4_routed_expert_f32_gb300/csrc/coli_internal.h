@@ -131,8 +131,8 @@ int launch_pack_int4(const float *w, int rows, int K, uint8_t *packed, float *sc
 int launch_pack_int8(const float *w, int rows, int K, int8_t *q, float *scale, cudaStream_t st);
 int launch_block_dots(const uint8_t *w4, int rows, int K, const int8_t *q, int32_t *I, cudaStream_t st);
 int launch_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *q, int32_t *I, cudaStream_t st);
-int launch_stream_read(const void *buf, size_t bytes, unsigned long long *sum, int *status, int num_sms,
-                       cudaStream_t st);
+int launch_stream_read(const void *buf, size_t bytes, int chunk, int stages, int blocks_per_sm,
+                       unsigned long long *sum, int *status, int num_sms, cudaStream_t st);
 
 int launch_router_logits(const float *x, int T, int H, const float *W, int E, float *logits,
                          cudaStream_t st);

@@ -1007,16 +1007,27 @@ int coli_moe_dbg_rmsnorm(const float *x, int n_tok, int hidden, float *xn, void 
     return COLI_OK;
 }
 
-int coli_moe_dbg_stream_read(const void *buf, size_t bytes, unsigned long long *sum, void *stream)
+int coli_moe_dbg_stream_read(const void *buf, size_t bytes, int chunk, int stages, int blocks_per_sm,
+                             unsigned long long *sum, void *stream)
 {
     if (!buf || !sum || !aligned16(buf) || bytes % 16 != 0 || ((uintptr_t)sum & 7) != 0) return COLI_E_INVAL;
+    if (chunk == 0) chunk = 16384;
+    if (stages == 0) stages = 3;
+    if (blocks_per_sm == 0) blocks_per_sm = 3;
+    // chunks of 1-64 KB in 1 KB steps, 2-16 stages, at most 200 KB of ring per block
+    if (chunk < 1024 || chunk > 65536 || chunk % 1024 != 0 || stages < 2 || stages > 16 ||
+        (long)chunk * stages > 200L * 1024 || blocks_per_sm < 1 || blocks_per_sm > 32)
+        return COLI_E_INVAL;
     cudaStream_t s = (cudaStream_t)stream;
-    CUDA_OK(cudaMemsetAsync(sum, 0, sizeof(unsigned long long), s));
-    if (bytes == 0) return COLI_OK;
-    int dev = 0, sms = 0;
+    int dev = 0, sms = 0, smem_sm = 0;
     CUDA_OK(cudaGetDevice(&dev));
     CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    LAUNCH_OK(launch_stream_read(buf, bytes, sum, nullptr, sms, s));
+    CUDA_OK(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+    // every block resident at once (1 KB of each block's shared memory is the system's)
+    if ((long)blocks_per_sm * ((long)chunk * stages + 2048) > smem_sm) return COLI_E_INVAL;
+    CUDA_OK(cudaMemsetAsync(sum, 0, sizeof(unsigned long long), s));
+    if (bytes == 0) return COLI_OK;
+    LAUNCH_OK(launch_stream_read(buf, bytes, chunk, stages, blocks_per_sm, sum, nullptr, sms, s));
     return COLI_OK;
 }
 

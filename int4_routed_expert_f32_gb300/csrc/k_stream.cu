@@ -7,10 +7,12 @@
 // is bounded by its ramp and tail, not only by the HBM copy rate measured on
 // gigabyte buffers.
 //
-// Each block streams one contiguous range of 16 KB chunks; the consumer reads
-// the first 16 bytes of every 1 KB of each chunk and adds their four 32-bit
-// words into a 64-bit sum, so that the call's result can be checked on the
-// host and the copies cannot be elided.
+// Each block streams one contiguous range of chunks (one bulk copy each, a
+// ring of `stages` of them); the consumer reads the first 16 bytes of every
+// 1 KB of each chunk and adds their four 32-bit words into a 64-bit sum, so
+// that the call's result can be checked on the host and the copies cannot be
+// elided.  Chunk size, ring depth and blocks per SM are parameters, so that
+// the same call sweeps the read's configurations.
 #include <cuda.h>
 
 #include "coli_common.cuh"
@@ -19,8 +21,7 @@
 
 namespace coli {
 
-constexpr int S_CHUNK = 16384;      // bytes per bulk copy (one ring stage)
-constexpr int S_STAGES = 3;
+constexpr int S_MAX_STAGES = 16;
 constexpr int S_THREADS = 64;       // warp 0 lane 0: producer; warp 1: consumer
 constexpr uint64_t S_WAIT_NS = 2000000000ull;
 
@@ -50,18 +51,18 @@ __device__ __forceinline__ bool s_wait(uint64_t *bar, uint32_t parity)
 }
 
 __global__ void __launch_bounds__(S_THREADS)
-k_stream_read(const unsigned char *__restrict__ buf, size_t bytes, unsigned long long *sum, int *status)
+k_stream_read(const unsigned char *__restrict__ buf, size_t bytes, int chunk, int stages, unsigned long long *sum,
+              int *status)
 {
-    extern __shared__ __align__(128) unsigned char s_ring[];   // [S_STAGES][S_CHUNK]
-    unsigned char(*ring)[S_CHUNK] = reinterpret_cast<unsigned char(*)[S_CHUNK]>(s_ring);
-    __shared__ __align__(8) uint64_t full[S_STAGES], empty[S_STAGES];
+    extern __shared__ __align__(128) unsigned char ring[];     // [stages][chunk]
+    __shared__ __align__(8) uint64_t full[S_MAX_STAGES], empty[S_MAX_STAGES];
     __shared__ int abort_flag;
-    const size_t n_chunks = (bytes + S_CHUNK - 1) / S_CHUNK;
+    const size_t n_chunks = (bytes + chunk - 1) / chunk;
     const size_t per = (n_chunks + gridDim.x - 1) / gridDim.x;
     const size_t c0 = (size_t)blockIdx.x * per;
     const size_t c1 = c0 + per < n_chunks ? c0 + per : n_chunks;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S_STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -73,18 +74,18 @@ k_stream_read(const unsigned char *__restrict__ buf, size_t bytes, unsigned long
     if (warp == 0) {
         if (lane == 0) {
             for (size_t c = c0; c < c1; ++c) {
-                const int i = (int)(c - c0), slot = i % S_STAGES;
-                if (i >= S_STAGES && !s_wait(&empty[slot], (uint32_t)(((i / S_STAGES) - 1) & 1))) {
+                const int i = (int)(c - c0), slot = i % stages;
+                if (i >= stages && !s_wait(&empty[slot], (uint32_t)(((i / stages) - 1) & 1))) {
                     set_status(status, ST_TIMEOUT);
                     abort_flag = 1;
                     // complete the consumer's pending phase without data
                     mbar_arrive(&full[slot]);
                     break;
                 }
-                const size_t off = c * S_CHUNK;
-                const uint32_t n = (uint32_t)(bytes - off < (size_t)S_CHUNK ? bytes - off : (size_t)S_CHUNK);
+                const size_t off = c * (size_t)chunk;
+                const uint32_t n = (uint32_t)(bytes - off < (size_t)chunk ? bytes - off : (size_t)chunk);
                 mbar_arrive_expect_tx(&full[slot], n);
-                bulk_load(ring[slot], buf + off, n, &full[slot]);
+                bulk_load(ring + (size_t)slot * chunk, buf + off, n, &full[slot]);
             }
         }
         return;
@@ -92,16 +93,16 @@ k_stream_read(const unsigned char *__restrict__ buf, size_t bytes, unsigned long
     // consumer warp
     unsigned long long acc = 0;
     for (size_t c = c0; c < c1; ++c) {
-        const int i = (int)(c - c0), slot = i % S_STAGES;
-        if (!s_wait(&full[slot], (uint32_t)((i / S_STAGES) & 1))) {
+        const int i = (int)(c - c0), slot = i % stages;
+        if (!s_wait(&full[slot], (uint32_t)((i / stages) & 1))) {
             if (lane == 0) set_status(status, ST_TIMEOUT);
             break;
         }
         if (abort_flag) break;
-        const size_t off = c * S_CHUNK;
-        const size_t n = bytes - off < (size_t)S_CHUNK ? bytes - off : (size_t)S_CHUNK;
-        if (lane < S_CHUNK / 1024 && (size_t)lane * 1024 < n) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(ring[slot] + lane * 1024);
+        const size_t off = c * (size_t)chunk;
+        const size_t n = bytes - off < (size_t)chunk ? bytes - off : (size_t)chunk;
+        for (int o = lane * 1024; (size_t)o < n; o += 32 * 1024) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(ring + (size_t)slot * chunk + o);
             acc += (unsigned long long)v.x + v.y + v.z + v.w;
         }
         __syncwarp();
@@ -112,20 +113,19 @@ k_stream_read(const unsigned char *__restrict__ buf, size_t bytes, unsigned long
     if (lane == 0) atomicAdd(sum, acc);
 }
 
-int launch_stream_read(const void *buf, size_t bytes, unsigned long long *sum, int *status, int num_sms,
-                       cudaStream_t st)
+int launch_stream_read(const void *buf, size_t bytes, int chunk, int stages, int blocks_per_sm,
+                       unsigned long long *sum, int *status, int num_sms, cudaStream_t st)
 {
     if (bytes == 0) return 0;
-    // three blocks per SM, like the expert kernel (48 KB of ring each)
-    constexpr int smem = S_STAGES * S_CHUNK;
-    static bool configured = false;
-    if (!configured) {
+    const int smem = chunk * stages;
+    static int configured = 0;
+    if (smem > configured) {
         if (cudaFuncSetAttribute(k_stream_read, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return -1;
-        configured = true;
+        configured = smem;
     }
-    k_stream_read<<<num_sms * 3, S_THREADS, smem, st>>>(static_cast<const unsigned char *>(buf), bytes, sum,
-                                                         status);
+    k_stream_read<<<num_sms * blocks_per_sm, S_THREADS, smem, st>>>(static_cast<const unsigned char *>(buf), bytes,
+                                                                      chunk, stages, sum, status);
     count_launch();
     return 0;
 }

@@ -89,12 +89,17 @@ def test_injection_kinds_are_checked(lib):
 
 def test_stream_read_argument_checks(lib):
     """The bare-read reference rejects unaligned buffers, sizes that are not a
-    multiple of 16 and unaligned result pointers before touching the device."""
+    multiple of 16, unaligned result pointers and out-of-range ring shapes
+    before touching the device."""
     import int4_routed_expert_f32_gb300 as coli
     L = coli.lib()
-    aligned, sink = 1 << 20, 1 << 21          # never dereferenced: rejected first
-    assert L.coli_moe_dbg_stream_read(None, 16, sink, None) == coli.E_INVAL
-    assert L.coli_moe_dbg_stream_read(aligned + 8, 16, sink, None) == coli.E_INVAL
-    assert L.coli_moe_dbg_stream_read(aligned, 24, sink, None) == coli.E_INVAL
-    assert L.coli_moe_dbg_stream_read(aligned, 16, sink + 4, None) == coli.E_INVAL
-    assert L.coli_moe_dbg_stream_read(aligned, 16, None, None) == coli.E_INVAL
+    a, sink = 1 << 20, 1 << 21          # never dereferenced: rejected first
+    assert L.coli_moe_dbg_stream_read(None, 16, 0, 0, 0, sink, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(a + 8, 16, 0, 0, 0, sink, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(a, 24, 0, 0, 0, sink, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(a, 16, 0, 0, 0, sink + 4, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(a, 16, 0, 0, 0, None, None) == coli.E_INVAL
+    assert L.coli_moe_dbg_stream_read(a, 16, 1000, 0, 0, sink, None) == coli.E_INVAL    # not 1 KB steps
+    assert L.coli_moe_dbg_stream_read(a, 16, 0, 1, 0, sink, None) == coli.E_INVAL       # one stage
+    assert L.coli_moe_dbg_stream_read(a, 16, 65536, 4, 0, sink, None) == coli.E_INVAL   # 256 KB ring
+    assert L.coli_moe_dbg_stream_read(a, 16, 0, 0, -1, sink, None) == coli.E_INVAL

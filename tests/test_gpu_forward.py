@@ -99,6 +99,23 @@ def test_tiny_hostio_matches_device_call(coli, tiny):
     np.testing.assert_array_equal(oh.numpy(), ref.forward(x))
 
 
+def test_prepared_layer_matches_the_plain_calls(coli, tiny):
+    """PreparedLayer marshals the weights once; its device and host-I/O
+    forwards give the oracle's output bit for bit, over several inputs."""
+    wl, L, ref = tiny
+    _configure(coli, wl, 8)
+    layer = coli.PreparedLayer(L["router_w"], L["router_b"], L["expert_w4"], L["expert_rs"], L["shared_w4"],
+                               L["shared_rs"])
+    oh = torch.empty((4, wl.hidden)).pin_memory()
+    for step in range(3):
+        x = synth.activations(wl, 70 + step, n_tok=4)
+        want = ref.forward(x)
+        np.testing.assert_array_equal(layer.forward(_cuda(x)).cpu().numpy(), want)
+        layer.forward_hostio(torch.from_numpy(x).pin_memory(), oh)
+        np.testing.assert_array_equal(oh.numpy(), want)
+    assert coli.get_device_status() == coli.OK
+
+
 @pytest.mark.parametrize("path", ["gemv", "gemm"])
 def test_hostio_pinned_and_pageable_outputs(coli, tiny, path):
     """Pinned (device-mapped) output buffers receive the combine's stores

