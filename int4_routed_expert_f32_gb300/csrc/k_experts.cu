@@ -52,10 +52,24 @@ constexpr int KC_MAX = 128;
 constexpr int NSUB_MAX = 2;                        // TMA boxes along K per stage
 constexpr int SUB_BYTES = STAGE_ROWS * KC_MAX;     // 8 KB: one box of 64 rows x 128 B
 constexpr int STAGE_BYTES = NSUB_MAX * SUB_BYTES;  // 16 KB
-constexpr int CONSUMER_WARPS = 2;
-constexpr int CONSUMERS = CONSUMER_WARPS * 32;     // one lane per stage row
-constexpr int EXPERT_THREADS = CONSUMERS + 32;
 constexpr int BAR_CONSUMERS = 1;                   // named barrier id (0 = __syncthreads)
+
+// Consumer warps of a block: two (lane r of warp w owns weight row 32w + r of
+// each stage) for one-token tiles; four for multi-token tiles, where each pair
+// of warps takes half of the tile's tokens over the same 64 rows.  Multi-token
+// tiles are bound by the block dots' issue rate (each weight feeds a dp4a
+// chain per token), so twice the warps issue them, with no exchange between
+// the pairs: every (row, token) fold stays in one lane.
+template <int MT> struct Cons {
+    static constexpr int WARPS = MT >= 2 ? 4 : 2;
+    static constexpr int N = WARPS * 32;            // consumer threads
+    static constexpr int THREADS = N + 32;          // and the producer warp
+    static constexpr int PAIRS = WARPS / 2;
+    static constexpr int TP = MT / PAIRS;           // tokens per pair
+    // three blocks per SM (as shared memory allows): for the 160-thread blocks
+    // this bounds the registers to 136
+    static constexpr int MIN_BLOCKS = 3;
+};
 constexpr uint64_t WAIT_NS = 2000000000ull;        // 2 s bound on every ring wait
 
 __device__ __forceinline__ uint64_t globaltimer()
@@ -172,6 +186,7 @@ __device__ __forceinline__ void stage_acts(const int8_t *__restrict__ q, const f
                                            uint4 *xlo, uint4 *xhi, int2 *xcd, int *status)
 {
     constexpr int SU = 4;
+    constexpr int CONSUMERS = Cons<MT>::N;
     const int NB = K / 32;
     for (int i0 = threadIdx.x; i0 < MT * NB; i0 += CONSUMERS * SU) {
         uint4 va[SU], vb[SU];
@@ -256,45 +271,56 @@ __device__ __forceinline__ int block_dot_i8(uint4 w0, uint4 w1, uint4 lo, uint4 
 // row's eight chunk offsets in the box).  All trip counts are compile-time
 // constants, so the block dots form one straight-line region the scheduler
 // can interleave.
-template <int MT, int NSUB, int BPS, int WB>
+template <int TP, int NSUB, int BPS, int WB>
 __device__ __forceinline__ void stage_rows(const unsigned char *base, const int (&woff)[8], const uint4 *xlo,
-                                           const uint4 *xhi, const int2 *xcd, int NB, int b0, int m,
-                                           float (&acc)[MT])
+                                           const uint4 *xhi, const int2 *xcd, int NB, int b0, int t0, int m,
+                                           float (&acc)[TP])
 {
     constexpr int CPB = WB == 4 ? 1 : 2;
-    uint4 wv[NSUB][BPS][CPB];
+    // One token: the whole stage's bytes in registers, then its block dots
+    // and fold.  Several tokens: one box (half a stage) at a time, every
+    // token's dots and fold for it, then the next box -- each token still
+    // folds its blocks in ascending order, and the row's bytes are loaded
+    // once for all tokens without holding the whole stage in registers.
+    constexpr int NCH = TP == 1 ? NSUB : 1;      // boxes whose bytes are held at once
 #pragma unroll
-    for (int c = 0; c < NSUB; ++c)
+    for (int c0 = 0; c0 < NSUB; c0 += NCH) {
+        uint4 wv[NCH][BPS][CPB];
 #pragma unroll
-        for (int jj = 0; jj < BPS; ++jj)
+        for (int c = 0; c < NCH; ++c)
 #pragma unroll
-            for (int p = 0; p < CPB; ++p)
-                wv[c][jj][p] = *reinterpret_cast<const uint4 *>(base + c * SUB_BYTES + woff[jj * CPB + p]);
+            for (int jj = 0; jj < BPS; ++jj)
 #pragma unroll
-    for (int t = 0; t < MT; ++t) {
-        if (t < m) {
-            const int xb0 = t * NB + b0;
-            int I[NSUB][BPS];
-            float dd[NSUB][BPS];
+                for (int p = 0; p < CPB; ++p)
+                    wv[c][jj][p] =
+                        *reinterpret_cast<const uint4 *>(base + (c0 + c) * SUB_BYTES + woff[jj * CPB + p]);
 #pragma unroll
-            for (int c = 0; c < NSUB; ++c)
+        for (int tt = 0; tt < TP; ++tt) {
+            const int t = t0 + tt;
+            if (t < m) {
+                const int xb0 = t * NB + b0 + c0 * BPS;
+                int I[NCH][BPS];
+                float dd[NCH][BPS];
 #pragma unroll
-                for (int jj = 0; jj < BPS; ++jj) {
-                    const int xb = xb0 + c * BPS + jj;
-                    const int2 cd = xcd[xb];
-                    if (WB == 4)
-                        I[c][jj] = block_dot_i(wv[c][jj][0], xlo[xb], xhi[xb], cd.x);
-                    else
-                        I[c][jj] = block_dot_i8(wv[c][jj][0], wv[c][jj][CPB - 1], xlo[xb], xhi[xb], cd.x);
-                    dd[c][jj] = __int_as_float(cd.y);
-                }
-            float cacc = acc[t];
+                for (int c = 0; c < NCH; ++c)
 #pragma unroll
-            for (int c = 0; c < NSUB; ++c)
+                    for (int jj = 0; jj < BPS; ++jj) {
+                        const int xb = xb0 + c * BPS + jj;
+                        const int2 cd = xcd[xb];
+                        if (WB == 4)
+                            I[c][jj] = block_dot_i(wv[c][jj][0], xlo[xb], xhi[xb], cd.x);
+                        else
+                            I[c][jj] = block_dot_i8(wv[c][jj][0], wv[c][jj][CPB - 1], xlo[xb], xhi[xb], cd.x);
+                        dd[c][jj] = __int_as_float(cd.y);
+                    }
+                float cacc = acc[tt];
 #pragma unroll
-                for (int jj = 0; jj < BPS; ++jj)
-                    cacc = __fmaf_rn(dd[c][jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
-            acc[t] = cacc;
+                for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                    for (int jj = 0; jj < BPS; ++jj)
+                        cacc = __fmaf_rn(dd[c][jj], __int_as_float(I[c][jj]) - MAGIC_F, cacc);
+                acc[tt] = cacc;
+            }
         }
     }
 }
@@ -326,9 +352,12 @@ __device__ __forceinline__ void decode_unit(long u, long n_gu, int G, int CH, bo
 // 128, 64 or 16; int8: 4, 2 or 1 for KC = 128, 64 or 32).
 // WB: weight container, 4 (packed nibbles) or 8 (one int8 code per byte).
 template <int MT, int BPS, int WB>
-__global__ void __launch_bounds__(EXPERT_THREADS)
+__global__ void __launch_bounds__(Cons<MT>::THREADS, Cons<MT>::MIN_BLOCKS)
 k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 {
+    constexpr int CONSUMER_WARPS = Cons<MT>::WARPS;
+    constexpr int CONSUMERS = Cons<MT>::N;
+    constexpr int TP = Cons<MT>::TP;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled TMA boxes, by pointer arithmetic on
     // the shared array itself so that every access stays a shared-memory access
@@ -483,7 +512,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     }
 
     // -------------------------------- consumers --------------------------------
-    const int r = threadIdx.x;                // this lane's weight row in the stage (0..63)
+    const int r = threadIdx.x & 63;           // this lane's weight row in the stage (0..63)
+    const int t0 = (threadIdx.x >> 6) * TP;   // this pair's first token of a tile
+    const int half = warp & 1;                // rows 0..31 (gate rows of a gate/up unit) or 32..63
     const bool swz = (KC == 128);
     int woff[8];
 #pragma unroll
@@ -497,9 +528,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 #pragma unroll
     for (int t = 0; t < GEMV_MT; ++t) staged_tok[t] = -1;
     trace_event(a, 1, -1);
-    float acc[MT];
+    float acc[TP];
 #pragma unroll
-    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < TP; ++t) acc[t] = 0.0f;
     bool gu = true;
     int tile = 0, j = 0, e = 0, pos0 = 0, m = 0, nst = 0, NB = 0, nsub = 1;
     const float *ers = nullptr;
@@ -560,7 +591,7 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                 trace_event(a, 3, u);
             }
 #pragma unroll
-            for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+            for (int t = 0; t < TP; ++t) acc[t] = 0.0f;
         }
 
         // ---- one stage: this lane's row, blocks b0 .. b0 + nsub * BPS - 1, in order ----
@@ -568,9 +599,9 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
             const unsigned char *base = ring + slot * STAGE_BYTES;
             const int b0 = s * nsub * BPS;
             if (nsub == 2)
-                stage_rows<MT, 2, BPS, WB>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
+                stage_rows<TP, 2, BPS, WB>(base, woff, xlo, xhi, xcd, NB, b0, t0, m, acc);
             else
-                stage_rows<MT, 1, BPS, WB>(base, woff, xlo, xhi, xcd, NB, b0, m, acc);
+                stage_rows<TP, 1, BPS, WB>(base, woff, xlo, xhi, xcd, NB, b0, t0, m, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -582,18 +613,22 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
 
         // ---- unit epilogue ----
         if (gu) {
-            // rows 0..31: gate rows 32j.., rows 32..63: the matching up rows
-            if (warp == 1)
-                for (int t = 0; t < m; ++t) red[t * 32 + lane] = acc[t];
+            // rows 0..31: gate rows 32j.., rows 32..63: the matching up rows;
+            // each pair of warps finishes its own tokens
+            if (half == 1)
+#pragma unroll
+                for (int tt = 0; tt < TP; ++tt)
+                    if (t0 + tt < m) red[(t0 + tt) * 32 + lane] = acc[tt];
             named_barrier(BAR_CONSUMERS, CONSUMERS);
-            if (warp == 0) {
+            if (half == 0) {
                 const int ii = 32 * j + lane;
                 const float sg = ers[ii], su = ers[F + ii];
 #pragma unroll
-                for (int t = 0; t < MT; ++t) {
+                for (int tt = 0; tt < TP; ++tt) {
+                    const int t = t0 + tt;
                     if (t < m) {
                         const int pos = pos0 + t;
-                        const float gg = __fmul_rn(sg, acc[t]);
+                        const float gg = __fmul_rn(sg, acc[tt]);
                         const float uu = __fmul_rn(su, red[t * 32 + lane]);
                         const float h = __fmul_rn(__fmul_rn(gg, own_sigmoid(gg)), uu);
                         float dq;
@@ -603,17 +638,17 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
                         if (a.h_dbg) a.h_dbg[(size_t)pos * F + ii] = h;
                     }
                 }
-                __syncwarp();
-                if (lane == 0) red_release_gpu(&a.g_done[tile], 1);
             }
-            named_barrier(BAR_CONSUMERS, CONSUMERS);   // red[] is reused by the next unit
+            named_barrier(BAR_CONSUMERS, CONSUMERS);   // h is written; red[] is reused by the next unit
+            // every consumer's h stores precede this release (the barrier)
+            if (threadIdx.x == 0) red_release_gpu(&a.g_done[tile], 1);
             trace_event(a, 4, u);
         } else {
             const int row = 64 * j + r;
             const float sd = ers[2 * F + row];
 #pragma unroll
-            for (int t = 0; t < MT; ++t)
-                if (t < m) a.y[(size_t)(pos0 + t) * H + row] = __fmul_rn(sd, acc[t]);
+            for (int tt = 0; tt < TP; ++tt)
+                if (t0 + tt < m) a.y[(size_t)(pos0 + t0 + tt) * H + row] = __fmul_rn(sd, acc[tt]);
             named_barrier(BAR_CONSUMERS, CONSUMERS);
             if (threadIdx.x == 0) {
                 __threadfence();
@@ -688,7 +723,7 @@ static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int
         if (cudaFuncSetAttribute(k_experts<MT, BPS, WB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return -1;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k_experts<MT, BPS, WB>, EXPERT_THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k_experts<MT, BPS, WB>, Cons<MT>::THREADS,
                                                           smem) != cudaSuccess ||
             blocks_per_sm < 1)
             return -1;
@@ -697,7 +732,7 @@ static int launch_experts_mt(const ExpertMaps &maps, const ExpertArgs &a_in, int
     // every block must be resident: down units wait on gate/up units of others
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms * blocks_per_sm);
-    cfg.blockDim = dim3(EXPERT_THREADS);
+    cfg.blockDim = dim3(Cons<MT>::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
