@@ -56,8 +56,8 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "d4388ee398f0753c37bf96d151725ffcb2840a69876c23c6e629e54129f2a774",
-        "bytes_per_launch": 171012096,   # 170.94 MB read + 0.07 MB written (median of three launches)
+        "sha256": "7ee7199e34dcef1f4292c84062a8444f4d76087093a74086f6b4dbfa774f757b",
+        "bytes_per_launch": 170990848,   # the median of three launches: 170.66 MB read + 0.33 MB written
         # a decode forward streams 8 routed + 1 shared expert; the capture ran
         # the decode workload itself
         "workloads": ("decode", "profile"),
@@ -65,7 +65,7 @@ TRAFFIC = {
     },
     "k_gemm_gateup": {
         "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "351881951d6db66c91ddb37435404225509274ec537f86dacadc48b4e7340e5c",
+        "sha256": "a3fa9b920d0525c9277e3f757eedea6d9121e4b0ef6d94cce555ba5d155ca998",
         "bytes_per_launch": 5379424000,  # 5284.00 MB read + 95.43 MB written
         "workloads": ("prefill",),
         "capture": "profiles/prefill_layer_launches.md",
