@@ -59,6 +59,7 @@ class Workload:
     zipf_s: float = 1.1
     layers: int = 1
     layer_corr: float = 0.0              # sweep: router rows correlated across layers
+    down_scale: float = 1.0              # a power of two multiplying the down rows' draw
     batches: tuple = ()
     weight_seed: int | None = None       # seed of the layer's weights (default: seed)
 
@@ -91,6 +92,13 @@ ZIPF_BETA = 0.16
 # 69.6% in the calibration run, 0.67 on the 128 normalised tokens of the
 # input-recipe test).
 SWEEP_LAYER_CORR = 0.97
+# The sweep's down rows are drawn at N(0, 0.02) x 1/32: each layer's residual
+# update is then ~6% of the stream, as in a trained stack, so consecutive
+# layers see nearly the same normalised input and route it alike (0.65 of the
+# top-8 shared at 1/16, 0.68 at 1/64, 0.42 at full size, where every random
+# layer rewrites the stream).  A power of two: the int4 codes are unchanged,
+# only the row scales are.
+SWEEP_DOWN_SCALE = 1.0 / 32
 
 WORKLOADS = {
     "tiny": Workload("tiny", 256, 128, 8, 2, 4, 0),
@@ -116,7 +124,7 @@ WORKLOADS = {
     "prefill_profile": Workload("prefill_profile", 6144, 2048, 16, 8, 256, 3, norm_jitter=True,
                                 weight_seed=1),
     "sweep": Workload("sweep", 6144, 2048, 256, 8, 128, 100, zipf_beta=ZIPF_BETA, layers=8,
-                      layer_corr=SWEEP_LAYER_CORR, batches=(1, 8, 32, 128)),
+                      layer_corr=SWEEP_LAYER_CORR, down_scale=SWEEP_DOWN_SCALE, batches=(1, 8, 32, 128)),
 }
 
 
@@ -171,9 +179,8 @@ def router(wl: Workload, layer: int = 0):
 def expert_f32(wl: Workload, e: int, layer: int = 0):
     """F32 weights of expert ``e`` (``e == n_experts`` is the shared expert):
     gate [F][H], up [F][H], down [H][F]."""
-    s = wl.layer_seed(layer)
+    a = expert_f32_rows(wl, e, layer)
     F, H = wl.ffn, wl.hidden
-    a = normal((3 * F * H,), 0.02, s, _T_EXPERT, e)
     return a[: F * H].reshape(F, H), a[F * H: 2 * F * H].reshape(F, H), a[2 * F * H:].reshape(H, F)
 
 
@@ -182,7 +189,10 @@ def expert_f32_rows(wl: Workload, e: int, layer: int = 0) -> np.ndarray:
     order (gate rows, up rows, down rows); rows are ragged (H or F long), so this
     returns the flat F32 buffer."""
     s = wl.layer_seed(layer)
-    return normal((3 * wl.ffn * wl.hidden,), 0.02, s, _T_EXPERT, e)
+    a = normal((3 * wl.ffn * wl.hidden,), 0.02, s, _T_EXPERT, e)
+    if wl.down_scale != 1.0:
+        a[2 * wl.ffn * wl.hidden:] *= np.float32(wl.down_scale)
+    return a
 
 
 def activations(wl: Workload, step: int, n_tok: int | None = None, layer: int = 0) -> np.ndarray:

@@ -5,6 +5,8 @@ statistics are part of what the benchmark numbers mean: the prefill batch's
 expert skew, the verify batch's token correlation and the sweep's
 layer-to-layer routing correlation.  Routing here is the oracle's (CPU).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -71,3 +73,21 @@ def test_sweep_layers_route_alike_on_the_same_tokens(orc):
     assert len(overlaps) == wl.layers - 1
     assert 0.6 <= float(np.mean(overlaps)) <= 0.8
     assert min(overlaps) > 0.55
+
+
+def test_sweep_down_rows_are_the_draw_times_a_power_of_two():
+    """The sweep's down rows are its N(0, 0.02) draw times 1/32 (a residual
+    update of a few percent of the stream, as in a trained stack); gate and
+    up rows are the draw itself.  A power of two: the scaled rows pack to the
+    same int4 codes, with row scales divided by 32."""
+    wl = synth.WORKLOADS["sweep"]
+    assert wl.down_scale == 1.0 / 32
+    plain = dataclasses.replace(wl, down_scale=1.0)
+    F, H = wl.ffn, wl.hidden
+    for e in (0, 17, wl.n_experts):
+        a = synth.expert_f32_rows(wl, e, 3)
+        b = synth.expert_f32_rows(plain, e, 3)
+        np.testing.assert_array_equal(a[: 2 * F * H], b[: 2 * F * H])
+        np.testing.assert_array_equal(a[2 * F * H:], b[2 * F * H:] / np.float32(32))
+    gate, up, down = synth.expert_f32(wl, 5, 1)
+    np.testing.assert_array_equal(down.ravel(), synth.expert_f32_rows(wl, 5, 1)[2 * F * H:])
