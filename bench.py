@@ -56,8 +56,8 @@ CSRC = os.path.join(ROOT, "int4_routed_expert_f32_gb300", "csrc")
 TRAFFIC = {
     "k_experts": {
         "sources": ["k_experts.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "7ee7199e34dcef1f4292c84062a8444f4d76087093a74086f6b4dbfa774f757b",
-        "bytes_per_launch": 170990848,   # the median of three launches: 170.66 MB read + 0.33 MB written
+        "sha256": "c074085f2c6edf20921080096aa39e35c1d4c78b0e6aec9036e00b4fa596fbc1",
+        "bytes_per_launch": 171017472,   # the median of three launches: 170.97 MB read + 0.05 MB written
         # a decode forward streams 8 routed + 1 shared expert; the capture ran
         # the decode workload itself
         "workloads": ("decode", "profile"),
@@ -65,7 +65,7 @@ TRAFFIC = {
     },
     "k_gemm_gateup": {
         "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "a3fa9b920d0525c9277e3f757eedea6d9121e4b0ef6d94cce555ba5d155ca998",
+        "sha256": "fa67daaae5c57c47e483817e8f3d09f811c6620bcdabdcb5522cc01303ab627a",
         "bytes_per_launch": 5379424000,  # 5284.00 MB read + 95.43 MB written
         "workloads": ("prefill",),
         "capture": "profiles/prefill_layer_launches.md",
@@ -601,8 +601,8 @@ def measure_stream(n_bytes: int, big_bytes: int = 1200 << 20):
                     continue
                 grid.append(timed(nb, chunk, stages, bps))
     best = max(grid, key=lambda r: r["gbs"])
-    default = next(r for r in grid if (r["chunk"], r["stages"], r["blocks_per_sm"]) == (16384, 3, 3))
-    big = [timed(big_bytes, c, s_, b) for c, s_, b in ((16384, 3, 3), (32768, 2, 3), (32768, 3, 2))]
+    default = next(r for r in grid if (r["chunk"], r["stages"], r["blocks_per_sm"]) == (16384, 3, 4))
+    big = [timed(big_bytes, c, s_, b) for c, s_, b in ((16384, 3, 4), (32768, 2, 3), (32768, 3, 2))]
     del buf, flush, sink
     torch.cuda.empty_cache()
     return {"bytes": nb, "peak": hbm_peak, "peak_kind": f"{peak_kind} hbm_gbs", "best": best,

@@ -361,8 +361,8 @@ int coli_moe_dbg_block_dots_w8(const int8_t *w8, int rows, int K, const int8_t *
  * `blocks_per_sm` blocks per SM, each block a contiguous range, and does no
  * arithmetic on the data but a checksum: *sum (a device u64, zeroed by the
  * call) receives the sum of the four 32-bit words at every offset o < bytes
- * with o % 1024 == 0.  0 for chunk, stages or blocks_per_sm takes the expert
- * kernel's arrangement (16384, 3, 3).  Limits: chunk 1024..65536 in steps of
+ * with o % 1024 == 0.  0 for chunk, stages or blocks_per_sm takes the one-token
+ * expert kernel's arrangement (16384, 3, 4).  Limits: chunk 1024..65536 in steps of
  * 1024, stages 2..16, chunk * stages <= 200 KB, blocks_per_sm >= 1 and all
  * blocks resident; buf 16-byte aligned, bytes % 16 == 0, sum 8-byte aligned;
  * otherwise COLI_E_INVAL.  Its duration is the single-pass read time of that

@@ -14,7 +14,7 @@ constexpr unsigned FULL = 0xffffffffu;
 // Device status word bits (read back by coli_moe_get_device_status).
 constexpr int ST_BAD_INDEX = 1;   // an expert index outside [0, E)
 constexpr int ST_TIMEOUT = 2;     // a bounded wait gave up
-constexpr int ST_BAD_SHAPE = 4;   // a kernel met a shape it does not support
+constexpr int ST_BAD_SHAPE = 4;   // a kernel met a shape (or a shared-memory base) it does not support
 
 // Tokens per GEMV tile: one pass over an expert's weights serves up to this
 // many of the tokens routed to it.

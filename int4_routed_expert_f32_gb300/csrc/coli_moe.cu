@@ -1013,7 +1013,7 @@ int coli_moe_dbg_stream_read(const void *buf, size_t bytes, int chunk, int stage
     if (!buf || !sum || !aligned16(buf) || bytes % 16 != 0 || ((uintptr_t)sum & 7) != 0) return COLI_E_INVAL;
     if (chunk == 0) chunk = 16384;
     if (stages == 0) stages = 3;
-    if (blocks_per_sm == 0) blocks_per_sm = 3;
+    if (blocks_per_sm == 0) blocks_per_sm = 4;
     // chunks of 1-64 KB in 1 KB steps, 2-16 stages, at most 200 KB of ring per block
     if (chunk < 1024 || chunk > 65536 || chunk % 1024 != 0 || stages < 2 || stages > 16 ||
         (long)chunk * stages > 200L * 1024 || blocks_per_sm < 1 || blocks_per_sm > 32)

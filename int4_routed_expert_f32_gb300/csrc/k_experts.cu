@@ -46,7 +46,7 @@
 
 namespace coli {
 
-constexpr int NSTAGE_MAX = 16;
+constexpr int NSTAGE_MAX = 6;
 constexpr int STAGE_ROWS = 64;
 constexpr int KC_MAX = 128;
 constexpr int NSUB_MAX = 2;                        // TMA boxes along K per stage
@@ -139,15 +139,19 @@ static size_t act_bytes(int H, int F, int mt)
 
 size_t experts_smem_bytes_mt(int H, int F, int mt, int nstage)
 {
-    return 1024 /*align slack*/ + (size_t)nstage * STAGE_BYTES + act_bytes(H, F, mt) +
+    // no alignment slack: the kernel takes its dynamic shared memory at a
+    // 1024-byte boundary (checked at its start), which lets four one-token
+    // blocks of the decode layer share an SM
+    return (size_t)nstage * STAGE_BYTES + act_bytes(H, F, mt) +
            (size_t)mt * 32 * 4 + sizeof(ExpertSmem);
 }
 
-// Ring depth.  More blocks per SM help more than deeper rings: each block's
-// consumers drain a bounded rate.  Three stages, unless three blocks of that
-// size do not fit in one SM's shared memory (several tokens' activations
-// make the block larger); then two, which keeps three blocks per SM (a
-// 4-token forward ran 26% faster that way).  COLI_MOE_RING_STAGES (2..16)
+// Ring depth.  More blocks per SM help more than deeper rings.  Three stages,
+// unless three blocks of that size do not fit in one SM's shared memory
+// (several tokens' activations make the block larger); then two, which keeps
+// three blocks per SM (a 4-token forward ran 26% faster that way).  The
+// one-token decode layer's 3-stage blocks fit four per SM, which runs every
+// gate/up unit of a forward in the first wave.  COLI_MOE_RING_STAGES (2..6)
 // overrides the choice for tuning.
 static int ring_stages(int H, int F, int mt)
 {
@@ -359,9 +363,15 @@ k_experts(const __grid_constant__ ExpertMaps maps, const ExpertArgs a)
     constexpr int CONSUMERS = Cons<MT>::N;
     constexpr int TP = Cons<MT>::TP;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte alignment for the swizzled TMA boxes, by pointer arithmetic on
-    // the shared array itself so that every access stays a shared-memory access
-    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    // The swizzled TMA boxes need 1024-byte alignment, and the size computed
+    // on the host has no slack for realigning: a block whose dynamic shared
+    // memory starts elsewhere reports ST_BAD_SHAPE and does nothing (every
+    // block of a launch sees the same offset).
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) set_status(a.status, ST_BAD_SHAPE);
+        return;
+    }
+    unsigned char *smem = smem_raw;
     unsigned char *ring = smem;
     const int NBmax = (a.H > a.F ? a.H : a.F) / 32;
     const int nstage = a.nstage;
