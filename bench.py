@@ -65,8 +65,8 @@ TRAFFIC = {
     },
     "k_gemm_gateup": {
         "sources": ["k_gemm.cu", "coli_common.cuh", "tma.cuh", "coli_internal.h"],
-        "sha256": "fa67daaae5c57c47e483817e8f3d09f811c6620bcdabdcb5522cc01303ab627a",
-        "bytes_per_launch": 5379424000,  # 5284.00 MB read + 95.43 MB written
+        "sha256": "37a282ced7fc5c0eb9521ca1ba4e922b36949240e2499bc3a5b3829b9671a378",
+        "bytes_per_launch": 3655883264,  # the median of three launches: 3541.60 MB read + 114.28 MB written
         "workloads": ("prefill",),
         "capture": "profiles/prefill_layer_launches.md",
     },
