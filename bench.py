@@ -860,7 +860,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"])
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "verify", "prefill", "profile",
-                                                          "route_profile", "prefill_profile", "verify_profile", "sweep"])
+                                                          "route_profile", "prefill_profile", "verify_profile", "batch_profile",
+                                                          "sweep"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-forwards", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

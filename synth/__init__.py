@@ -123,6 +123,11 @@ WORKLOADS = {
     # the grouped-GEMM kernels
     "prefill_profile": Workload("prefill_profile", 6144, 2048, 16, 8, 256, 3, norm_jitter=True,
                                 weight_seed=1),
+    # the decode shape with 64 routed experts and 32 tokens under the skewed
+    # router bias (~1.2 GB resident): four tokens per expert on average, so the
+    # 4-token tiles are about as full as those of a 128-token batch over 256
+    # experts; a small case for capturing the expert kernel at that fill
+    "batch_profile": Workload("batch_profile", 6144, 2048, 64, 8, 32, 100, zipf_beta=ZIPF_BETA),
     "sweep": Workload("sweep", 6144, 2048, 256, 8, 128, 100, zipf_beta=ZIPF_BETA, layers=8,
                       layer_corr=SWEEP_LAYER_CORR, down_scale=SWEEP_DOWN_SCALE, batches=(1, 8, 32, 128)),
 }
