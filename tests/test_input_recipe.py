@@ -29,6 +29,22 @@ def test_prefill_batch_has_the_stated_expert_skew(orc, seed):
     assert 30 <= np.median(counts) <= 100
 
 
+def test_batch_profile_fills_four_token_tiles_like_a_128_token_batch(orc):
+    """The batch_profile case (64 experts, 32 tokens, the skewed bias) stands
+    in for a 128-token batch over 256 experts in expert-kernel captures: four
+    routed tokens per expert on average, and 4-token tiles about as full
+    (0.73 at batch 128 over 256 experts)."""
+    wl = synth.WORKLOADS["batch_profile"]
+    W, b = synth.router(wl)
+    x = synth.activations(wl, 0)
+    idx, _ = orc.route(x, W, b, wl.top_k, wl.routed_scale)
+    counts = np.bincount(idx.ravel(), minlength=wl.n_experts)
+    assert counts.sum() == wl.n_tok * wl.top_k == 4 * wl.n_experts
+    tiles = np.ceil(counts / 4).sum()
+    assert 0.68 <= counts.sum() / (4 * tiles) <= 0.80
+    assert (counts > 0).sum() >= 56
+
+
 def test_prefill_tokens_have_norm_jitter():
     """x ~ N(0, 1) * U(0.5, 2) per token: row norms spread over a factor of
     about four around sqrt(H)."""
