@@ -318,12 +318,31 @@ int coli_moe_route_noalloc(const coli_moe_shape *s, const float *x, int n_tok,
  *                             forward completes, and
  *                             coli_moe_get_device_status() then returns
  *                             COLI_E_TIMEOUT
- * 0 <= arg <= 1000000.  Returns COLI_E_INVAL for an unknown kind. */
+ *   COLI_INJECT_GUARD         one byte of workspace guard region `arg`
+ *                             (0 <= arg < the count coli_moe_dbg_check_guards
+ *                             reports) is overwritten from the host, as a
+ *                             stray device write past a buffer's end would
+ *                             overwrite it; synchronises the device
+ * 0 <= arg <= 1000000.  Returns COLI_E_INVAL for an unknown kind or an arg out
+ * of range, COLI_E_NOSHAPE for COLI_INJECT_GUARD before configure. */
 #define COLI_INJECT_NONE 0
 #define COLI_INJECT_ALLOC_FAIL 1
 #define COLI_INJECT_LAUNCH_FAIL 2
 #define COLI_INJECT_WAIT_TIMEOUT 3
+#define COLI_INJECT_GUARD 4
 int coli_moe_dbg_inject(int what, long long arg);
+
+/* ---- workspace guards (bounds checking without a sanitizer) ----------------
+ * coli_moe_configure leaves a guard region between consecutive buffers of its
+ * workspace (from each buffer's last byte at the configured maximum sizes to
+ * the next buffer, at least 256 bytes) and 256 bytes before the first, filled
+ * with the byte 0xA5.  No kernel writes there, so a guard that changed means
+ * a write past a buffer's end.  This call synchronises the device, reads
+ * every guard region back, restores the changed ones, and returns how many
+ * had changed (0: all intact), or a negative coli_status (COLI_E_NOSHAPE
+ * before configure, COLI_E_CUDA).  `n_guards` (optional) receives the number
+ * of guard regions. */
+int coli_moe_dbg_check_guards(int *n_guards);
 
 /* ---- stage entry points (tests; same conventions, configured shape) ------- */
 

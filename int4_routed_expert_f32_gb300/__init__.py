@@ -42,9 +42,9 @@ EXPORTS = (
     "coli_moe_dbg_expert_hidden", "coli_moe_route_noalloc", "coli_moe_dbg_inject",
     "coli_moe_layer_forward_residual_prefetch", "coli_moe_pack_int8", "coli_moe_set_weight_bits",
     "coli_moe_dbg_block_dots_w8", "coli_moe_tier_configure", "coli_moe_tier_forward", "coli_moe_tier_stats",
-    "coli_moe_tier_release", "coli_moe_dbg_stream_read",
+    "coli_moe_tier_release", "coli_moe_dbg_stream_read", "coli_moe_dbg_check_guards",
 )
-INJECT_NONE, INJECT_ALLOC_FAIL, INJECT_LAUNCH_FAIL, INJECT_WAIT_TIMEOUT = 0, 1, 2, 3
+INJECT_NONE, INJECT_ALLOC_FAIL, INJECT_LAUNCH_FAIL, INJECT_WAIT_TIMEOUT, INJECT_GUARD = 0, 1, 2, 3, 4
 
 
 class ColiError(RuntimeError):
@@ -100,6 +100,7 @@ def _load():
         "coli_moe_tier_stats": ([ctypes.POINTER(ctypes.c_longlong)] * 3 + [ctypes.POINTER(ctypes.c_int)], i),
         "coli_moe_tier_release": ([], None),
         "coli_moe_dbg_stream_read": ([P, ctypes.c_size_t, i, i, i, P, P], i),
+        "coli_moe_dbg_check_guards": ([ctypes.POINTER(ctypes.c_int)], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -374,9 +375,20 @@ def route_noalloc(x, router_w, router_bias, hidden, n_experts, top_k, routed_sca
 
 def dbg_inject(what: int, arg: int = 0):
     """Failure injection for tests (see the header): INJECT_ALLOC_FAIL,
-    INJECT_LAUNCH_FAIL, INJECT_WAIT_TIMEOUT (arg in microseconds) or
-    INJECT_NONE to clear."""
+    INJECT_LAUNCH_FAIL, INJECT_WAIT_TIMEOUT (arg in microseconds),
+    INJECT_GUARD (arg: a workspace guard region) or INJECT_NONE to clear."""
     _check(_lib.coli_moe_dbg_inject(int(what), int(arg)), "dbg_inject")
+
+
+def dbg_check_guards():
+    """(changed, total): how many workspace guard regions had changed since
+    configure or the last check (they are restored), and how many there are.
+    Synchronises the device; raises ColiError before configure."""
+    n = ctypes.c_int(0)
+    r = _lib.coli_moe_dbg_check_guards(ctypes.byref(n))
+    if r < 0:
+        raise ColiError(r, "dbg_check_guards")
+    return r, n.value
 
 
 # ---- stage entry points ---------------------------------------------------- #

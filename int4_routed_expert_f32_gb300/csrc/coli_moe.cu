@@ -14,6 +14,7 @@
 //   expert), k_gemm<gate/up> (+ SiLU*up + Q8_0 of h), k_gemm<down>, k_combine.
 #include <cstdio>
 #include <cstring>
+#include <utility>
 #include <vector>
 
 #include "../../include/coli_moe.h"
@@ -51,7 +52,13 @@ struct Workspace {
     uint16_t *qhb = nullptr;         // [R'][F] bf16 codes of h by dispatch position
     int32_t *item_expert = nullptr, *item_pos0 = nullptr, *item_m = nullptr, *n_items = nullptr;
     int rows_alloc = 0;              // R' = max(P + T, 128) rows of xg and qhb
+    // guard regions: from each piece's end to the next piece (at least
+    // WS_GUARD bytes), and WS_GUARD bytes before the first piece, filled with
+    // WS_GUARD_BYTE at configure; a write past a piece's end lands in one
+    std::vector<std::pair<size_t, size_t>> guards;   // (offset, bytes)
 };
+constexpr size_t WS_GUARD = 256;
+constexpr unsigned char WS_GUARD_BYTE = 0xA5;
 
 struct State {
     bool configured = false;
@@ -450,8 +457,8 @@ int coli_moe_configure(const coli_moe_shape *s)
         {(void **)&w.item_m, items * 4},
         {(void **)&w.n_items, 4},
     };
-    size_t total = 0;
-    for (auto &p : pieces) total += align_up(p.bytes, 256);
+    size_t total = WS_GUARD;
+    for (auto &p : pieces) total += align_up(p.bytes, 256) + WS_GUARD;
     void *base = nullptr;
     if (g_inj.alloc_fail > 0) {
         --g_inj.alloc_fail;        // injected: behave as a failed cudaMalloc
@@ -461,14 +468,20 @@ int coli_moe_configure(const coli_moe_shape *s)
         (void)cudaGetLastError();
         return COLI_E_NOMEM;
     }
-    size_t off = 0;
+    size_t off = WS_GUARD;
+    w.guards.emplace_back(0, WS_GUARD);
     for (auto &p : pieces) {
         *p.dst = (char *)base + off;
-        off += align_up(p.bytes, 256);
+        const size_t end = off + align_up(p.bytes, 256) + WS_GUARD;
+        w.guards.emplace_back(off + p.bytes, end - (off + p.bytes));
+        off = end;
     }
     w.base = base;
     w.bytes = total;
-    if (cudaMemset(base, 0, total) != cudaSuccess) {
+    bool filled = cudaMemset(base, 0, total) == cudaSuccess;
+    for (auto &gd : w.guards)
+        filled = filled && cudaMemset((char *)base + gd.first, WS_GUARD_BYTE, gd.second) == cudaSuccess;
+    if (!filled) {
         cudaFree(base);
         return cuda_fail(cudaErrorUnknown);
     }
@@ -508,9 +521,39 @@ int coli_moe_dbg_inject(int what, long long arg)
         if (arg < 0 || arg > 1000000) return COLI_E_INVAL;
         g_inj.wait_us = arg;
         return COLI_OK;
+    case COLI_INJECT_GUARD:
+        // host-side: one byte of guard region `arg` changes, as a stray
+        // device write past a piece's end would change it
+        if (!g.configured) return COLI_E_NOSHAPE;
+        if (arg < 0 || arg >= (long long)g.ws.guards.size()) return COLI_E_INVAL;
+        CUDA_OK(cudaDeviceSynchronize());
+        CUDA_OK(cudaMemset((char *)g.ws.base + g.ws.guards[(size_t)arg].first, 0, 1));
+        return COLI_OK;
     default:
         return COLI_E_INVAL;
     }
+}
+
+int coli_moe_dbg_check_guards(int *n_guards)
+{
+    if (!g.configured) return COLI_E_NOSHAPE;
+    const auto &gs = g.ws.guards;
+    if (n_guards) *n_guards = (int)gs.size();
+    CUDA_OK(cudaDeviceSynchronize());
+    int bad = 0;
+    std::vector<unsigned char> h;
+    for (auto &gd : gs) {
+        h.resize(gd.second);
+        CUDA_OK(cudaMemcpy(h.data(), (char *)g.ws.base + gd.first, gd.second, cudaMemcpyDeviceToHost));
+        bool ok = true;
+        for (unsigned char c : h) ok = ok && (c == WS_GUARD_BYTE);
+        if (!ok) {
+            ++bad;
+            CUDA_OK(cudaMemset((char *)g.ws.base + gd.first, WS_GUARD_BYTE, gd.second));   // re-arm
+        }
+    }
+    CUDA_OK(cudaDeviceSynchronize());
+    return bad;
 }
 
 int coli_moe_set_path(int path, int gemm_min_tokens)

@@ -13,6 +13,24 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: full-size workload (minutes)")
 
 
+@pytest.fixture(autouse=True)
+def _workspace_guards_intact(request):
+    """After every GPU test: no kernel wrote past the end of a buffer of the
+    library's workspace (its guard regions are unchanged).  The bounds check
+    that stands in for a memory sanitizer on every GPU test."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    coli = sys.modules.get("int4_routed_expert_f32_gb300")
+    if coli is None:
+        return
+    try:
+        changed, total = coli.dbg_check_guards()
+    except coli.ColiError:
+        return          # not configured (released, or a failed configure under test)
+    assert changed == 0, f"{changed} of {total} workspace guard regions changed: a write past a buffer's end"
+
+
 @pytest.fixture(scope="session")
 def orc():
     import oracle

@@ -77,6 +77,8 @@ def test_calls_before_configure_report_noshape(lib):
     assert L.coli_moe_dbg_quantize(None, 31, None, None, None) == coli.E_INVAL
     assert L.coli_moe_set_path(7, 0) == coli.E_INVAL
     assert L.coli_moe_strerror(coli.E_NOSHAPE) == b"layer shape not configured"
+    assert L.coli_moe_dbg_check_guards(None) == coli.E_NOSHAPE
+    assert L.coli_moe_dbg_inject(coli.INJECT_GUARD, 0) == coli.E_NOSHAPE
 
 
 def test_injection_kinds_are_checked(lib):

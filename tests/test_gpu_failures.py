@@ -100,3 +100,26 @@ def test_launch_failure_reports_cuda_error(coli, tiny, path, T, nth):
     finally:
         coli.dbg_inject(coli.INJECT_NONE)
         coli.set_path(coli.PATH_AUTO)
+
+
+def test_workspace_guard_change_is_reported(coli, tiny):
+    """The guard regions between the workspace's buffers (the bounds check
+    every GPU test ends with) report a changed byte: guard regions changed from
+    the host, as a stray device write past a buffer would change them, are
+    counted and restored, and the next forward is bit-exact."""
+    wl, L, ref = tiny
+    _configure(coli, wl, 8)
+    x = synth.activations(wl, 71, n_tok=8)
+    np.testing.assert_array_equal(_fwd(coli, L, x), ref.forward(x))
+    changed, total = coli.dbg_check_guards()
+    assert changed == 0 and total >= 30
+    for k in (0, total // 2, total - 1):
+        coli.dbg_inject(coli.INJECT_GUARD, k)
+        assert coli.dbg_check_guards() == (1, total)
+        assert coli.dbg_check_guards() == (0, total)       # restored
+    coli.dbg_inject(coli.INJECT_GUARD, 1)
+    coli.dbg_inject(coli.INJECT_GUARD, 2)
+    assert coli.dbg_check_guards() == (2, total)
+    with pytest.raises(coli.ColiError):
+        coli.dbg_inject(coli.INJECT_GUARD, total)
+    np.testing.assert_array_equal(_fwd(coli, L, x), ref.forward(x))
