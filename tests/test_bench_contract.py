@@ -40,3 +40,37 @@ def test_fewer_than_three_warmup_steps_are_rejected():
     r = _run("--impl", "reference", "--steps", "1", "--warmup", "2", "--workload", "tiny", timeout=120)
     assert r.returncode != 0
     assert "warmup" in r.stderr
+
+
+def _bench_module():
+    import importlib
+    return importlib.import_module("bench")
+
+
+def test_traffic_entries_apply_to_the_sources_in_the_tree():
+    """Every captured DRAM-traffic figure applies to the kernel sources as they
+    are: the bench line carries it for the captured workloads (a stale hash
+    would silently leave the roofline's traffic null), and for no other."""
+    b = _bench_module()
+    for kernel, t in b.TRAFFIC.items():
+        for wl in t["workloads"]:
+            assert b.kernel_traffic(kernel, wl) == t["bytes_per_launch"], kernel
+        assert b.kernel_traffic(kernel, "tiny") is None
+
+
+def test_traffic_is_dropped_once_a_kernel_source_changes(tmp_path, monkeypatch):
+    """A captured figure describes one version of the kernel: after any change
+    to one of its sources the bench line reports traffic as null."""
+    import shutil
+    b = _bench_module()
+    for f in {f for t in b.TRAFFIC.values() for f in t["sources"]}:
+        shutil.copy(os.path.join(b.CSRC, f), tmp_path / f)
+    monkeypatch.setattr(b, "CSRC", str(tmp_path))
+    for kernel, t in b.TRAFFIC.items():
+        wl = t["workloads"][0]
+        assert b.kernel_traffic(kernel, wl) == t["bytes_per_launch"]
+        src = tmp_path / t["sources"][0]
+        original = src.read_bytes()
+        src.write_bytes(original + b"\n// changed\n")
+        assert b.kernel_traffic(kernel, wl) is None
+        src.write_bytes(original)
